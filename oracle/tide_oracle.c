@@ -1,0 +1,213 @@
+/*
+ * CPU oracle for the FSDP2 layout-folded reduce-scatter and all-gather
+ * placement described in "The Endgame of FSDP Communication: Layout-Aware
+ * Collectives on Copy Engines, RDMA, and NVSwitch" (TIDE).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline do.  It shares no code, header or table with the CUDA library.
+ *
+ * Plain, slow and single-threaded on purpose.  Build with
+ *   gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fPIC -shared
+ * so that every float operation below is one IEEE binary32 operation with
+ * round-to-nearest-even (no FMA contraction, no flush-to-zero).
+ *
+ * Notation follows Section 2.1 / Table 2 of the paper, with W for the number
+ * of (virtual) ranks the paper calls N:
+ *   D_p  dim-0 extent of parameter p,   K_p  product of its trailing dims,
+ *   R_p  = ceil(D_p / W) padded rows per rank,
+ *   o_p  = sum_{q<p} R_q K_q  (prefix offset, in elements),
+ *   S    = sum_p R_p K_p      (elements per rank slot).
+ * Rank r owns rows [r R_p, (r+1) R_p) of parameter p; rows past D_p are zero
+ * (Section 2.1, "The backward reduce-scatter boundary").  The number of real
+ * rows rank r holds is therefore v_{p,r} = clamp(D_p - r R_p, 0, R_p).
+ *
+ * Parity pins: every function here is pinned by the CPU tests (brute force on
+ * tiny shapes, torch.chunk / torch._chunk_cat library equivalence, exact
+ * integer sums, a closed-form summation-order probe, fp64 error bounds,
+ * special values and hand-worked fixtures).
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL 1
+#define ORACLE_ENOMEM 2
+
+/* Exact widening of a bf16 bit pattern: bf16 is the top half of binary32. */
+static float bf16_to_f32(uint16_t bits)
+{
+    uint32_t w = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return f;
+}
+
+/* Section 2.1: padded per-rank rows R_p = ceil(D_p / W) and the prefix
+ * offsets o_p of the parameter-major concatenation inside one rank slot. */
+int oracle_geometry(int32_t world, int32_t nparams, const int64_t *dim0, const int64_t *row_numel,
+                    int64_t *rows_per_rank, int64_t *shard_offset, int64_t *slot_numel)
+{
+    if (world < 1 || nparams < 0)
+        return ORACLE_EINVAL;
+    int64_t off = 0;
+    for (int32_t p = 0; p < nparams; ++p) {
+        if (dim0[p] < 0 || row_numel[p] < 0)
+            return ORACLE_EINVAL;
+        int64_t R = (dim0[p] + world - 1) / world;
+        rows_per_rank[p] = R;
+        shard_offset[p] = off;
+        off += R * row_numel[p];
+    }
+    *slot_numel = off;
+    return ORACLE_OK;
+}
+
+/* Real (unpadded) rows of parameter p that rank r holds. */
+int64_t oracle_valid_rows(int64_t dim0, int64_t rows_per_rank, int32_t r)
+{
+    int64_t v = dim0 - (int64_t)r * rows_per_rank;
+    if (v < 0)
+        v = 0;
+    if (v > rows_per_rank)
+        v = rows_per_rank;
+    return v;
+}
+
+/*
+ * Equations (3) and (5) for one window of one destination shard.
+ *
+ * src[u] points at the first real element of the window in source rank u's
+ * gradient; the window holds n_valid real elements followed by n_pad padding
+ * elements (rows past D_p).
+ *
+ * Pass 1 (Eq. 3, FSDP2's pack): each source rank's contribution is sliced,
+ * zero-padded and widened to fp32 into its own buffer.
+ * Pass 2 (Eq. 5): the W buffers are added in rank order 0, 1, ..., W-1,
+ * starting from rank 0's value, in fp32; the sum is scaled by alpha and, in
+ * accumulate mode, added to the existing shard value.
+ *
+ * old may equal out (in-place accumulate).  Returns ORACLE_ENOMEM if the
+ * pack buffer cannot be allocated.
+ */
+int oracle_rs_window(int32_t world, int64_t n_valid, int64_t n_pad, const uint16_t *const *src,
+                     float alpha, int32_t accumulate, const float *old, float *out)
+{
+    int64_t n = n_valid + n_pad;
+    if (world < 1 || n_valid < 0 || n_pad < 0)
+        return ORACLE_EINVAL;
+    if (n == 0)
+        return ORACLE_OK;
+    float *pack = (float *)malloc((size_t)world * (size_t)n * sizeof(float));
+    if (!pack)
+        return ORACLE_ENOMEM;
+
+    /* pass 1: slice, zero-pad, upcast */
+    for (int32_t u = 0; u < world; ++u) {
+        float *dst = pack + (size_t)u * (size_t)n;
+        for (int64_t j = 0; j < n_valid; ++j)
+            dst[j] = bf16_to_f32(src[u][j]);
+        for (int64_t j = n_valid; j < n; ++j)
+            dst[j] = 0.0f;
+    }
+
+    /* pass 2: rank-ordered fp32 reduction, scale, optional accumulate */
+    for (int64_t j = 0; j < n; ++j) {
+        float acc = pack[j];
+        for (int32_t u = 1; u < world; ++u)
+            acc = acc + pack[(size_t)u * (size_t)n + (size_t)j];
+        float y = alpha * acc;
+        out[j] = accumulate ? old[j] + y : y;
+    }
+    free(pack);
+    return ORACLE_OK;
+}
+
+/*
+ * Full reduce-scatter of one parameter group (Eq. 5 for every p and r).
+ *
+ * grads[p * world + u] points at parameter p's full gradient on source rank
+ * u, row-major (D_p, K_p) bf16 bits.  out is W rank slots of `stride`
+ * elements each (stride >= S); rank r's shard of p lands at
+ * out[r * stride + o_p].  Elements of a slot past S are not touched.
+ */
+int oracle_rs(int32_t world, int32_t nparams, const int64_t *dim0, const int64_t *row_numel,
+              const uint16_t *const *grads, float alpha, int32_t accumulate, float *out, int64_t stride)
+{
+    int64_t *R = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nparams > 0 ? nparams : 1));
+    int64_t *o = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nparams > 0 ? nparams : 1));
+    const uint16_t **src = (const uint16_t **)malloc(sizeof(uint16_t *) * (size_t)world);
+    int64_t S = 0;
+    int rc = ORACLE_OK;
+    if (!R || !o || !src) {
+        rc = ORACLE_ENOMEM;
+        goto done;
+    }
+    rc = oracle_geometry(world, nparams, dim0, row_numel, R, o, &S);
+    if (rc != ORACLE_OK)
+        goto done;
+    if (stride < S) {
+        rc = ORACLE_EINVAL;
+        goto done;
+    }
+    for (int32_t p = 0; p < nparams && rc == ORACLE_OK; ++p) {
+        int64_t K = row_numel[p];
+        for (int32_t r = 0; r < world && rc == ORACLE_OK; ++r) {
+            int64_t v = oracle_valid_rows(dim0[p], R[p], r);
+            for (int32_t u = 0; u < world; ++u)
+                src[u] = grads[(size_t)p * (size_t)world + (size_t)u] + (size_t)r * (size_t)R[p] * (size_t)K;
+            float *dst = out + (size_t)r * (size_t)stride + (size_t)o[p];
+            rc = oracle_rs_window(world, v * K, (R[p] - v) * K, src, alpha, accumulate, dst, dst);
+        }
+    }
+done:
+    free(R);
+    free(o);
+    free((void *)src);
+    return rc;
+}
+
+/*
+ * All-gather placement (Section 2.1, Eq. 2): rank r's shard of p sits in the
+ * rank-major input at slot r, offset o_p; its i-th real row becomes row
+ * r R_p + i of the full (D_p, K_p) tensor.  Padding rows are dropped.
+ *
+ * slots is W rank slots of `stride` bf16 elements; full[p] is parameter p's
+ * output tensor.
+ */
+int oracle_ag(int32_t world, int32_t nparams, const int64_t *dim0, const int64_t *row_numel,
+              const uint16_t *slots, int64_t stride, uint16_t *const *full)
+{
+    int64_t *R = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nparams > 0 ? nparams : 1));
+    int64_t *o = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nparams > 0 ? nparams : 1));
+    int64_t S = 0;
+    int rc = ORACLE_OK;
+    if (!R || !o) {
+        rc = ORACLE_ENOMEM;
+        goto done;
+    }
+    rc = oracle_geometry(world, nparams, dim0, row_numel, R, o, &S);
+    if (rc != ORACLE_OK)
+        goto done;
+    if (stride < S) {
+        rc = ORACLE_EINVAL;
+        goto done;
+    }
+    for (int32_t p = 0; p < nparams; ++p) {
+        int64_t K = row_numel[p];
+        for (int32_t r = 0; r < world; ++r) {
+            int64_t v = oracle_valid_rows(dim0[p], R[p], r);
+            for (int64_t i = 0; i < v; ++i) {
+                const uint16_t *from = slots + (size_t)r * (size_t)stride + (size_t)o[p] + (size_t)(i * K);
+                uint16_t *to = full[p] + (size_t)((r * R[p] + i) * K);
+                for (int64_t k = 0; k < K; ++k)
+                    to[k] = from[k];
+            }
+        }
+    }
+done:
+    free(R);
+    free(o);
+    return rc;
+}
