@@ -1,0 +1,78 @@
+// All-gather placement kernel: TIDE paper Section 2.1, Equation (2).  Rank r's
+// shard of parameter p sits in the rank-major input at slot r, offset o_p; its
+// v_{p,r} real rows land at rows [r R_p, r R_p + v_{p,r}) of the full tensor,
+// which is the contiguous element range starting at r R_p K_p.  Padding rows
+// are never read.  A pure HBM copy: one persistent grid walks (piece, chunk)
+// work items and moves 16-byte vectors when source and destination share
+// their alignment phase.
+#include <cuda_runtime.h>
+
+#include "tide_internal.h"
+
+namespace tide {
+namespace {
+
+__device__ __forceinline__ uint4 ld_once_v4(const uint16_t *p)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+constexpr int kAgUnroll = 4;
+
+__global__ void __launch_bounds__(kAgThreads) ag_place_kernel(const __grid_constant__ AgParams ap)
+{
+    constexpr int NT = kAgThreads;
+    const int tid = threadIdx.x;
+    for (int64_t i = ap.item_begin + blockIdx.x; i < ap.item_end; i += gridDim.x) {
+        const Item item = ap.items[i];
+        const Seg seg = ap.segs[item.seg];
+        const int64_t count = int64_t(item.count_kind & ~kItemPad);
+        const uint16_t *src = ap.slots + int64_t(seg.rank) * ap.stride + seg.dst_elem + item.begin;
+        uint16_t *dst = ap.full[seg.param - ap.param_base] + seg.src_elem + item.begin;
+        const uintptr_t sa = reinterpret_cast<uintptr_t>(src), da = reinterpret_cast<uintptr_t>(dst);
+        if (((sa ^ da) & 15u) == 0) {
+            int64_t h = int64_t(((16u - (sa & 15u)) & 15u) >> 1);
+            if (h > count)
+                h = count;
+            const int64_t nv = (count - h) >> 3;
+            const uint16_t *s8 = src + h;
+            uint4 *d8 = reinterpret_cast<uint4 *>(dst + h);
+            for (int64_t v = tid; v < nv; v += int64_t(NT) * kAgUnroll) {
+                uint4 x[kAgUnroll];
+#pragma unroll
+                for (int j = 0; j < kAgUnroll; ++j) {
+                    const int64_t vj = v + int64_t(j) * NT;
+                    if (vj < nv)
+                        x[j] = ld_once_v4(s8 + vj * 8);
+                }
+#pragma unroll
+                for (int j = 0; j < kAgUnroll; ++j) {
+                    const int64_t vj = v + int64_t(j) * NT;
+                    if (vj < nv)
+                        d8[vj] = x[j];
+                }
+            }
+            for (int64_t e = tid; e < h; e += NT)
+                dst[e] = src[e];
+            for (int64_t e = h + nv * 8 + tid; e < count; e += NT)
+                dst[e] = src[e];
+        } else {
+            for (int64_t e = tid; e < count; e += NT)
+                dst[e] = src[e];
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_ag(const AgParams &ap, int grid, cudaStream_t stream)
+{
+    ag_place_kernel<<<grid, kAgThreads, 0, stream>>>(ap);
+    return cudaGetLastError();
+}
+
+}  // namespace tide

@@ -1,0 +1,273 @@
+// Reduce-scatter fold kernels: TIDE paper Section 4, Equation (5), with every
+// one of the W ranks virtual (all gradient sets in this GPU's memory).
+//
+// For every (parameter p, rank r) piece and every element j of it:
+//     acc  = f32(G_p^(0)[r R_p K_p + j])
+//     acc  = acc + f32(G_p^(u)[...])   for u = 1 .. W-1    (fp32, RN, rank order)
+//     y    = alpha * acc
+//     out[r * stride + o_p + j] = accumulate ? out_old + y : y
+// and for padding positions (rows past D_p) the same with zero contributions.
+//
+// The work is HBM-bound (W bf16 reads + one fp32 write, +1 fp32 read when
+// accumulating, per output element; ~0.4 flop/byte), so the kernels are built
+// around bytes in flight: one persistent grid that walks the plan's work list,
+// each CTA streaming the W rank rows of one chunk with 16-byte vector loads
+// straight from the gradients' own storage (no pack buffer), adding in fp32
+// registers and writing the shard with 16-byte streaming stores.
+#include <cuda_runtime.h>
+
+#include "tide_internal.h"
+
+namespace tide {
+namespace {
+
+// 16 bytes of read-once gradient data: non-coherent path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const uint16_t *p)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ld_bf16(const uint16_t *p)
+{
+    unsigned short v;
+    asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return __uint_as_float(uint32_t(v) << 16);
+}
+
+// bf16 -> fp32 is exact: a bf16 is the upper half of a binary32.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4 &x, float (&f)[8])
+{
+    f[0] = bf_lo(x.x); f[1] = bf_hi(x.x);
+    f[2] = bf_lo(x.y); f[3] = bf_hi(x.y);
+    f[4] = bf_lo(x.z); f[5] = bf_hi(x.z);
+    f[6] = bf_lo(x.w); f[7] = bf_hi(x.w);
+}
+
+template <bool ACC>
+__device__ __forceinline__ void store8(float *d, const float (&acc)[8], float alpha, bool vec)
+{
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        y[e] = __fmul_rn(alpha, acc[e]);
+    if (vec) {
+        float4 *d4 = reinterpret_cast<float4 *>(d);
+        if (ACC) {
+            const float4 o0 = __ldcs(d4), o1 = __ldcs(d4 + 1);
+            y[0] = __fadd_rn(o0.x, y[0]); y[1] = __fadd_rn(o0.y, y[1]);
+            y[2] = __fadd_rn(o0.z, y[2]); y[3] = __fadd_rn(o0.w, y[3]);
+            y[4] = __fadd_rn(o1.x, y[4]); y[5] = __fadd_rn(o1.y, y[5]);
+            y[6] = __fadd_rn(o1.z, y[6]); y[7] = __fadd_rn(o1.w, y[7]);
+        }
+        __stcs(d4, make_float4(y[0], y[1], y[2], y[3]));
+        __stcs(d4 + 1, make_float4(y[4], y[5], y[6], y[7]));
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float v = y[e];
+            if (ACC)
+                v = __fadd_rn(d[e], v);
+            __stcs(d + e, v);
+        }
+    }
+}
+
+// One element by scalar loads (misaligned heads, tails and pieces).
+template <int WT, bool ACC>
+__device__ __forceinline__ void fold_scalar(const uint64_t *s_src, int W, int64_t e, float *dst, float alpha)
+{
+    float acc = ld_bf16(reinterpret_cast<const uint16_t *>(s_src[0]) + e);
+#pragma unroll 4
+    for (int u = 1; u < (WT > 0 ? WT : W); ++u)
+        acc = __fadd_rn(acc, ld_bf16(reinterpret_cast<const uint16_t *>(s_src[u]) + e));
+    float y = __fmul_rn(alpha, acc);
+    if (ACC)
+        y = __fadd_rn(dst[e], y);
+    __stcs(dst + e, y);
+}
+
+// Padding rows: W zero contributions sum to +0, then scale / accumulate.
+template <bool ACC>
+__device__ void fold_pad(float *dst, int64_t count, float alpha)
+{
+    const float y = __fmul_rn(alpha, 0.0f);
+    const int64_t mis = int64_t((reinterpret_cast<uintptr_t>(dst) >> 2) & 3u);
+    int64_t head = (4 - mis) & 3;
+    if (head > count)
+        head = count;
+    for (int64_t e = threadIdx.x; e < head; e += blockDim.x)
+        __stcs(dst + e, ACC ? __fadd_rn(dst[e], y) : y);
+    const int64_t nv = (count - head) >> 2;
+    float4 *d4 = reinterpret_cast<float4 *>(dst + head);
+    for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
+        float4 o = make_float4(y, y, y, y);
+        if (ACC) {
+            const float4 p = __ldcs(d4 + v);
+            o = make_float4(__fadd_rn(p.x, y), __fadd_rn(p.y, y), __fadd_rn(p.z, y), __fadd_rn(p.w, y));
+        }
+        __stcs(d4 + v, o);
+    }
+    for (int64_t e = head + nv * 4 + threadIdx.x; e < count; e += blockDim.x)
+        __stcs(dst + e, ACC ? __fadd_rn(dst[e], y) : y);
+}
+
+// WT: compile-time world (0 = runtime).  G: ranks whose loads are issued
+// together before their adds.  VPT: 8-element vectors per thread per pass.
+template <int WT, int G, int VPT, bool ACC>
+__global__ void __launch_bounds__(kFoldThreads) fold_direct_kernel(const FoldParams fp)
+{
+    extern __shared__ uint64_t s_src[];  // this item's W source pointers
+    __shared__ int64_t s_next;
+    const int W = WT > 0 ? WT : fp.world;
+    const int tid = threadIdx.x;
+    constexpr int NT = kFoldThreads;
+    const float alpha = fp.alpha;
+    const bool dynamic = fp.sched == TIDE_SCHED_DYNAMIC;
+
+    int64_t it;
+    if (dynamic) {
+        if (tid == 0)
+            s_next = int64_t(atomicAdd(fp.counters, 1u));
+        __syncthreads();
+        it = s_next;
+    } else {
+        it = blockIdx.x;
+    }
+
+    while (it < fp.n_items) {
+        const Item item = fp.items[it];
+        const Seg seg = fp.segs[item.seg];
+        const int64_t count = int64_t(item.count_kind & ~kItemPad);
+        const bool pad = (item.count_kind & kItemPad) != 0;
+        float *dst = fp.out + int64_t(seg.rank) * fp.stride + seg.dst_elem + (pad ? seg.n_valid : 0) + item.begin;
+
+        if (pad) {
+            fold_pad<ACC>(dst, count, alpha);
+        } else {
+            for (int u = tid; u < W; u += NT)
+                s_src[u] = fp.ptrs[int64_t(seg.param) * W + u] + uint64_t(seg.src_elem + item.begin) * 2u;
+            __syncthreads();
+            if (seg.src_phase >= 0) {
+                // Every rank's row starts at the same phase: after h scalar
+                // elements all W sources are 16-byte aligned.
+                int64_t h = (8 - seg.src_phase) & 7;
+                if (h > count)
+                    h = count;
+                const int64_t nvec = (count - h) >> 3;
+                float *dv = dst + h;
+                const bool dst_vec = (reinterpret_cast<uintptr_t>(dv) & 15u) == 0;
+                for (int64_t v = tid; v < nvec; v += int64_t(NT) * VPT) {
+                    float acc[VPT][8];
+#pragma unroll
+                    for (int u0 = 0; u0 < (WT > 0 ? WT : W); u0 += G) {
+                        uint4 x[G][VPT];
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            if (u0 + g < W) {
+                                const uint16_t *sp = reinterpret_cast<const uint16_t *>(s_src[u0 + g]) + h;
+#pragma unroll
+                                for (int j = 0; j < VPT; ++j) {
+                                    const int64_t vj = v + int64_t(j) * NT;
+                                    x[g][j] = vj < nvec ? ld_stream_v4(sp + vj * 8) : make_uint4(0, 0, 0, 0);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            if (u0 + g < W) {
+#pragma unroll
+                                for (int j = 0; j < VPT; ++j) {
+                                    float f[8];
+                                    unpack8(x[g][j], f);
+                                    if (u0 + g == 0) {
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e)
+                                            acc[j][e] = f[e];
+                                    } else {
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e)
+                                            acc[j][e] = __fadd_rn(acc[j][e], f[e]);
+                                    }
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < VPT; ++j) {
+                        const int64_t vj = v + int64_t(j) * NT;
+                        if (vj < nvec)
+                            store8<ACC>(dv + vj * 8, acc[j], alpha, dst_vec);
+                    }
+                }
+                for (int64_t e = tid; e < h; e += NT)
+                    fold_scalar<WT, ACC>(s_src, W, e, dst, alpha);
+                for (int64_t e = h + nvec * 8 + tid; e < count; e += NT)
+                    fold_scalar<WT, ACC>(s_src, W, e, dst, alpha);
+            } else {
+                for (int64_t e = tid; e < count; e += NT)
+                    fold_scalar<WT, ACC>(s_src, W, e, dst, alpha);
+            }
+        }
+        __syncthreads();  // s_src / s_next are rewritten for the next item
+        if (dynamic) {
+            if (tid == 0)
+                s_next = int64_t(atomicAdd(fp.counters, 1u));
+            __syncthreads();
+            it = s_next;
+        } else {
+            it += gridDim.x;
+        }
+    }
+
+    if (dynamic && tid == 0) {
+        // The last CTA to finish resets the counters for the next launch.
+        __threadfence();
+        const unsigned done = atomicAdd(fp.counters + 1, 1u);
+        if (done == gridDim.x - 1) {
+            atomicExch(fp.counters, 0u);
+            atomicExch(fp.counters + 1, 0u);
+        }
+    }
+}
+
+using FoldKernel = void (*)(const FoldParams);
+
+template <bool ACC>
+FoldKernel pick_direct(int world)
+{
+    switch (world) {
+    case 1: return fold_direct_kernel<1, 1, 4, ACC>;
+    case 2: return fold_direct_kernel<2, 2, 4, ACC>;
+    case 4: return fold_direct_kernel<4, 4, 4, ACC>;
+    case 8: return fold_direct_kernel<8, 8, 2, ACC>;
+    case 16: return fold_direct_kernel<16, 8, 2, ACC>;
+    case 32: return fold_direct_kernel<32, 8, 2, ACC>;
+    default: return fold_direct_kernel<0, 4, 2, ACC>;
+    }
+}
+
+}  // namespace
+
+size_t fold_smem_bytes(int /*kernel*/, int world, int64_t /*chunk_elems*/) { return size_t(world) * sizeof(uint64_t); }
+
+cudaError_t fold_occupancy(int /*kernel*/, int world, int block, size_t smem, int *blocks_per_sm)
+{
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, pick_direct<false>(world), block, smem);
+}
+
+cudaError_t launch_fold(const FoldParams &fp, int /*kernel*/, int accumulate, int grid, int block, size_t smem,
+                        cudaStream_t stream)
+{
+    FoldKernel k = accumulate ? pick_direct<true>(fp.world) : pick_direct<false>(fp.world);
+    k<<<grid, block, smem, stream>>>(fp);
+    return cudaGetLastError();
+}
+
+}  // namespace tide

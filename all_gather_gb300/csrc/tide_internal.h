@@ -1,0 +1,112 @@
+// Internal definitions shared by the host plan code and the CUDA kernels of
+// libtide.  Not part of the C ABI (see include/tide.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <string>
+#include <vector>
+
+#include "../../include/tide.h"
+
+namespace tide {
+
+constexpr int kMaxWorld = 1024;
+constexpr int kFoldThreads = 256;            // threads per fold CTA (direct kernel)
+constexpr int kAgThreads = 256;              // threads per placement CTA
+constexpr int kAgParamsPerLaunch = 1024;     // full[] pointers passed by value per placement launch
+constexpr int64_t kDefaultChunkBytes = 16384;  // bf16 bytes per rank per fold work item
+constexpr int64_t kAgChunkElems = 16384;     // bf16 elements per placement work item
+
+// One (parameter, rank) shard piece.  Element offsets; the output address is
+// out_base + rank * stride + dst_elem, the source address of rank u is
+// ptrs[param * W + u] + src_elem.
+struct Seg {
+    int64_t src_elem;
+    int64_t dst_elem;
+    int64_t n_valid;
+    int64_t n_pad;
+    int32_t param;
+    int32_t rank;
+    int32_t src_phase;  // (address / 2) mod 8 of every rank's first element, -1 if ranks differ
+    int32_t pad_;
+};
+static_assert(sizeof(Seg) == 48, "Seg layout");
+
+// One work item: `count` elements starting `begin` elements into the piece's
+// real data (kind 0) or into its padding (kind 1).
+struct Item {
+    int32_t seg;
+    uint32_t count_kind;  // bit 31: padding item; bits 0..30: count
+    int64_t begin;
+};
+static_assert(sizeof(Item) == 16, "Item layout");
+constexpr uint32_t kItemPad = 0x80000000u;
+
+struct FoldParams {
+    const uint64_t *ptrs;  // [P * W] gradient base pointers
+    const Seg *segs;
+    const Item *items;
+    int64_t n_items;
+    float *out;
+    int64_t stride;
+    float alpha;
+    int32_t world;
+    int32_t sched;
+    uint32_t *counters;    // [2] dynamic-schedule ticket and done counters
+    int32_t *status;       // device status word
+    uint32_t debug;
+};
+
+struct AgParams {
+    const Seg *segs;
+    const Item *items;
+    int64_t item_begin, item_end;  // this launch's item range
+    const uint16_t *slots;
+    int64_t stride;
+    int32_t param_base;            // full[0] is parameter param_base
+    int32_t n_full;
+    uint16_t *full[kAgParamsPerLaunch];
+};
+
+// Launchers (rs_fold.cu / ag_place.cu).  Return cudaGetLastError() of the launch.
+cudaError_t launch_fold(const FoldParams &fp, int kernel, int accumulate, int grid, int block, size_t smem,
+                        cudaStream_t stream);
+cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *blocks_per_sm);
+size_t fold_smem_bytes(int kernel, int world, int64_t chunk_elems);
+cudaError_t launch_ag(const AgParams &ap, int grid, cudaStream_t stream);
+
+extern std::atomic<uint64_t> g_launches;
+
+}  // namespace tide
+
+struct tide_plan {
+    int32_t world = 0;
+    int32_t nparams = 0;
+    int64_t slot_numel = 0;
+    std::vector<int64_t> dim0, row_numel, rows, offset;
+    std::vector<uint64_t> ptrs;          // [P * W]
+    std::vector<tide::Seg> segs;         // [P * W], param-major
+    std::vector<tide::Item> rs_items;
+    std::vector<tide::Item> ag_items;    // real data only, ordered by parameter
+    std::vector<int64_t> ag_param_item_begin;  // [P + 1]
+    tide_plan_flags_t flags{};
+    int64_t chunk_elems = 0;
+    int32_t grid = 0, block = 0, sms = 0;
+    size_t fold_smem = 0;
+    int kernel = TIDE_KERNEL_DIRECT;
+    bool host_only = false;
+    int device = -1;
+    uintptr_t src_lo = 0, src_hi = 0;    // hull of all gradient ranges
+    // device side
+    void *d_block = nullptr;
+    uint64_t *d_ptrs = nullptr;
+    tide::Seg *d_segs = nullptr;
+    tide::Item *d_rs_items = nullptr;
+    tide::Item *d_ag_items = nullptr;
+    uint32_t *d_counters = nullptr;
+    int32_t *d_status = nullptr;
+    cudaEvent_t last_use = nullptr;
+};

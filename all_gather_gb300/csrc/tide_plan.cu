@@ -1,0 +1,669 @@
+// Host side of libtide: plan geometry (TIDE paper, Section 2.1), validation,
+// device tables, and the C-ABI entry points declared in include/tide.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "tide_internal.h"
+
+namespace tide {
+std::atomic<uint64_t> g_launches{0};
+}
+
+namespace {
+
+thread_local std::string t_last_error;
+
+tide_status_t fail(tide_status_t st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+tide_status_t fail(tide_status_t st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
+tide_status_t cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(TIDE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int64_t kMaxElems = int64_t(1) << 60;
+
+bool mul_ok(int64_t a, int64_t b, int64_t *out)
+{
+    if (a < 0 || b < 0)
+        return false;
+    if (a != 0 && b > kMaxElems / a)
+        return false;
+    *out = a * b;
+    return true;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Source phase of a piece: (address / 2) mod 8 of rank u's first element when
+// every rank agrees, else -1 (the fold then uses scalar loads for it).
+int32_t piece_phase(const uint64_t *ptrs_p, int32_t W, int64_t src_elem)
+{
+    int32_t ph = -1;
+    for (int32_t u = 0; u < W; ++u) {
+        int32_t x = int32_t(((ptrs_p[u] >> 1) + uint64_t(src_elem)) & 7u);
+        if (u == 0)
+            ph = x;
+        else if (x != ph)
+            return -1;
+    }
+    return ph;
+}
+
+tide_status_t check_flags(const tide_plan_flags_t &f)
+{
+    for (int i = 0; i < 5; ++i)
+        if (f.reserved[i] != 0)
+            return fail(TIDE_ERR_INVALID_ARG, "flags.reserved[%d] must be zero", i);
+    if (f.cta_budget < 0)
+        return fail(TIDE_ERR_INVALID_ARG, "flags.cta_budget %d < 0", f.cta_budget);
+    if (f.chunk_bytes != 0 && (f.chunk_bytes < 256 || f.chunk_bytes % 256 != 0 || f.chunk_bytes > (1 << 26)))
+        return fail(TIDE_ERR_INVALID_ARG, "flags.chunk_bytes %d: need 0 or a multiple of 256 in [256, 2^26]",
+                    f.chunk_bytes);
+    if (f.order != TIDE_ORDER_RANK_ASC)
+        return fail(TIDE_ERR_UNSUPPORTED, "flags.order %d is not implemented", f.order);
+    if (f.sched != TIDE_SCHED_STATIC && f.sched != TIDE_SCHED_DYNAMIC)
+        return fail(TIDE_ERR_INVALID_ARG, "flags.sched %d", f.sched);
+    if (f.kernel != TIDE_KERNEL_AUTO && f.kernel != TIDE_KERNEL_DIRECT && f.kernel != TIDE_KERNEL_BULK)
+        return fail(TIDE_ERR_INVALID_ARG, "flags.kernel %d", f.kernel);
+    if (f.grad_dtype != TIDE_DTYPE_BF16)
+        return fail(TIDE_ERR_UNSUPPORTED, "flags.grad_dtype %d is not implemented", f.grad_dtype);
+    if (f.debug & ~TIDE_DEBUG_HOST_ONLY)
+        return fail(TIDE_ERR_INVALID_ARG, "unknown debug bits 0x%x", f.debug);
+    return TIDE_OK;
+}
+
+// Copy and check the gradient pointers of every parameter into plan->ptrs and
+// recompute each piece's source phase and the address hull.
+tide_status_t load_pointers(tide_plan_t *plan, const tide_param_desc_t *params)
+{
+    const int32_t W = plan->world;
+    uintptr_t lo = UINTPTR_MAX, hi = 0;
+    for (int32_t p = 0; p < plan->nparams; ++p) {
+        const int64_t numel = plan->dim0[p] * plan->row_numel[p];
+        if (params[p].rank_base == nullptr)
+            return fail(TIDE_ERR_INVALID_ARG, "params[%d].rank_base is NULL", p);
+        for (int32_t u = 0; u < W; ++u) {
+            uintptr_t a = reinterpret_cast<uintptr_t>(params[p].rank_base[u]);
+            if (numel > 0 && a == 0)
+                return fail(TIDE_ERR_INVALID_ARG, "params[%d].rank_base[%d] is NULL", p, u);
+            if (a & 1u)
+                return fail(TIDE_ERR_ALIGNMENT, "params[%d].rank_base[%d] is not 2-byte aligned", p, u);
+            plan->ptrs[size_t(p) * W + u] = a;
+            if (numel > 0) {
+                lo = std::min(lo, a);
+                hi = std::max(hi, a + uintptr_t(numel) * 2u);
+            }
+        }
+    }
+    plan->src_lo = lo;
+    plan->src_hi = hi;
+    for (auto &s : plan->segs)
+        s.src_phase = piece_phase(&plan->ptrs[size_t(s.param) * W], W, s.src_elem);
+    return TIDE_OK;
+}
+
+bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+// Does [lo, hi) overlap any gradient tensor of the plan?
+bool overlaps_gradients(const tide_plan_t *plan, uintptr_t lo, uintptr_t hi)
+{
+    if (lo >= hi || !ranges_overlap(lo, hi, plan->src_lo, plan->src_hi))
+        return false;
+    for (int32_t p = 0; p < plan->nparams; ++p) {
+        const uintptr_t bytes = uintptr_t(plan->dim0[p] * plan->row_numel[p]) * 2u;
+        for (int32_t u = 0; u < plan->world; ++u) {
+            uintptr_t a = plan->ptrs[size_t(p) * plan->world + u];
+            if (bytes && ranges_overlap(lo, hi, a, a + bytes))
+                return true;
+        }
+    }
+    return false;
+}
+
+tide_status_t upload_tables(tide_plan_t *plan, cudaStream_t stream, bool pointers_only)
+{
+    cudaError_t e;
+    if (!pointers_only) {
+        e = cudaMemcpyAsync(plan->d_rs_items, plan->rs_items.data(), plan->rs_items.size() * sizeof(tide::Item),
+                            cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "upload work items");
+        e = cudaMemcpyAsync(plan->d_ag_items, plan->ag_items.data(), plan->ag_items.size() * sizeof(tide::Item),
+                            cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "upload placement items");
+    }
+    e = cudaMemcpyAsync(plan->d_ptrs, plan->ptrs.data(), plan->ptrs.size() * sizeof(uint64_t),
+                        cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "upload pointer table");
+    e = cudaMemcpyAsync(plan->d_segs, plan->segs.data(), plan->segs.size() * sizeof(tide::Seg),
+                        cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "upload segment table");
+    e = cudaEventRecord(plan->last_use, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "record plan event");
+    return TIDE_OK;
+}
+
+void free_device(tide_plan_t *plan)
+{
+    if (plan->last_use) {
+        cudaEventSynchronize(plan->last_use);
+        cudaEventDestroy(plan->last_use);
+        plan->last_use = nullptr;
+    }
+    if (plan->d_block) {
+        cudaFree(plan->d_block);
+        plan->d_block = nullptr;
+    }
+}
+
+tide_status_t check_device(const tide_plan_t *plan)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev != plan->device)
+        return fail(TIDE_ERR_INVALID_ARG, "plan was built on device %d but device %d is current", plan->device, dev);
+    return TIDE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *tide_status_string(tide_status_t s)
+{
+    switch (s) {
+    case TIDE_OK: return "TIDE_OK";
+    case TIDE_ERR_INVALID_ARG: return "TIDE_ERR_INVALID_ARG";
+    case TIDE_ERR_ALIGNMENT: return "TIDE_ERR_ALIGNMENT";
+    case TIDE_ERR_UNSUPPORTED: return "TIDE_ERR_UNSUPPORTED";
+    case TIDE_ERR_OOM: return "TIDE_ERR_OOM";
+    case TIDE_ERR_CUDA: return "TIDE_ERR_CUDA";
+    case TIDE_ERR_TIMEOUT: return "TIDE_ERR_TIMEOUT";
+    }
+    return "TIDE_ERR_UNKNOWN";
+}
+
+const char *tide_last_error(void) { return t_last_error.c_str(); }
+
+uint64_t tide_launch_count(void) { return tide::g_launches.load(); }
+
+tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_param_desc_t *params,
+                              const tide_plan_flags_t *flags, void *stream_, tide_plan_t **plan_out)
+{
+    t_last_error.clear();
+    if (!plan_out)
+        return fail(TIDE_ERR_INVALID_ARG, "plan_out is NULL");
+    *plan_out = nullptr;
+    if (world < 1 || world > tide::kMaxWorld)
+        return fail(TIDE_ERR_INVALID_ARG, "world %d outside [1, %d]", world, tide::kMaxWorld);
+    if (num_params < 0)
+        return fail(TIDE_ERR_INVALID_ARG, "num_params %d < 0", num_params);
+    if (num_params > 0 && !params)
+        return fail(TIDE_ERR_INVALID_ARG, "params is NULL");
+    tide_plan_flags_t f{};
+    if (flags)
+        f = *flags;
+    tide_status_t st = check_flags(f);
+    if (st != TIDE_OK)
+        return st;
+
+    auto *plan = new (std::nothrow) tide_plan_t();
+    if (!plan)
+        return fail(TIDE_ERR_OOM, "host allocation of the plan failed");
+    auto bail = [&](tide_status_t s) {
+        free_device(plan);
+        delete plan;
+        return s;
+    };
+    plan->world = world;
+    plan->nparams = num_params;
+    plan->flags = f;
+    plan->host_only = (f.debug & TIDE_DEBUG_HOST_ONLY) != 0;
+    plan->chunk_elems = (f.chunk_bytes ? f.chunk_bytes : tide::kDefaultChunkBytes) / 2;
+    plan->kernel = f.kernel == TIDE_KERNEL_AUTO ? TIDE_KERNEL_DIRECT : f.kernel;
+    if (plan->kernel == TIDE_KERNEL_BULK)
+        return bail(fail(TIDE_ERR_UNSUPPORTED, "the bulk-copy kernel is not available in this build"));
+
+    // --- geometry (Section 2.1): R_p = ceil(D_p / W), o_p, S -------------
+    plan->dim0.resize(num_params);
+    plan->row_numel.resize(num_params);
+    plan->rows.resize(num_params);
+    plan->offset.resize(num_params);
+    int64_t running = 0, S = 0;
+    for (int32_t p = 0; p < num_params; ++p) {
+        const int64_t D = params[p].dim0, K = params[p].row_numel;
+        int64_t numel, piece, span;
+        if (D < 0 || K < 0)
+            return bail(fail(TIDE_ERR_INVALID_ARG, "params[%d]: dim0 %lld, row_numel %lld", p, (long long)D,
+                             (long long)K));
+        const int64_t R = (D + world - 1) / world;
+        if (!mul_ok(D, K, &numel) || !mul_ok(R, K, &piece) || !mul_ok(piece, world, &span))
+            return bail(fail(TIDE_ERR_INVALID_ARG, "params[%d]: size overflows", p));
+        int64_t o = params[p].shard_offset;
+        if (o < -1)
+            return bail(fail(TIDE_ERR_INVALID_ARG, "params[%d].shard_offset %lld", p, (long long)o));
+        if (o == -1)
+            o = running;
+        if (o > kMaxElems - piece)
+            return bail(fail(TIDE_ERR_INVALID_ARG, "params[%d]: offset overflows", p));
+        plan->dim0[p] = D;
+        plan->row_numel[p] = K;
+        plan->rows[p] = R;
+        plan->offset[p] = o;
+        running = o + piece;
+        S = std::max(S, running);
+    }
+    {   // explicit offsets must not make shards overlap
+        std::vector<std::pair<int64_t, int64_t>> iv;
+        for (int32_t p = 0; p < num_params; ++p)
+            if (plan->rows[p] * plan->row_numel[p] > 0)
+                iv.emplace_back(plan->offset[p], plan->offset[p] + plan->rows[p] * plan->row_numel[p]);
+        std::sort(iv.begin(), iv.end());
+        for (size_t i = 1; i < iv.size(); ++i)
+            if (iv[i].first < iv[i - 1].second)
+                return bail(fail(TIDE_ERR_INVALID_ARG, "shard offsets make two parameters overlap in the slot"));
+    }
+    plan->slot_numel = S;
+    int64_t total;
+    if (!mul_ok(S, world, &total))
+        return bail(fail(TIDE_ERR_INVALID_ARG, "W * S overflows"));
+
+    // --- pieces: rank r owns rows [r R_p, (r+1) R_p), v = clamp(D - r R, 0, R)
+    plan->segs.reserve(size_t(num_params) * world);
+    for (int32_t p = 0; p < num_params; ++p) {
+        const int64_t D = plan->dim0[p], K = plan->row_numel[p], R = plan->rows[p];
+        for (int32_t r = 0; r < world; ++r) {
+            int64_t v = std::min(std::max(D - int64_t(r) * R, int64_t(0)), R);
+            tide::Seg s{};
+            s.src_elem = int64_t(r) * R * K;
+            s.dst_elem = plan->offset[p];
+            s.n_valid = v * K;
+            s.n_pad = (R - v) * K;
+            s.param = p;
+            s.rank = r;
+            s.src_phase = -1;
+            plan->segs.push_back(s);
+        }
+    }
+    plan->ptrs.assign(size_t(num_params) * world, 0);
+    st = load_pointers(plan, params);
+    if (st != TIDE_OK)
+        return bail(st);
+
+    // --- work lists --------------------------------------------------------
+    const int64_t CH = plan->chunk_elems;
+    for (size_t i = 0; i < plan->segs.size(); ++i) {
+        const tide::Seg &s = plan->segs[i];
+        for (int64_t b = 0; b < s.n_valid; b += CH)
+            plan->rs_items.push_back({int32_t(i), uint32_t(std::min(CH, s.n_valid - b)), b});
+        for (int64_t b = 0; b < s.n_pad; b += CH)
+            plan->rs_items.push_back({int32_t(i), uint32_t(std::min(CH, s.n_pad - b)) | tide::kItemPad, b});
+    }
+    plan->ag_param_item_begin.assign(size_t(num_params) + 1, 0);
+    for (size_t i = 0; i < plan->segs.size(); ++i) {
+        const tide::Seg &s = plan->segs[i];
+        if (s.rank == 0)
+            plan->ag_param_item_begin[s.param] = int64_t(plan->ag_items.size());
+        for (int64_t b = 0; b < s.n_valid; b += tide::kAgChunkElems)
+            plan->ag_items.push_back({int32_t(i), uint32_t(std::min(tide::kAgChunkElems, s.n_valid - b)), b});
+    }
+    plan->ag_param_item_begin[num_params] = int64_t(plan->ag_items.size());
+    if (plan->segs.size() > size_t(INT32_MAX) || plan->rs_items.size() > size_t(INT32_MAX))
+        return bail(fail(TIDE_ERR_UNSUPPORTED, "too many work items; raise chunk_bytes"));
+
+    plan->block = tide::kFoldThreads;
+    plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, CH);
+    if (plan->host_only) {
+        plan->grid = f.cta_budget ? f.cta_budget : 0;
+        *plan_out = plan;
+        return TIDE_OK;
+    }
+
+    // --- device tables -----------------------------------------------------
+    cudaError_t e = cudaGetDevice(&plan->device);
+    if (e != cudaSuccess)
+        return bail(cuda_fail(e, "cudaGetDevice"));
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, plan->device);
+    if (e != cudaSuccess)
+        return bail(cuda_fail(e, "query SM count"));
+    int per_sm = 0;
+    e = tide::fold_occupancy(plan->kernel, world, plan->block, plan->fold_smem, &per_sm);
+    if (e != cudaSuccess)
+        return bail(cuda_fail(e, "fold occupancy"));
+    if (per_sm < 1)
+        return bail(fail(TIDE_ERR_UNSUPPORTED, "fold kernel does not fit on an SM (world %d)", world));
+    plan->grid = f.cta_budget ? f.cta_budget : sms * per_sm;
+    plan->sms = sms;
+
+    size_t off = 0;
+    auto carve = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + std::max<size_t>(bytes, 1), 256);
+        return at;
+    };
+    const size_t o_ptrs = carve(plan->ptrs.size() * sizeof(uint64_t));
+    const size_t o_segs = carve(plan->segs.size() * sizeof(tide::Seg));
+    const size_t o_rs = carve(plan->rs_items.size() * sizeof(tide::Item));
+    const size_t o_ag = carve(plan->ag_items.size() * sizeof(tide::Item));
+    const size_t o_cnt = carve(2 * sizeof(uint32_t));
+    const size_t o_st = carve(sizeof(int32_t));
+    e = cudaMalloc(&plan->d_block, off);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return bail(fail(TIDE_ERR_OOM, "cudaMalloc of %zu table bytes: %s", off, cudaGetErrorString(e)));
+    }
+    char *base = static_cast<char *>(plan->d_block);
+    plan->d_ptrs = reinterpret_cast<uint64_t *>(base + o_ptrs);
+    plan->d_segs = reinterpret_cast<tide::Seg *>(base + o_segs);
+    plan->d_rs_items = reinterpret_cast<tide::Item *>(base + o_rs);
+    plan->d_ag_items = reinterpret_cast<tide::Item *>(base + o_ag);
+    plan->d_counters = reinterpret_cast<uint32_t *>(base + o_cnt);
+    plan->d_status = reinterpret_cast<int32_t *>(base + o_st);
+    e = cudaEventCreateWithFlags(&plan->last_use, cudaEventDisableTiming);
+    if (e != cudaSuccess)
+        return bail(cuda_fail(e, "create plan event"));
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    e = cudaMemsetAsync(base + o_cnt, 0, o_st + sizeof(int32_t) - o_cnt, stream);
+    if (e != cudaSuccess)
+        return bail(cuda_fail(e, "clear counters"));
+    st = upload_tables(plan, stream, false);
+    if (st != TIDE_OK)
+        return bail(st);
+    *plan_out = plan;
+    return TIDE_OK;
+}
+
+tide_status_t tide_plan_rebind(tide_plan_t *plan, const tide_param_desc_t *params, void *stream)
+{
+    t_last_error.clear();
+    if (!plan)
+        return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+    if (plan->nparams > 0 && !params)
+        return fail(TIDE_ERR_INVALID_ARG, "params is NULL");
+    for (int32_t p = 0; p < plan->nparams; ++p) {
+        const int64_t o = params[p].shard_offset;
+        if (params[p].dim0 != plan->dim0[p] || params[p].row_numel != plan->row_numel[p] ||
+            (o != -1 && o != plan->offset[p]))
+            return fail(TIDE_ERR_INVALID_ARG, "params[%d] geometry differs from the plan's", p);
+    }
+    std::vector<uint64_t> keep_ptrs = plan->ptrs;
+    std::vector<tide::Seg> keep_segs = plan->segs;
+    uintptr_t keep_lo = plan->src_lo, keep_hi = plan->src_hi;
+    tide_status_t st = load_pointers(plan, params);
+    if (st != TIDE_OK) {
+        plan->ptrs.swap(keep_ptrs);
+        plan->segs.swap(keep_segs);
+        plan->src_lo = keep_lo;
+        plan->src_hi = keep_hi;
+        return st;
+    }
+    if (plan->host_only)
+        return TIDE_OK;
+    st = check_device(plan);
+    if (st != TIDE_OK)
+        return st;
+    return upload_tables(plan, static_cast<cudaStream_t>(stream), true);
+}
+
+tide_status_t tide_rs_fold(tide_plan_t *plan, float *out_base, int64_t out_slot_stride, float alpha,
+                           int32_t accumulate, void *stream_)
+{
+    t_last_error.clear();
+    if (!plan)
+        return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+    if (plan->host_only)
+        return fail(TIDE_ERR_INVALID_ARG, "plan was built host-only and cannot be launched");
+    if (accumulate != 0 && accumulate != 1)
+        return fail(TIDE_ERR_INVALID_ARG, "accumulate must be 0 or 1");
+    if (out_slot_stride < plan->slot_numel)
+        return fail(TIDE_ERR_INVALID_ARG, "out_slot_stride %lld < S %lld", (long long)out_slot_stride,
+                    (long long)plan->slot_numel);
+    if (plan->rs_items.empty())
+        return TIDE_OK;
+    if (!out_base)
+        return fail(TIDE_ERR_INVALID_ARG, "out_base is NULL");
+    if (reinterpret_cast<uintptr_t>(out_base) & 3u)
+        return fail(TIDE_ERR_ALIGNMENT, "out_base is not 4-byte aligned");
+    int64_t span;
+    if (!mul_ok(out_slot_stride, plan->world - 1, &span) || span > kMaxElems - plan->slot_numel)
+        return fail(TIDE_ERR_INVALID_ARG, "output extent overflows");
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(out_base);
+    const uintptr_t hi = lo + uintptr_t(span + plan->slot_numel) * 4u;
+    if (overlaps_gradients(plan, lo, hi))
+        return fail(TIDE_ERR_INVALID_ARG, "the output overlaps a gradient tensor");
+    tide_status_t st = check_device(plan);
+    if (st != TIDE_OK)
+        return st;
+
+    tide::FoldParams fp{};
+    fp.ptrs = plan->d_ptrs;
+    fp.segs = plan->d_segs;
+    fp.items = plan->d_rs_items;
+    fp.n_items = int64_t(plan->rs_items.size());
+    fp.out = out_base;
+    fp.stride = out_slot_stride;
+    fp.alpha = alpha;
+    fp.world = plan->world;
+    fp.sched = plan->flags.sched;
+    fp.counters = plan->d_counters;
+    fp.status = plan->d_status;
+    fp.debug = plan->flags.debug;
+    const int grid = int(std::min<int64_t>(plan->grid, fp.n_items));
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    cudaError_t e = tide::launch_fold(fp, plan->kernel, accumulate, grid, plan->block, plan->fold_smem, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "fold launch");
+    tide::g_launches.fetch_add(1);
+    e = cudaEventRecord(plan->last_use, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "record plan event");
+    return TIDE_OK;
+}
+
+tide_status_t tide_ag_place(tide_plan_t *plan, const void *slots_base, int64_t slot_stride, void *const *full,
+                            int32_t mode, void *stream_)
+{
+    t_last_error.clear();
+    if (!plan)
+        return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+    if (plan->host_only)
+        return fail(TIDE_ERR_INVALID_ARG, "plan was built host-only and cannot be launched");
+    if (mode != TIDE_AG_SM && mode != TIDE_AG_CE_2D && mode != TIDE_AG_CE_1D)
+        return fail(TIDE_ERR_INVALID_ARG, "unknown placement mode %d", mode);
+    if (slot_stride < plan->slot_numel)
+        return fail(TIDE_ERR_INVALID_ARG, "slot_stride %lld < S %lld", (long long)slot_stride,
+                    (long long)plan->slot_numel);
+    if (plan->ag_items.empty())
+        return TIDE_OK;
+    if (!slots_base || !full)
+        return fail(TIDE_ERR_INVALID_ARG, "slots_base or full is NULL");
+    if (reinterpret_cast<uintptr_t>(slots_base) & 1u)
+        return fail(TIDE_ERR_ALIGNMENT, "slots_base is not 2-byte aligned");
+    int64_t span;
+    if (!mul_ok(slot_stride, plan->world - 1, &span) || span > kMaxElems - plan->slot_numel)
+        return fail(TIDE_ERR_INVALID_ARG, "slot extent overflows");
+    const uintptr_t s_lo = reinterpret_cast<uintptr_t>(slots_base);
+    const uintptr_t s_hi = s_lo + uintptr_t(span + plan->slot_numel) * 2u;
+    std::vector<std::pair<uintptr_t, uintptr_t>> iv;
+    iv.reserve(plan->nparams);
+    for (int32_t p = 0; p < plan->nparams; ++p) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(full[p]);
+        const uintptr_t bytes = uintptr_t(plan->dim0[p] * plan->row_numel[p]) * 2u;
+        if (bytes == 0)
+            continue;
+        if (a == 0)
+            return fail(TIDE_ERR_INVALID_ARG, "full[%d] is NULL", p);
+        if (a & 1u)
+            return fail(TIDE_ERR_ALIGNMENT, "full[%d] is not 2-byte aligned", p);
+        if (ranges_overlap(a, a + bytes, s_lo, s_hi))
+            return fail(TIDE_ERR_INVALID_ARG, "full[%d] overlaps the shard slots", p);
+        iv.emplace_back(a, a + bytes);
+    }
+    std::sort(iv.begin(), iv.end());
+    for (size_t i = 1; i < iv.size(); ++i)
+        if (iv[i].first < iv[i - 1].second)
+            return fail(TIDE_ERR_INVALID_ARG, "two full[] tensors overlap");
+    tide_status_t st = check_device(plan);
+    if (st != TIDE_OK)
+        return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const auto *slots = static_cast<const uint16_t *>(slots_base);
+    cudaError_t e = cudaSuccess;
+
+    if (mode == TIDE_AG_SM) {
+        static thread_local tide::AgParams ap;  // ~8 KB: keep it off the stack
+        for (int32_t p0 = 0; p0 < plan->nparams; p0 += tide::kAgParamsPerLaunch) {
+            const int32_t p1 = std::min(plan->nparams, p0 + tide::kAgParamsPerLaunch);
+            ap.segs = plan->d_segs;
+            ap.items = plan->d_ag_items;
+            ap.item_begin = plan->ag_param_item_begin[p0];
+            ap.item_end = plan->ag_param_item_begin[p1];
+            if (ap.item_end == ap.item_begin)
+                continue;
+            ap.slots = slots;
+            ap.stride = slot_stride;
+            ap.param_base = p0;
+            ap.n_full = p1 - p0;
+            for (int32_t p = p0; p < p1; ++p)
+                ap.full[p - p0] = static_cast<uint16_t *>(full[p]);
+            const int64_t n = ap.item_end - ap.item_begin;
+            const int grid = int(std::min<int64_t>(n, int64_t(plan->sms) * 8));
+            e = tide::launch_ag(ap, grid, stream);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "placement launch");
+            tide::g_launches.fetch_add(1);
+        }
+    } else {
+        // Copy engines.  Rank r's piece of p: slot r at o_p -> full_p rows [r R, r R + v).
+        for (int32_t p = 0; p < plan->nparams; ++p) {
+            const int64_t D = plan->dim0[p], K = plan->row_numel[p], R = plan->rows[p];
+            if (D * K == 0)
+                continue;
+            char *dst = static_cast<char *>(full[p]);
+            const char *src = reinterpret_cast<const char *>(slots + plan->offset[p]);
+            const size_t piece = size_t(R * K) * 2u;
+            const int64_t nfull = D / R;  // ranks holding R real rows
+            if (mode == TIDE_AG_CE_2D && nfull > 0) {
+                e = cudaMemcpy2DAsync(dst, piece, src, size_t(slot_stride) * 2u, piece, size_t(nfull),
+                                      cudaMemcpyDeviceToDevice, stream);
+                if (e != cudaSuccess)
+                    return cuda_fail(e, "2D placement copy");
+            } else {
+                for (int64_t r = 0; r < nfull; ++r) {
+                    e = cudaMemcpyAsync(dst + size_t(r) * piece, src + size_t(r * slot_stride) * 2u, piece,
+                                        cudaMemcpyDeviceToDevice, stream);
+                    if (e != cudaSuccess)
+                        return cuda_fail(e, "1D placement copy");
+                }
+            }
+            const int64_t tail_rows = D - nfull * R;
+            if (tail_rows > 0) {
+                e = cudaMemcpyAsync(dst + size_t(nfull) * piece, src + size_t(nfull * slot_stride) * 2u,
+                                    size_t(tail_rows * K) * 2u, cudaMemcpyDeviceToDevice, stream);
+                if (e != cudaSuccess)
+                    return cuda_fail(e, "tail placement copy");
+            }
+        }
+    }
+    e = cudaEventRecord(plan->last_use, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "record plan event");
+    return TIDE_OK;
+}
+
+tide_status_t tide_plan_destroy(tide_plan_t *plan)
+{
+    t_last_error.clear();
+    if (!plan)
+        return TIDE_OK;
+    free_device(plan);
+    delete plan;
+    return TIDE_OK;
+}
+
+int64_t tide_plan_slot_numel(const tide_plan_t *plan) { return plan ? plan->slot_numel : -1; }
+
+int64_t tide_plan_num_segments(const tide_plan_t *plan) { return plan ? int64_t(plan->segs.size()) : -1; }
+
+tide_status_t tide_plan_segment(const tide_plan_t *plan, int64_t index, tide_segment_t *out)
+{
+    if (!plan || !out)
+        return fail(TIDE_ERR_INVALID_ARG, "plan or out is NULL");
+    if (index < 0 || index >= int64_t(plan->segs.size()))
+        return fail(TIDE_ERR_INVALID_ARG, "segment index %lld out of range", (long long)index);
+    const tide::Seg &s = plan->segs[size_t(index)];
+    out->param = s.param;
+    out->rank = s.rank;
+    out->src_elem = s.src_elem;
+    out->dst_elem = s.dst_elem;
+    out->n_valid = s.n_valid;
+    out->n_pad = s.n_pad;
+    return TIDE_OK;
+}
+
+tide_status_t tide_plan_fold_config(const tide_plan_t *plan, int32_t *grid, int32_t *block, int64_t *items,
+                                    int64_t *chunk_elems)
+{
+    if (!plan)
+        return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+    const int64_t n = int64_t(plan->rs_items.size());
+    if (grid)
+        *grid = int32_t(std::min<int64_t>(plan->grid, n));
+    if (block)
+        *block = plan->block;
+    if (items)
+        *items = n;
+    if (chunk_elems)
+        *chunk_elems = plan->chunk_elems;
+    return TIDE_OK;
+}
+
+tide_status_t tide_last_device_status(tide_plan_t *plan, void *stream_)
+{
+    t_last_error.clear();
+    if (!plan)
+        return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
+    if (plan->host_only)
+        return TIDE_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    int32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, plan->d_status, sizeof word, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "read device status");
+    if (word != 0) {
+        e = cudaMemsetAsync(plan->d_status, 0, sizeof(int32_t), stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "clear device status");
+        return fail(TIDE_ERR_TIMEOUT, "a bounded device wait expired (code %d)", word);
+    }
+    return TIDE_OK;
+}
+
+}  // extern "C"

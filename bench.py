@@ -1,0 +1,444 @@
+"""Benchmark of the layout-folded reduce-scatter + all-gather placement step.
+
+One step = one pass of the hot path over one gradient group: the fused
+bf16 -> fp32 reduce-scatter fold of W virtual ranks (tide_rs_fold) followed
+by the all-gather placement of W bf16 shard slots into the group's full
+parameter tensors (tide_ag_place).  Default workload: one Llama-3.1-8B
+decoder block, W = 8 (218,112,000 elements per gradient set).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  ``value`` is the whole-job effective
+bandwidth: algorithmic bytes of all steps on all GPUs / max-over-ranks time,
+with the RS fold counting W*N*2 read + N*4 written (+N*4 read when
+accumulating) and the placement N*2 read + N*2 written.  Inputs are larger
+than L2 (no flush needed); timing uses CUDA events on the launching stream.
+
+``--impl reference`` times the CPU oracle (the plain two-pass definition) on
+a bounded sample of the same workload, on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused bf16→fp32 reduce-scatter effective GB/s and % of GB300 HBM roofline"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "llama3.1_8b_block"
+SAMPLE_PARAMS = ("q_proj", "k_proj", "v_proj", "o_proj")  # CPU sample: the attention projections
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--ag-mode", choices=["sm", "ce2d", "ce1d"], default="sm")
+    ap.add_argument("--kernel", choices=["auto", "direct", "bulk"], default="auto")
+    ap.add_argument("--sched", choices=["static", "dynamic"], default="static")
+    ap.add_argument("--cta-budget", type=int, default=0)
+    ap.add_argument("--chunk-bytes", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-baseline", action="store_true", help="skip the two-pass GPU baseline")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def alg_bytes(w, numel: int):
+    rs = w.world * numel * 2 + numel * 4 + (numel * 4 if w.accumulate else 0)
+    ag = numel * 2 + numel * 2
+    return rs, ag
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons) while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5:
+            time.sleep(0.05)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((t, parts))
+        inside = [r for t, r in rows if t0 <= t <= t1]
+        window = "timed"
+        if not inside:  # the timed region was shorter than the sampling period
+            inside = [r for t, r in rows if t0 - 1.0 <= t <= t1 + 1.0]
+            window = "timed+-1s"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = sorted(v for v in (num(r[1]) for r in inside) if v is not None)
+        mx = [v for v in (num(r[2]) for r in inside) if v is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside), "window": window,
+                "power_w_max": max((num(r[3]) or 0.0) for r in inside)}
+
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def profile_traffic(workload: str):
+    """Per-launch DRAM bytes of the fold kernel from the committed ncu summary,
+    or None if there is none or the kernel source changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"rs_fold_{workload}_traffic.txt")
+    src = os.path.join(ROOT, "all_gather_gb300", "csrc", "rs_fold.cu")
+    try:
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("rs_fold_cu_sha256_16") != digest:
+            return None
+        return float(kv["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+def cpu_oracle_sample(w, host_grads=None, min_seconds=10.0, max_reps=50):
+    """Time the CPU oracle (reduce-scatter then placement) on the attention
+    projections of the workload.  host_grads[p][u]: uint16 arrays, or None to
+    generate them on the CPU with the same recipe."""
+    import numpy as np
+
+    import oracle
+    import workloads
+    idx = [w.names.index(n) for n in SAMPLE_PARAMS if n in w.names]
+    dims_all = w.dim0_rownumel()
+    dims = [dims_all[i] for i in idx]
+    if host_grads is None:
+        host_grads = []
+        for i in idx:
+            n = dims_all[i][0] * dims_all[i][1]
+            host_grads.append([workloads.normal_fp32(n, workloads.grad_seed(w, u, i), w.sigma, "cpu", w.outlier_rate,
+                                                     w.outlier_scale).to(__import__("torch").bfloat16)
+                               .view(__import__("torch").int16).numpy().view(np.uint16) for u in range(w.world)])
+    orc = oracle.load()
+    _, _, S = orc.geometry(w.world, dims)
+    out = np.zeros((w.world, S), np.float32)
+    slots = np.random.default_rng(0).integers(0, 0x3F00, size=(w.world, S), dtype=np.uint16)
+    numel = sum(d * k for d, k in dims)
+    rs_b, ag_b = alg_bytes(w, numel)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        orc.rs(w.world, dims, host_grads, w.alpha, w.accumulate, out)
+        orc.ag(w.world, dims, slots)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    return {"value": round((rs_b + ag_b) * reps / el / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{'+'.join(SAMPLE_PARAMS)} of {w.name}, all {w.world} ranks "
+                      f"({numel} elements per gradient set), reduce-scatter + placement, {reps} reps in {el:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    import workloads
+    w = workloads.get(args.workload)
+    if rank != 0:
+        return 0
+    sample = None
+    import numpy as np
+
+    import oracle
+    idx = [w.names.index(n) for n in SAMPLE_PARAMS if n in w.names]
+    dims_all = w.dim0_rownumel()
+    dims = [dims_all[i] for i in idx]
+    import torch
+    host = [[workloads.normal_fp32(dims_all[i][0] * dims_all[i][1], workloads.grad_seed(w, u, i), w.sigma, "cpu",
+                                   w.outlier_rate, w.outlier_scale).to(torch.bfloat16).view(torch.int16).numpy()
+             .view(np.uint16) for u in range(w.world)] for i in idx]
+    orc = oracle.load()
+    _, _, S = orc.geometry(w.world, dims)
+    out = np.zeros((w.world, S), np.float32)
+    slots = np.random.default_rng(0).integers(0, 0x3F00, size=(w.world, S), dtype=np.uint16)
+    numel = sum(d * k for d, k in dims)
+    rs_b, ag_b = alg_bytes(w, numel)
+
+    def step():
+        orc.rs(w.world, dims, host, w.alpha, w.accumulate, out)
+        orc.ag(w.world, dims, slots)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = (rs_b + ag_b) * args.steps / el / 1e9
+    sample = (f"{'+'.join(SAMPLE_PARAMS)} of {w.name}, all {w.world} ranks ({numel} elements per gradient set), "
+              f"reduce-scatter + placement per step")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": w.name, "world": w.world, "sample": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import all_gather_gb300 as tide
+    import workloads
+    from all_gather_gb300 import baselines
+    from all_gather_gb300 import build as _build
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    _build.build()
+    dev = torch.device("cuda", local)
+    w = workloads.get(args.workload)
+    numel = w.total_numel()
+    rs_b, ag_b = alg_bytes(w, numel)
+    step_bytes = rs_b + ag_b
+
+    gs = workloads.make_grads(w, device=dev)
+    flags = tide.make_flags(cta_budget=args.cta_budget, chunk_bytes=args.chunk_bytes,
+                            sched={"static": 0, "dynamic": 1}[args.sched],
+                            kernel={"auto": 0, "direct": 1, "bulk": 2}[args.kernel])
+    plan = tide.Plan(gs.views, flags)
+    S = plan.slot_numel
+    cfg = plan.fold_config()
+    out = workloads.make_out_init(w, S, device=dev) if w.accumulate else torch.zeros(w.world, S, device=dev)
+    slots = workloads.make_slots(w, S, device=dev)
+    full = [torch.empty(s, dtype=torch.bfloat16, device=dev) for s in w.shapes]
+    stream = torch.cuda.current_stream()
+
+    def step():
+        plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
+        plan.ag_place(slots, full, mode=args.ag_mode)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = tide.tide_launch_count()
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
+        ev[i][1].record(stream)
+        plan.ag_place(slots, full, mode=args.ag_mode)
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    launches = tide.tide_launch_count() - launches0
+    clocks.stop()
+    total_ms = start.elapsed_time(end)
+    rs_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    ag_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    rs_mean = sum(rs_ms) / K
+    ag_mean = sum(ag_ms) / K
+    peak, peak_kind = measured_peak_gbs()
+    achieved = rs_b / (rs_mean * 1e-3) / 1e9
+    clk = clocks.summary(t_wall0, t_wall1)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "world": w.world, "params": w.num_params, "elements": numel,
+                   "alpha": w.alpha, "accumulate": w.accumulate, "ag_mode": args.ag_mode,
+                   "fold_grid": cfg["grid"], "fold_block": cfg["block"], "fold_items": cfg["items"],
+                   "chunk_elems": cfg["chunk_elems"], "l2": "inputs larger than L2 (no flush)",
+                   "step": "tide_rs_fold + tide_ag_place", "parallelism": f"weak: {world} independent replicas"},
+        "parts": {"rs_fold": {"ms": round(rs_mean, 4), "gbs": round(achieved, 1), "alg_bytes": rs_b},
+                  "ag_place": {"ms": round(ag_mean, 4), "gbs": round(ag_b / (ag_mean * 1e-3) / 1e9, 1),
+                               "alg_bytes": ag_b}},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profile_traffic(w.name),
+                     "kernel": "tide_rs_fold", "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "frac_of_8tbs_nominal": round(achieved / 8000.0, 4)},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+
+    # two-pass stock-FSDP2-style baseline (chunk_cat pack to fp32, then reduce), timed alone
+    if not args.no_baseline and rank == 0:
+        result["baseline_two_pass"] = baselines.time_two_pass(w, gs.views, S, out, slots, full, steps=min(K, 10))
+        b = result["baseline_two_pass"]
+        b["fused_speedup_rs"] = round(b["rs_ms"] / rs_mean, 3)
+        b["fused_speedup_ag"] = round(b["ag_ms"] / ag_mean, 3)
+
+    # end to end through the public API: pinned host inputs -> device -> fold + place -> host
+    if not args.no_e2e:
+        result["e2e"] = e2e(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world)
+
+    if rank == 0 and not args.no_cpu_baseline:
+        host = []
+        for name in SAMPLE_PARAMS:
+            i = w.names.index(name)
+            host.append([gs.views[u][i].reshape(-1).view(torch.int16).cpu().numpy().view(np.uint16)
+                         for u in range(w.world)])
+        result["cpu_baseline"] = cpu_oracle_sample(w, host)
+
+    plan.close()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world):
+    import torch
+    import torch.distributed as dist
+    stream = torch.cuda.current_stream()
+    h_arenas = [a.cpu().pin_memory() for a in gs.arenas]
+    h_slots = slots.cpu().pin_memory()
+    h_out0 = out.cpu().pin_memory()
+    h_out = torch.empty_like(h_out0).pin_memory()
+    h_full = [torch.empty(f.shape, dtype=f.dtype).pin_memory() for f in full]
+    h2d = sum(a.numel() * a.element_size() for a in h_arenas) + h_slots.numel() * 2
+    h2d += h_out0.numel() * 4 if w.accumulate else 0
+    d2h = h_out.numel() * 4 + sum(f.numel() * 2 for f in h_full)
+    K = max(1, args.e2e_steps)
+
+    def one():
+        for a, h in zip(gs.arenas, h_arenas):
+            a.copy_(h, non_blocking=True)
+        slots.copy_(h_slots, non_blocking=True)
+        if w.accumulate:
+            out.copy_(h_out0, non_blocking=True)
+        plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
+        plan.ag_place(slots, full, mode=args.ag_mode)
+        h_out.copy_(out, non_blocking=True)
+        for f, h in zip(full, h_full):
+            h.copy_(f, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(K):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / K
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "steps": K,
+            "note": "pinned host grads+slots -> device, tide_rs_fold + tide_ag_place, shards+full params -> host"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,233 @@
+/*
+ * tide.h -- C ABI of the GB300 layout-folded reduce-scatter (TIDE-RS fold)
+ * and all-gather placement (TIDE-AG addressing) for FSDP2 parameter groups.
+ *
+ * Source of the operations: "The Endgame of FSDP Communication: Layout-Aware
+ * Collectives on Copy Engines, RDMA, and NVSwitch" (TIDE).
+ *   - Section 2.1 and Table 2: dim-0 shard geometry.  Parameter p is viewed as
+ *     (D_p, K_p); each of the W ranks owns R_p = ceil(D_p / W) rows (rows past
+ *     D_p are zero padding); rank shards are concatenated parameter-major at
+ *     prefix offsets o_p inside one rank slot of S = sum_p R_p K_p elements.
+ *   - Section 4, Equation (5): out_{p,r} <- (accumulate ? out_{p,r} : 0)
+ *       + alpha * sum_{u=0}^{W-1} G_p^(u)[rows of rank r].
+ *   - Section 2.1, Equation (2): all-gather landing; rank r's shard of p moves
+ *     from slot r, offset o_p to rows [r R_p, r R_p + v_{p,r}) of the full
+ *     parameter tensor, padding dropped.
+ *   - Section 6: no metadata is copied to the GPU per call; the gradient
+ *     pointer table is uploaded once when the plan is built (or rebound).
+ *
+ * Here all W ranks are virtual: their gradients and shard slots are W sets
+ * of buffers in the same GPU's memory, and the collective becomes one W-way
+ * gather-sum kernel (reduce-scatter) and one placement kernel or copy-engine
+ * copy (all-gather).  There is no inter-GPU traffic.
+ *
+ * Conventions for every call:
+ *   - Ownership: the caller owns every tensor (gradients, fp32 shards, bf16
+ *     slots, full parameters).  A plan owns only its device tables (allocated
+ *     in tide_plan_build, freed in tide_plan_destroy).  tide_rs_fold and
+ *     tide_ag_place allocate nothing.
+ *   - Pointers named "device" must be CUDA device (or managed) memory of the
+ *     current device; pointers named "host" are ordinary host memory read
+ *     before the call returns.
+ *   - Streams are cudaStream_t values passed as void*; NULL is the legacy
+ *     default stream.  Hot calls are asynchronous and stream-ordered; a plan
+ *     must not be used on two streams at once without caller synchronisation.
+ *   - Errors are returned as tide_status_t, never thrown; on failure nothing
+ *     was enqueued.  tide_last_error() gives a human-readable detail for the
+ *     last failing call on the calling thread.
+ *   - Numerics: bf16 -> fp32 widening is exact; the W contributions are added
+ *     in fp32, round-to-nearest-even, in rank order 0, 1, ..., W-1 starting
+ *     from rank 0's value; then y = alpha * sum; then out = old + y in
+ *     accumulate mode.  No FMA contraction, no flush-to-zero.  Results are
+ *     bitwise independent of CTA budget, chunk size and scheduling.
+ */
+#ifndef TIDE_H
+#define TIDE_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TIDE_API __attribute__((visibility("default")))
+#else
+#define TIDE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TIDE_OK = 0,
+    TIDE_ERR_INVALID_ARG = 1,  /* bad count, size, null pointer, aliasing, ... */
+    TIDE_ERR_ALIGNMENT = 2,    /* pointer not aligned to its element size */
+    TIDE_ERR_UNSUPPORTED = 3,  /* valid request this build does not implement: fall back to the two-pass path */
+    TIDE_ERR_OOM = 4,          /* plan tables could not be allocated */
+    TIDE_ERR_CUDA = 5,         /* a CUDA runtime call failed (detail in tide_last_error) */
+    TIDE_ERR_TIMEOUT = 6       /* a bounded device-side wait expired (tide_last_device_status) */
+} tide_status_t;
+
+/* Opaque plan: geometry, work list and device tables of one parameter group. */
+typedef struct tide_plan tide_plan_t;
+
+/* One parameter of the group (Section 2.1 notation). */
+typedef struct {
+    /* Host array of W device pointers: rank_base[u] is G_p^(u), the bf16
+     * gradient of this parameter on virtual rank u, row-major and contiguous
+     * (dim0 * row_numel elements).  2-byte aligned; 16-byte alignment enables
+     * the vector path.  The array itself is copied during the call. */
+    const void *const *rank_base;
+    int64_t dim0;          /* D_p >= 0: extent of dimension 0 (0 = empty tensor, pointers may be NULL) */
+    int64_t row_numel;     /* K_p >= 0: product of the trailing dimensions (1 for a vector) */
+    int64_t shard_offset;  /* o_p in elements inside a rank slot, or -1 to use the prefix sum
+                              of the preceding parameters' R_q K_q.  Explicit offsets must not
+                              make two shards overlap. */
+} tide_param_desc_t;
+
+/* Summation order of the reduce-scatter fold. */
+enum {
+    TIDE_ORDER_RANK_ASC = 0  /* ((G0 + G1) + G2) + ... : the bit-exact contract */
+};
+
+/* Work distribution of the fold's persistent grid (bitwise identical results). */
+enum {
+    TIDE_SCHED_STATIC = 0,   /* work item i goes to CTA i mod grid */
+    TIDE_SCHED_DYNAMIC = 1   /* CTAs claim items from a device counter that resets itself */
+};
+
+/* Reduce-scatter kernel family. */
+enum {
+    TIDE_KERNEL_AUTO = 0,    /* the library's default */
+    TIDE_KERNEL_DIRECT = 1,  /* 16-byte vector loads of the W rank rows straight into registers */
+    TIDE_KERNEL_BULK = 2     /* warp-specialised: bulk async copies (cp.async.bulk + mbarrier)
+                                stage the W rank rows in shared memory */
+};
+
+/* All-gather placement engines. */
+enum {
+    TIDE_AG_SM = 0,      /* placement kernel: 16-byte vector copies per (parameter, rank) piece */
+    TIDE_AG_CE_2D = 1,   /* copy engines: one 2D copy per parameter over its full-shard ranks
+                            (source pitch = slot stride, destination pitch = R_p K_p) + 1 tail copy */
+    TIDE_AG_CE_1D = 2    /* copy engines: one 1D copy per (parameter, rank) piece */
+};
+
+/* Gradient element type. */
+enum {
+    TIDE_DTYPE_BF16 = 0
+};
+
+/* Debug bits. */
+#define TIDE_DEBUG_HOST_ONLY 0x1u  /* build geometry and work list only: no device tables, no CUDA calls.
+                                      Such a plan can be inspected but not launched. */
+
+typedef struct {
+    int32_t cta_budget;   /* CTAs of the fold's persistent grid; 0 = one wave at full occupancy */
+    int32_t chunk_bytes;  /* bf16 bytes per rank in one work item (multiple of 256); 0 = default */
+    int32_t order;        /* TIDE_ORDER_* */
+    int32_t sched;        /* TIDE_SCHED_* */
+    int32_t kernel;       /* TIDE_KERNEL_* */
+    int32_t grad_dtype;   /* TIDE_DTYPE_* */
+    uint32_t debug;       /* TIDE_DEBUG_* bits */
+    int32_t reserved[5];  /* must be zero */
+} tide_plan_flags_t;
+
+/* Read-only view of one (parameter, rank) shard piece of a plan. */
+typedef struct {
+    int32_t param;       /* p */
+    int32_t rank;        /* r */
+    int64_t src_elem;    /* first element of rank r's rows in G_p^(u): r * R_p * K_p */
+    int64_t dst_elem;    /* o_p: element offset of the piece inside rank r's slot */
+    int64_t n_valid;     /* v_{p,r} * K_p real elements */
+    int64_t n_pad;       /* (R_p - v_{p,r}) * K_p padding elements */
+} tide_segment_t;
+
+/*
+ * Build a plan for one parameter group of `num_params` parameters sharded over
+ * `world` virtual ranks (1 <= world <= 1024).  Computes R_p, o_p, S and the
+ * P*W shard pieces (Section 2.1), splits them into work items, validates
+ * every descriptor, allocates the plan's device tables and uploads them with
+ * asynchronous copies on `stream`.  `params` is a host array; `flags` may be
+ * NULL for defaults.  On success *plan_out owns the tables.
+ * Errors: INVALID_ARG (world, counts, dims, null pointers, overlapping
+ * explicit offsets, nonzero reserved fields), ALIGNMENT (a gradient pointer
+ * not 2-byte aligned), UNSUPPORTED (an order, dtype or kernel this build
+ * lacks), OOM, CUDA.
+ */
+TIDE_API tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_param_desc_t *params,
+                              const tide_plan_flags_t *flags, void *stream, tide_plan_t **plan_out);
+
+/*
+ * Point an existing plan at new gradient storage with the same geometry (for
+ * example, the next step's gradients).  dim0, row_numel and shard_offset must
+ * equal the plan's.  The new pointer table is uploaded on `stream`, ordered
+ * after earlier work on that stream.
+ */
+TIDE_API tide_status_t tide_plan_rebind(tide_plan_t *plan, const tide_param_desc_t *params, void *stream);
+
+/*
+ * Reduce-scatter fold (Section 4, Equation (5)) of every parameter into every
+ * virtual rank's fp32 shard.
+ *   out_base: device fp32, W rank slots; rank r's slot starts at
+ *             out_base + r * out_slot_stride and its shard of parameter p at
+ *             offset o_p.  Padding positions receive alpha * (+0) (or old +
+ *             alpha * (+0) in accumulate mode).  Elements of a slot past S are
+ *             not touched.  4-byte aligned.  Must not overlap any gradient.
+ *   out_slot_stride: elements between rank slots, >= S.
+ *   alpha: scale applied to the fp32 sum (1/W for an average).
+ *   accumulate: 0 = overwrite, 1 = add into the existing shard values.
+ * Enqueued on `stream`; returns without waiting.
+ */
+TIDE_API tide_status_t tide_rs_fold(tide_plan_t *plan, float *out_base, int64_t out_slot_stride, float alpha,
+                           int32_t accumulate, void *stream);
+
+/*
+ * All-gather placement (Section 2.1, Equation (2)).
+ *   slots_base: device bf16, W rank slots of `slot_stride` elements (>= S);
+ *               rank r's shard of parameter p is read from
+ *               slots_base + r * slot_stride + o_p.  Padding is never read.
+ *   full: host array of P device pointers; full[p] receives parameter p as a
+ *         contiguous row-major (dim0, row_numel) bf16 tensor.  2-byte aligned;
+ *         must not overlap the slots or each other.
+ *   mode: TIDE_AG_SM, TIDE_AG_CE_2D or TIDE_AG_CE_1D.
+ * Bitwise copy; enqueued on `stream`.
+ */
+TIDE_API tide_status_t tide_ag_place(tide_plan_t *plan, const void *slots_base, int64_t slot_stride, void *const *full,
+                            int32_t mode, void *stream);
+
+/* Free the plan's device tables after synchronising the stream of its last use. */
+TIDE_API tide_status_t tide_plan_destroy(tide_plan_t *plan);
+
+/* S: elements per rank slot (the smallest valid out_slot_stride / slot_stride); -1 for NULL. */
+TIDE_API int64_t tide_plan_slot_numel(const tide_plan_t *plan);
+
+/* Number of (parameter, rank) shard pieces, P * W; -1 for NULL. */
+TIDE_API int64_t tide_plan_num_segments(const tide_plan_t *plan);
+
+/* Copy shard piece `index` (ordered by parameter, then rank) into *out. */
+TIDE_API tide_status_t tide_plan_segment(const tide_plan_t *plan, int64_t index, tide_segment_t *out);
+
+/* Launch geometry the plan will use for the fold: grid CTAs, threads per CTA,
+ * work items, elements per item.  Any pointer may be NULL. */
+TIDE_API tide_status_t tide_plan_fold_config(const tide_plan_t *plan, int32_t *grid, int32_t *block, int64_t *items,
+                                    int64_t *chunk_elems);
+
+/*
+ * Read and clear the plan's device status word (synchronises `stream`).
+ * Returns TIDE_ERR_TIMEOUT if a bounded device-side wait of an earlier fold
+ * on this plan expired (that fold's output is then incomplete), else TIDE_OK.
+ */
+TIDE_API tide_status_t tide_last_device_status(tide_plan_t *plan, void *stream);
+
+/* Kernels this library has launched in this process (all plans, all calls). */
+TIDE_API uint64_t tide_launch_count(void);
+
+/* Human-readable name of a status code. */
+TIDE_API const char *tide_status_string(tide_status_t status);
+
+/* Detail message of the last failing call on this thread ("" if none). */
+TIDE_API const char *tide_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TIDE_H */

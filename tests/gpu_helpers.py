@@ -1,0 +1,81 @@
+"""Helpers for the GPU parity tests: host copies, oracle runs, sampled checks."""
+from __future__ import annotations
+
+import random
+from typing import List, Sequence, Tuple
+
+import numpy as np
+import torch
+
+import oracle
+from bits import assert_same_f32, assert_same_u16
+
+
+def bits16(t: torch.Tensor) -> np.ndarray:
+    """A bf16 tensor (any device) as a flat host uint16 array."""
+    return t.detach().reshape(-1).view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def oracle_rs_full(world: int, dims, grads_uv: Sequence[Sequence[torch.Tensor]], alpha: float, accumulate: bool,
+                   out_before: torch.Tensor) -> np.ndarray:
+    """Run the oracle over everything (small cases).  grads_uv[u][p]."""
+    host = [[bits16(grads_uv[u][p]) for u in range(world)] for p in range(len(dims))]
+    want = out_before.detach().cpu().numpy().astype(np.float32, copy=True)
+    oracle.rs(world, dims, host, alpha, accumulate, want)
+    return want
+
+
+def row_windows(R: int, v: int, rnd: random.Random, span: int = 3) -> List[Tuple[int, int]]:
+    """Row windows of one piece: its first rows, its last rows (padding if any),
+    the boundary between real and padding rows, and one random window."""
+    if R == 0:
+        return []
+    wins = {(0, min(span, R)), (max(0, R - span), R)}
+    if 0 < v < R:
+        wins.add((max(0, v - 1), min(R, v + 1)))
+    a = rnd.randrange(R)
+    wins.add((a, min(R, a + span)))
+    return sorted(wins)
+
+
+def sampled_rs_check(world: int, dims, grads_uv, out_before: torch.Tensor, out_after: torch.Tensor, alpha: float,
+                     accumulate: bool, seed: int = 0, ranks_per_param: int = 3, what: str = "") -> int:
+    """Compare sampled windows of a full-size fold with the oracle, window by
+    window (oracle.rs_window).  Returns the number of elements compared."""
+    rnd = random.Random(seed)
+    R, o, S = oracle.geometry(world, dims)
+    checked = 0
+    for p, (d, k) in enumerate(dims):
+        ranks = sorted({0, world - 1, rnd.randrange(world)} if ranks_per_param >= 3 else {rnd.randrange(world)})
+        for r in ranks:
+            v = oracle.valid_rows(d, R[p], r)
+            for (i0, i1) in row_windows(R[p], v, rnd):
+                lo, hi = i0 * k, i1 * k
+                nv = max(0, min(hi, v * k) - lo)
+                base = r * R[p] * k + lo
+                srcs = [bits16(grads_uv[u][p].reshape(-1)[base:base + nv]) for u in range(world)]
+                old = out_before[r, o[p] + lo:o[p] + hi].cpu().numpy() if accumulate else None
+                want = oracle.rs_window(srcs, nv, (hi - lo) - nv, alpha, accumulate, old)
+                got = out_after[r, o[p] + lo:o[p] + hi].cpu().numpy()
+                assert_same_f32(got, want, f"{what} p={p} r={r} rows [{i0},{i1})")
+                checked += hi - lo
+    return checked
+
+
+def ag_expected(world: int, dims, slots: torch.Tensor) -> List[np.ndarray]:
+    return oracle.ag(world, dims, bits16(slots).reshape(world, -1))
+
+
+def sentinel_slots(world: int, dims, stride: int, seed: int, device="cuda") -> torch.Tensor:
+    """bf16 [W, stride] slots: random real rows, NaN sentinel (0x7FC1) in padding
+    and past S, so that any padding read shows up in the output."""
+    R, o, S = oracle.geometry(world, dims)
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    vals = torch.randint(0, 0x7F00, (world, stride), generator=g, dtype=torch.int32).to(torch.int16)
+    mask = np.ones((world, stride), dtype=bool)
+    for p, (d, k) in enumerate(dims):
+        for r in range(world):
+            v = oracle.valid_rows(d, R[p], r)
+            mask[r, o[p]:o[p] + v * k] = False
+    vals[torch.from_numpy(mask)] = 0x7FC1
+    return vals.view(torch.bfloat16).to(device)

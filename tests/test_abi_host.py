@@ -1,0 +1,212 @@
+"""Host logic of the C-ABI library, no GPU needed: the library loads and
+exports every symbol include/tide.h declares; host-only plans reproduce the
+oracle's shard geometry (Section 2.1) and tile each slot exactly; argument
+validation returns the documented status codes without touching the device."""
+import os
+import random
+import re
+
+import pytest
+
+import oracle
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def tide():
+    from all_gather_gb300 import build
+    build.build()
+    import all_gather_gb300
+    all_gather_gb300.load_library()
+    return all_gather_gb300
+
+
+def _fake_ptrs(W, P, numels, align=256, base=0x7F0000000000):
+    """Distinct, non-overlapping fake device addresses [p][u]."""
+    ptrs, cur = [], base
+    for p in range(P):
+        row = []
+        for u in range(W):
+            row.append(cur)
+            cur += (max(numels[p], 1) * 2 + align - 1) // align * align + align
+        ptrs.append(row)
+    return ptrs, cur
+
+
+def _host_plan(tide, W, dims, ptrs=None, offsets=None, **flag_kw):
+    numels = [d * k for d, k in dims]
+    if ptrs is None:
+        ptrs, _ = _fake_ptrs(W, len(dims), numels)
+    params = [(ptrs[p], d, k, -1 if offsets is None else offsets[p]) for p, (d, k) in enumerate(dims)]
+    flags = tide.make_flags(debug=tide.TIDE_DEBUG_HOST_ONLY, **flag_kw)
+    return tide.tide_plan_build(W, params, flags, 0)
+
+
+def test_exports_match_header(tide):
+    with open(os.path.join(ROOT, "include", "tide.h")) as f:
+        declared = set(re.findall(r"TIDE_API[^;(]*?\b(tide_\w+)\s*\(", f.read()))
+    assert declared == set(tide.EXPORTED), declared ^ set(tide.EXPORTED)
+    lib = tide.load_library()
+    for name in declared:
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_status_strings(tide):
+    for code, name in [(0, "TIDE_OK"), (1, "TIDE_ERR_INVALID_ARG"), (2, "TIDE_ERR_ALIGNMENT"),
+                       (3, "TIDE_ERR_UNSUPPORTED"), (4, "TIDE_ERR_OOM"), (5, "TIDE_ERR_CUDA"),
+                       (6, "TIDE_ERR_TIMEOUT")]:
+        assert tide.tide_status_string(code) == name
+
+
+def _check_geometry(tide, W, dims):
+    plan = _host_plan(tide, W, dims)
+    try:
+        R, o, S = oracle.geometry(W, dims)
+        assert tide.tide_plan_slot_numel(plan) == S
+        segs = [tide.tide_plan_segment(plan, i) for i in range(tide.tide_plan_num_segments(plan))]
+        assert len(segs) == W * len(dims)
+        covered = [[0] * S for _ in range(W)] if S * W <= 200_000 else None
+        pad_total = 0
+        for s in segs:
+            p, r = s["param"], s["rank"]
+            d, k = dims[p]
+            v = oracle.valid_rows(d, R[p], r)
+            assert s["src_elem"] == r * R[p] * k
+            assert s["dst_elem"] == o[p]
+            assert (s["n_valid"], s["n_pad"]) == (v * k, (R[p] - v) * k)
+            pad_total += s["n_pad"]
+            if covered is not None:
+                for j in range(s["n_valid"] + s["n_pad"]):
+                    covered[r][o[p] + j] += 1
+        assert pad_total == W * S - sum(d * k for d, k in dims)
+        if covered is not None:
+            assert all(c == 1 for row in covered for c in row), "pieces must tile every slot exactly once"
+        cfg = tide.tide_plan_fold_config(plan)
+        ch = cfg["chunk_elems"]
+        want_items = sum(-(-s["n_valid"] // ch) + -(-s["n_pad"] // ch) for s in segs)
+        assert cfg["items"] == want_items
+    finally:
+        tide.tide_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("w", workloads.WORKLOADS, ids=[w.name for w in workloads.WORKLOADS])
+def test_geometry_matches_oracle_workloads(tide, w):
+    _check_geometry(tide, w.world, w.dim0_rownumel())
+
+
+def test_geometry_matches_oracle_random(tide):
+    rnd = random.Random(1)
+    for _ in range(60):
+        W = rnd.choice([1, 2, 3, 4, 5, 7, 8, 16, 32, 33])
+        dims = [(rnd.choice([0, 1, 2, W - 1 or 1, W, W + 1, 3 * W + 2, 100]), rnd.choice([0, 1, 3, 8, 17]))
+                for _ in range(rnd.randint(0, 6))]
+        _check_geometry(tide, W, dims)
+
+
+def test_explicit_offsets(tide):
+    dims = [(10, 4), (3, 3)]
+    plan = _host_plan(tide, 2, dims, offsets=[64, 0])
+    try:
+        assert tide.tide_plan_slot_numel(plan) == 64 + 5 * 4
+        seg = tide.tide_plan_segment(plan, 0)
+        assert seg["dst_elem"] == 64
+    finally:
+        tide.tide_plan_destroy(plan)
+    with pytest.raises(tide.TideError) as e:
+        _host_plan(tide, 2, dims, offsets=[0, 10])  # [0, 20) and [10, 16) overlap
+    assert e.value.status == tide.TIDE_ERR_INVALID_ARG
+
+
+def test_empty_group(tide):
+    plan = _host_plan(tide, 4, [])
+    try:
+        assert tide.tide_plan_slot_numel(plan) == 0
+        assert tide.tide_plan_fold_config(plan)["items"] == 0
+    finally:
+        tide.tide_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("case, status", [
+    ("world0", "TIDE_ERR_INVALID_ARG"), ("world_big", "TIDE_ERR_INVALID_ARG"),
+    ("neg_dim", "TIDE_ERR_INVALID_ARG"), ("null_ptr", "TIDE_ERR_INVALID_ARG"),
+    ("odd_ptr", "TIDE_ERR_ALIGNMENT"), ("reserved", "TIDE_ERR_INVALID_ARG"),
+    ("chunk", "TIDE_ERR_INVALID_ARG"), ("order", "TIDE_ERR_UNSUPPORTED"),
+    ("dtype", "TIDE_ERR_UNSUPPORTED"), ("overflow", "TIDE_ERR_INVALID_ARG"),
+    ("neg_offset", "TIDE_ERR_INVALID_ARG"), ("sched", "TIDE_ERR_INVALID_ARG"),
+])
+def test_build_validation(tide, case, status):
+    W, dims = 4, [(8, 8), (5, 1)]
+    ptrs, _ = _fake_ptrs(W, 2, [64, 5])
+    kw = {}
+    offsets = None
+    world = W
+    if case == "world0":
+        world = 0
+    elif case == "world_big":
+        world = 1025
+        ptrs = [[0x10000] * 1025, [0x20000] * 1025]
+    elif case == "neg_dim":
+        dims = [(-1, 8), (5, 1)]
+    elif case == "null_ptr":
+        ptrs[1][2] = 0
+    elif case == "odd_ptr":
+        ptrs[0][3] += 1
+    elif case == "chunk":
+        kw["chunk_bytes"] = 300
+    elif case == "order":
+        kw["order"] = 7
+    elif case == "dtype":
+        kw["grad_dtype"] = 1
+    elif case == "overflow":
+        dims = [(1 << 40, 1 << 30), (5, 1)]
+    elif case == "neg_offset":
+        offsets = [-2, -1]
+    elif case == "sched":
+        kw["sched"] = 9
+    flags = tide.make_flags(debug=tide.TIDE_DEBUG_HOST_ONLY, **kw)
+    if case == "reserved":
+        flags.reserved[2] = 1
+    params = [(ptrs[p], d, k, -1 if offsets is None else offsets[p]) for p, (d, k) in enumerate(dims)]
+    with pytest.raises(tide.TideError) as e:
+        tide.tide_plan_build(world, params, flags, 0)
+    assert tide.tide_status_string(e.value.status) == status, str(e.value)
+    assert e.value.detail, "a failing call must leave a detail message"
+
+
+def test_host_only_plan_cannot_launch(tide):
+    plan = _host_plan(tide, 2, [(4, 4)])
+    try:
+        with pytest.raises(tide.TideError) as e:
+            tide.tide_rs_fold(plan, 0x1000, 100, 1.0, 0, 0)
+        assert e.value.status == tide.TIDE_ERR_INVALID_ARG
+        with pytest.raises(tide.TideError) as e:
+            tide.tide_ag_place(plan, 0x1000, 100, [0x2000], tide.TIDE_AG_SM, 0)
+        assert e.value.status == tide.TIDE_ERR_INVALID_ARG
+    finally:
+        tide.tide_plan_destroy(plan)
+
+
+def test_rebind_checks_geometry(tide):
+    W, dims = 2, [(4, 4), (3, 1)]
+    plan = _host_plan(tide, W, dims)
+    try:
+        ptrs, _ = _fake_ptrs(W, 2, [16, 3], base=0x6F0000000000)
+        tide.tide_plan_rebind(plan, [(ptrs[0], 4, 4, -1), (ptrs[1], 3, 1, -1)], 0)
+        with pytest.raises(tide.TideError):
+            tide.tide_plan_rebind(plan, [(ptrs[0], 5, 4, -1), (ptrs[1], 3, 1, -1)], 0)
+        bad = [list(ptrs[0]), list(ptrs[1])]
+        bad[0][1] += 1
+        with pytest.raises(tide.TideError) as e:
+            tide.tide_plan_rebind(plan, [(bad[0], 4, 4, -1), (bad[1], 3, 1, -1)], 0)
+        assert e.value.status == tide.TIDE_ERR_ALIGNMENT
+    finally:
+        tide.tide_plan_destroy(plan)
+
+
+def test_launch_count_starts_at_zero_without_gpu(tide):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("only meaningful before any GPU work")
+    assert tide.tide_launch_count() == 0

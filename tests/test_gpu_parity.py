@@ -1,0 +1,338 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Reduce-scatter fold: bit-exact (rank-ascending fp32 order is the contract).
+All-gather placement: bit-exact.  Small cases compare every element; the
+full-size workloads compare sampled windows, each recomputed by the oracle.
+"""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import all_gather_gb300 as tide
+import oracle
+import workloads
+from bits import assert_same_f32, assert_same_u16, f32_to_bf16_bits
+from gpu_helpers import (ag_expected, bits16, oracle_rs_full, sampled_rs_check, sentinel_slots)
+
+pytestmark = pytest.mark.gpu
+
+CANARY = float.fromhex("0x1.deadbep+100")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from all_gather_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+
+
+def _fold(w_or_world, grads_uv, alpha, acc, out, **flag_kw):
+    world = len(grads_uv)
+    flags = tide.make_flags(**flag_kw) if flag_kw else None
+    with tide.Plan(grads_uv, flags) as plan:
+        plan.rs_fold(out, alpha=alpha, accumulate=acc)
+        torch.cuda.synchronize()
+        assert plan.device_status() == tide.TIDE_OK
+    return out
+
+
+def _random_grads(world, shapes, seed, scale=1e-3):
+    w = workloads.custom(world, shapes, sigma=scale, index=50 + seed % 1000)
+    return w, workloads.make_grads(w, device="cuda")
+
+
+def _guarded_out(world, S, extra, init=None):
+    """fp32 [W, S + extra] inside a larger buffer with canary bands around it."""
+    stride = S + extra
+    buf = torch.full((world * stride + 64,), CANARY, device="cuda", dtype=torch.float32)
+    out = buf[32:32 + world * stride].view(world, stride)
+    if init is not None:
+        out[:, :S].copy_(init[:, :S])
+    return buf, out
+
+
+def _check_canaries(buf, out, S):
+    host = buf.cpu().numpy()
+    assert (host[:32] == np.float32(CANARY)).all(), "wrote before the output"
+    assert (host[32 + out.numel():] == np.float32(CANARY)).all(), "wrote after the output"
+    tail = out[:, S:].cpu().numpy()
+    assert (tail == np.float32(CANARY)).all(), "wrote past S inside a slot"
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("acc", [False, True])
+@pytest.mark.parametrize("alpha", ["1/W", 1.0])
+@pytest.mark.parametrize("sched", [tide.TIDE_SCHED_STATIC, tide.TIDE_SCHED_DYNAMIC])
+def test_toy_full_parity(acc, alpha, sched):
+    w = workloads.get(1)
+    a = 1.0 / w.world if alpha == "1/W" else alpha
+    dims = w.dim0_rownumel()
+    gs = workloads.make_grads(w, device="cuda")
+    _, _, S = oracle.geometry(w.world, dims)
+    init = workloads.make_out_init(w, S, device="cuda") if acc else None
+    buf, out = _guarded_out(w.world, S, 5, init)
+    before = out.clone()
+    _fold(w, gs.views, a, acc, out, sched=sched)
+    want = oracle_rs_full(w.world, dims, gs.views, a, acc, before)
+    assert_same_f32(out[:, :S].cpu().numpy(), want[:, :S], f"toy alpha={a} acc={acc} sched={sched}")
+    _check_canaries(buf, out, S)
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 5, 8, 16, 32])
+@pytest.mark.parametrize("chunk", [256, 0])
+def test_ragged_shapes(world, chunk):
+    rnd = random.Random(world * 101 + chunk)
+    shapes = [(rnd.randint(1, 3 * world + 7), rnd.choice([1, 3, 8, 17, 64, 129])) for _ in range(5)]
+    shapes += [(world * 37 + 5, 100), (rnd.randint(1, world), 7), (4099,)]
+    w, gs = _random_grads(world, shapes, seed=world + chunk)
+    dims = w.dim0_rownumel()
+    _, _, S = oracle.geometry(world, dims)
+    for acc in (False, True):
+        init = torch.randn(world, S, device="cuda") if acc else None
+        buf, out = _guarded_out(world, S, 3, init)
+        before = out.clone()
+        _fold(w, gs.views, 1.0 / world, acc, out, chunk_bytes=chunk)
+        want = oracle_rs_full(world, dims, gs.views, 1.0 / world, acc, before)
+        assert_same_f32(out[:, :S].cpu().numpy(), want[:, :S], f"ragged W={world} chunk={chunk} acc={acc}")
+        _check_canaries(buf, out, S)
+
+
+@pytest.mark.parametrize("case", ["uniform_phase", "mixed_phase", "odd_out", "odd_stride"])
+def test_misaligned(case):
+    world, shapes = 4, [(67, 33), (9, 8), (130, 64), (5,)]
+    rnd = random.Random(7)
+    numels = [int(np.prod(s)) for s in shapes]
+    # each rank's tensors live at chosen element offsets inside one buffer
+    views = []
+    for u in range(world):
+        shift = {"uniform_phase": 3, "mixed_phase": u, "odd_out": 0, "odd_stride": 0}[case]
+        buf = torch.empty(sum(numels) + 64 * len(shapes) + 16, dtype=torch.bfloat16, device="cuda")
+        vs, cur = [], shift
+        for s, n in zip(shapes, numels):
+            x = torch.randn(n, device="cuda") * 1e-3
+            vs.append(buf[cur:cur + n].view(s))
+            vs[-1].copy_(x.view(s).to(torch.bfloat16))
+            cur += n + 8 * rnd.randint(0, 3) + (1 if case == "mixed_phase" else 0)
+        views.append(vs)
+    dims = [(s[0], int(np.prod(s[1:])) if len(s) > 1 else 1) for s in shapes]
+    _, _, S = oracle.geometry(world, dims)
+    stride = S + (3 if case == "odd_stride" else 0)
+    base = torch.full((world * stride + 8,), CANARY, device="cuda", dtype=torch.float32)
+    off = 1 if case == "odd_out" else 0
+    out = base[off:off + world * stride].view(world, stride)
+    before = out.clone()
+    _fold(None, views, 0.25, False, out)
+    want = oracle_rs_full(world, dims, views, 0.25, False, before)
+    assert_same_f32(out[:, :S].cpu().numpy(), want[:, :S], case)
+
+
+def test_special_values():
+    world, shapes = 5, [(41, 24), (13,), (7, 9)]
+    specials = np.array([np.nan, np.inf, -np.inf, -0.0, 0.0, 2.0 ** -133, -(2.0 ** -130), 3.3895e38, -3.3895e38,
+                         1.0, 2.0 ** -24], dtype=np.float32)
+    rng = np.random.default_rng(3)
+
+    def fill(u, p, n, device):
+        x = rng.standard_normal(n).astype(np.float32)
+        m = rng.random(n) < 0.3
+        x[m] = rng.choice(specials, size=int(m.sum()))
+        return torch.from_numpy(x).to(device)
+
+    w = workloads.custom(world, shapes, index=77)
+    gs = workloads.make_grads(w, device="cuda", fill=fill)
+    dims = w.dim0_rownumel()
+    _, _, S = oracle.geometry(world, dims)
+    for acc in (False, True):
+        init = torch.from_numpy(rng.choice(specials, size=(world, S))).cuda() if acc else None
+        buf, out = _guarded_out(world, S, 0, init)
+        before = out.clone()
+        _fold(w, gs.views, 1.0, acc, out)
+        want = oracle_rs_full(world, dims, gs.views, 1.0, acc, before)
+        assert_same_f32(out.cpu().numpy(), want, f"special values acc={acc}")
+
+
+@pytest.mark.parametrize("world", [2, 3, 8, 32])
+def test_order_probe(world):
+    """Closed form: 1.0 on rank 0 and 2^-24 elsewhere sums to exactly 1.0 in
+    rank order; 1.0 on the last rank gives round(1 + (W-1) 2^-24)."""
+    n = 4096 + 3
+    for big_rank, expect in ((0, 1.0), (world - 1, float(np.float32(1.0 + (world - 1) * 2.0 ** -24)))):
+        grads = [[torch.full((n,), 1.0 if u == big_rank else 2.0 ** -24, device="cuda").to(torch.bfloat16)]
+                 for u in range(world)]
+        out = torch.zeros(world, -(-n // world), device="cuda")
+        _fold(None, grads, 1.0, False, out)
+        R = -(-n // world)
+        flat = out.reshape(-1)[:n].cpu().numpy()
+        assert_same_f32(flat, np.full(n, expect, np.float32), f"order probe W={world} big={big_rank}")
+
+
+def test_determinism_across_launch_shapes():
+    w = workloads.get(1)
+    gs = workloads.make_grads(w, device="cuda")
+    _, _, S = oracle.geometry(w.world, w.dim0_rownumel())
+    ref = None
+    for kw in ({}, {"cta_budget": 1}, {"cta_budget": 3}, {"cta_budget": 152}, {"chunk_bytes": 256},
+               {"chunk_bytes": 65536}, {"sched": tide.TIDE_SCHED_DYNAMIC, "cta_budget": 7},
+               {"sched": tide.TIDE_SCHED_DYNAMIC, "chunk_bytes": 512}):
+        out = torch.zeros(w.world, S, device="cuda")
+        _fold(w, gs.views, 0.25, False, out, **kw)
+        got = out.cpu().numpy()
+        if ref is None:
+            ref = got
+        else:
+            assert_same_f32(got, ref, f"launch shape {kw}")
+
+
+def test_repeated_calls_and_rebind():
+    w = workloads.get(1)
+    dims = w.dim0_rownumel()
+    g1 = workloads.make_grads(w, device="cuda")
+    w2 = workloads.custom(w.world, w.shapes, index=91)
+    g2 = workloads.make_grads(w2, device="cuda")
+    _, _, S = oracle.geometry(w.world, dims)
+    flags = tide.make_flags(sched=tide.TIDE_SCHED_DYNAMIC)
+    with tide.Plan(g1.views, flags) as plan:
+        for grads in (g1, g2, g1):
+            plan.rebind(grads.views)
+            for _ in range(3):  # the dynamic-schedule counters must reset between launches
+                out = torch.zeros(w.world, S, device="cuda")
+                plan.rs_fold(out, alpha=0.5)
+                torch.cuda.synchronize()
+                want = oracle_rs_full(w.world, dims, grads.views, 0.5, False, torch.zeros(w.world, S))
+                assert_same_f32(out.cpu().numpy(), want, "rebind")
+
+
+def test_empty_and_degenerate():
+    # no parameters at all
+    with tide.Plan([[] for _ in range(3)]) as plan:
+        assert plan.slot_numel == 0
+        plan.rs_fold(torch.zeros(3, 1, device="cuda"))
+    # zero-size parameters mixed with real ones
+    shapes = [(0, 5), (3, 2), (4, 0)]
+    grads = [[torch.zeros(s, dtype=torch.bfloat16, device="cuda") + u for s in shapes] for u in range(2)]
+    dims = [(0, 5), (3, 2), (4, 0)]
+    _, _, S = oracle.geometry(2, dims)
+    out = torch.full((2, S), 9.0, device="cuda")
+    with tide.Plan(grads) as plan:
+        assert plan.slot_numel == S
+        plan.rs_fold(out)
+        torch.cuda.synchronize()
+    want = oracle_rs_full(2, dims, grads, 1.0, False, torch.full((2, S), 9.0))
+    assert_same_f32(out.cpu().numpy(), want, "degenerate shapes")
+
+
+def test_call_errors():
+    w = workloads.get(1)
+    gs = workloads.make_grads(w, device="cuda")
+    with tide.Plan(gs.views) as plan:
+        S = plan.slot_numel
+        with pytest.raises(tide.TideError) as e:  # output aliasing a gradient
+            tide.tide_rs_fold(plan.handle, gs.arenas[2].data_ptr(), S, 1.0, 0, 0)
+        assert e.value.status == tide.TIDE_ERR_INVALID_ARG
+        out = torch.zeros(w.world * S + 1, device="cuda")
+        with pytest.raises(tide.TideError) as e:  # 2-byte misaligned fp32 output
+            tide.tide_rs_fold(plan.handle, out.data_ptr() + 2, S, 1.0, 0, 0)
+        assert e.value.status == tide.TIDE_ERR_ALIGNMENT
+        with pytest.raises(tide.TideError) as e:  # stride below S
+            tide.tide_rs_fold(plan.handle, out.data_ptr(), S - 1, 1.0, 0, 0)
+        assert e.value.status == tide.TIDE_ERR_INVALID_ARG
+        with pytest.raises(tide.TideError):
+            tide.tide_rs_fold(plan.handle, out.data_ptr(), S, 1.0, 2, 0)
+        slots = torch.zeros(w.world, S, dtype=torch.bfloat16, device="cuda")
+        full = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for s in w.shapes]
+        with pytest.raises(tide.TideError) as e:  # a full tensor inside the slots
+            tide.tide_ag_place(plan.handle, slots.data_ptr(), S, [slots.data_ptr()] + [f.data_ptr() for f in full[1:]],
+                               tide.TIDE_AG_SM, 0)
+        assert e.value.status == tide.TIDE_ERR_INVALID_ARG
+        with pytest.raises(tide.TideError):
+            tide.tide_ag_place(plan.handle, slots.data_ptr(), S, [f.data_ptr() for f in full], 9, 0)
+
+
+# ---------------------------------------------------------------------------
+# all-gather placement
+@pytest.mark.parametrize("mode", ["sm", "ce2d", "ce1d"])
+def test_ag_toy_and_ragged(mode):
+    cases = [workloads.get(1)]
+    rnd = random.Random(5)
+    for world in (1, 3, 8, 16):
+        shapes = [(rnd.randint(1, 4 * world + 3), rnd.choice([1, 5, 8, 64])) for _ in range(4)] + [(world * 100 + 1,)]
+        cases.append(workloads.custom(world, shapes, index=60 + world))
+    for w in cases:
+        dims = w.dim0_rownumel()
+        _, _, S = oracle.geometry(w.world, dims)
+        grads = workloads.make_grads(w, device="cuda")  # only used to build the plan's geometry
+        slots = sentinel_slots(w.world, dims, S + 7, seed=w.index)
+        total = sum(d * k for d, k in dims)
+        guard = 64
+        buf = torch.full((total + guard * (len(dims) + 1),), -7.0, device="cuda").to(torch.bfloat16)
+        full, cur = [], guard
+        for s, (d, k) in zip(w.shapes, dims):
+            full.append(buf[cur:cur + d * k].view(s))
+            cur += d * k + guard
+        with tide.Plan(grads.views) as plan:
+            plan.ag_place(slots, full, mode=mode)
+            torch.cuda.synchronize()
+        want = ag_expected(w.world, dims, slots)
+        for p, f in enumerate(full):
+            assert_same_u16(bits16(f), want[p], f"ag {mode} {w.name} p={p}")
+        host = bits16(buf)
+        guard_bits = bits16(torch.tensor([-7.0], dtype=torch.bfloat16))[0]
+        cur = 0
+        for d, k in dims:
+            assert (host[cur:cur + guard] == guard_bits).all(), "placement wrote outside a full tensor"
+            cur += guard + d * k
+        assert (host[cur:] == guard_bits).all()
+
+
+def test_ag_shard_roundtrip_identity():
+    """AG(shard(x)) == x for full-size-like shapes with misaligned offsets."""
+    world = 8
+    shapes = [(1000, 33), (77,), (64, 64)]
+    xs = [torch.randn(s, device="cuda").to(torch.bfloat16) for s in shapes]
+    dims = [(s[0], int(np.prod(s[1:])) if len(s) > 1 else 1) for s in shapes]
+    R, o, S = oracle.geometry(world, dims)
+    slots = torch.full((world, S + 1), float("nan"), device="cuda").to(torch.bfloat16)
+    for p, x in enumerate(xs):
+        for r, ch in enumerate(torch.chunk(x, world)):
+            slots[r, o[p]:o[p] + ch.numel()] = ch.reshape(-1)
+    grads = [[torch.empty(s, dtype=torch.bfloat16, device="cuda") for s in shapes] for _ in range(world)]
+    for mode in ("sm", "ce2d", "ce1d"):
+        full = [torch.empty_like(x) for x in xs]
+        with tide.Plan(grads) as plan:
+            plan.ag_place(slots, full, mode=mode)
+            torch.cuda.synchronize()
+        for p, (x, f) in enumerate(zip(xs, full)):
+            assert_same_u16(bits16(f), bits16(x), f"AG(shard(x)) {mode} p={p}")
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads in the benchmark's launch configuration
+@pytest.mark.parametrize("index", [2, 3, 4, 5])
+def test_full_size_sampled(index):
+    w = workloads.get(index)
+    dims = w.dim0_rownumel()
+    gs = workloads.make_grads(w, device="cuda")
+    R, o, S = oracle.geometry(w.world, dims)
+    with tide.Plan(gs.views) as plan:   # default flags: what the benchmark times
+        assert plan.slot_numel == S
+        for alpha, acc in ((w.alpha, w.accumulate), (1.0 / w.world, not w.accumulate)):
+            out = workloads.make_out_init(w, S, device="cuda") if acc else torch.empty(w.world, S, device="cuda")
+            before = out.clone() if acc else None
+            plan.rs_fold(out, alpha=alpha, accumulate=acc)
+            torch.cuda.synchronize()
+            n = sampled_rs_check(w.world, dims, gs.views, before, out, alpha, acc, seed=index,
+                                 what=f"{w.name} alpha={alpha} acc={acc}")
+            assert n > 0
+            del out, before
+        # all-gather placement of full-size slots, every element
+        slots = workloads.make_slots(w, S, device="cuda")
+        full = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for s in w.shapes]
+        plan.ag_place(slots, full, mode="sm")
+        torch.cuda.synchronize()
+        want = ag_expected(w.world, dims, slots)
+        for p, f in enumerate(full):
+            assert_same_u16(bits16(f), want[p], f"{w.name} ag p={p}")
+    del gs
+    torch.cuda.empty_cache()
