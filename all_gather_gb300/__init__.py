@@ -17,7 +17,8 @@ from __future__ import annotations
 from typing import List, Optional, Sequence
 
 from ._binding import (  # noqa: F401  (re-exported C-ABI names)
-    EXPORTED, LIB_PATH, TIDE_AG_CE_1D, TIDE_AG_CE_2D, TIDE_AG_SM, TIDE_DEBUG_HOST_ONLY, TIDE_DTYPE_BF16,
+    EXPORTED, LIB_PATH, TIDE_AG_CE_1D, TIDE_AG_CE_2D, TIDE_AG_SM, TIDE_DEBUG_HOST_ONLY, TIDE_DEBUG_SHORT_WAIT,
+    TIDE_DEBUG_SKIP_FILL, TIDE_DTYPE_BF16,
     TIDE_ERR_ALIGNMENT, TIDE_ERR_CUDA, TIDE_ERR_INVALID_ARG, TIDE_ERR_OOM, TIDE_ERR_TIMEOUT, TIDE_ERR_UNSUPPORTED,
     TIDE_KERNEL_AUTO, TIDE_KERNEL_BULK, TIDE_KERNEL_DIRECT, TIDE_OK, TIDE_ORDER_RANK_ASC, TIDE_SCHED_DYNAMIC,
     TIDE_SCHED_STATIC, PlanFlags, TideError, load_library, make_flags, tide_ag_place, tide_last_device_status,

@@ -29,6 +29,8 @@ TIDE_KERNEL_AUTO, TIDE_KERNEL_DIRECT, TIDE_KERNEL_BULK = 0, 1, 2
 TIDE_AG_SM, TIDE_AG_CE_2D, TIDE_AG_CE_1D = 0, 1, 2
 TIDE_DTYPE_BF16 = 0
 TIDE_DEBUG_HOST_ONLY = 0x1
+TIDE_DEBUG_SHORT_WAIT = 0x2
+TIDE_DEBUG_SKIP_FILL = 0x4
 
 EXPORTED = ("tide_plan_build", "tide_plan_rebind", "tide_rs_fold", "tide_ag_place", "tide_plan_destroy",
             "tide_plan_slot_numel", "tide_plan_num_segments", "tide_plan_segment", "tide_plan_fold_config",

@@ -253,19 +253,324 @@ FoldKernel pick_direct(int world)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Bulk-copy kernel.  Warp 0 is the producer: one elected lane streams each
+// work item's W rank rows into a ring of shared-memory stages with
+// cp.async.bulk (the TMA engine's non-tensor copy), one copy per rank per
+// fill, completing on the stage's "full" mbarrier with a transaction count.
+// Warps 1..4 consume a stage (fp32 adds in rank order from shared memory,
+// scale, optional accumulate, 16-byte streaming stores) and release it on
+// its "empty" mbarrier.  Every wait is bounded by %globaltimer: on expiry
+// the kernel records a status word, stops issuing, waits (bounded) for the
+// copies it already issued, and returns.
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `parity` to complete; false if `budget_ns` passed
+// or another warp raised the abort flag first.
+__device__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t budget_ns, volatile int32_t *abort_flag)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (abort_flag && *abort_flag)
+            return false;
+        if (global_ns() - t0 > budget_ns)
+            return false;
+    }
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 lds_v4(const uint16_t *p)
+{
+    return *reinterpret_cast<const uint4 *>(p);
+}
+
+constexpr int32_t kStatusConsumerTimeout = 1;
+constexpr int32_t kStatusProducerTimeout = 2;
+constexpr int32_t kStatusDrainTimeout = 3;
+
+// One element from global memory (pieces the producer does not stage).
+template <int WT, bool ACC>
+__device__ __forceinline__ void fold_scalar_global(const uint64_t *bp, int W, int64_t src_off, float *dst, float alpha)
+{
+    float acc = ld_bf16(reinterpret_cast<const uint16_t *>(bp[0]) + src_off);
+    for (int u = 1; u < (WT > 0 ? WT : W); ++u)
+        acc = __fadd_rn(acc, ld_bf16(reinterpret_cast<const uint16_t *>(bp[u]) + src_off));
+    float y = __fmul_rn(alpha, acc);
+    if (ACC)
+        y = __fadd_rn(*dst, y);
+    __stcs(dst, y);
+}
+
+template <int WT, bool ACC>
+__global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParams fp)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int W = WT > 0 ? WT : fp.world;
+    const int STAGES = fp.stages;
+    const int64_t FILL = fp.fill_elems;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + STAGES;
+    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(empty + STAGES);
+    uint16_t *ring = reinterpret_cast<uint16_t *>(smem + ((size_t(2 * STAGES) * 8 + 8 + 127) / 128) * 128);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float alpha = fp.alpha;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kBulkConsumerWarps);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        if (lane != 0)
+            return;
+        // ------------------------------------------------------------ producer
+        uint32_t stage = 0, phase = 0;
+        int64_t fills = 0, skipped = -1;
+        bool stop = false;
+        for (int64_t it = blockIdx.x; it < fp.n_items && !stop; it += gridDim.x) {
+            const Item item = fp.items[it];
+            const Seg seg = fp.segs[item.seg];
+            if ((item.count_kind & kItemPad) || seg.src_phase != 0)
+                continue;
+            const int64_t count = int64_t(item.count_kind & ~kItemPad);
+            const uint64_t *bp = fp.ptrs + int64_t(seg.param) * W;
+            for (int64_t c = 0; c < count; c += FILL) {
+                const int64_t len = count - c < FILL ? count - c : FILL;
+                const uint32_t bytes = uint32_t(len & ~int64_t(7)) * 2u;
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, fp.wait_budget_ns, abort_flag)) {
+                    if (!*abort_flag)
+                        atomicExch(fp.status, kStatusProducerTimeout);
+                    *abort_flag = 1;
+                    stop = true;
+                    break;
+                }
+                if ((fp.debug & TIDE_DEBUG_SKIP_FILL) && blockIdx.x == 0 && fills == 0) {
+                    skipped = fills;  // leave this stage unfilled: its consumers' wait expires
+                } else {
+                    mbar_arrive_expect_tx(&full[stage], uint32_t(W) * bytes);
+                    if (bytes) {
+                        uint16_t *dst = ring + size_t(stage) * W * FILL;
+                        const int64_t off = seg.src_elem + item.begin + c;
+                        for (int u = 0; u < W; ++u)
+                            bulk_copy_g2s(dst + size_t(u) * FILL, reinterpret_cast<const uint16_t *>(bp[u]) + off,
+                                          bytes, &full[stage]);
+                    }
+                }
+                ++fills;
+                if (++stage == uint32_t(STAGES)) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        // Drain: the last fills of each stage must land before this CTA exits.
+        const int64_t first = fills > STAGES ? fills - STAGES : 0;
+        for (int64_t f = first; f < fills; ++f) {
+            if (f == skipped)
+                continue;
+            const uint32_t s = uint32_t(f % STAGES), par = uint32_t((f / STAGES) & 1);
+            if (!mbar_wait_bounded(&full[s], par, fp.wait_budget_ns, nullptr))
+                atomicExch(fp.status, kStatusDrainTimeout);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int ctid = threadIdx.x - 32;
+    constexpr int NCT = 32 * kBulkConsumerWarps;
+    uint32_t stage = 0, phase = 0;
+    for (int64_t it = blockIdx.x; it < fp.n_items; it += gridDim.x) {
+        const Item item = fp.items[it];
+        const Seg seg = fp.segs[item.seg];
+        const int64_t count = int64_t(item.count_kind & ~kItemPad);
+        const bool pad = (item.count_kind & kItemPad) != 0;
+        float *dst = fp.out + int64_t(seg.rank) * fp.stride + seg.dst_elem + (pad ? seg.n_valid : 0) + item.begin;
+        const uint64_t *bp = fp.ptrs + int64_t(seg.param) * W;
+        if (pad) {
+            const float y = __fmul_rn(alpha, 0.0f);
+            for (int64_t e = ctid; e < count; e += NCT)
+                __stcs(dst + e, ACC ? __fadd_rn(dst[e], y) : y);
+            continue;
+        }
+        if (seg.src_phase != 0) {
+            for (int64_t e = ctid; e < count; e += NCT)
+                fold_scalar_global<WT, ACC>(bp, W, seg.src_elem + item.begin + e, dst + e, alpha);
+            continue;
+        }
+        const bool dst_vec = (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
+        for (int64_t c = 0; c < count; c += FILL) {
+            const int64_t len = count - c < FILL ? count - c : FILL;
+            if (!mbar_wait_bounded(&full[stage], phase, fp.wait_budget_ns, abort_flag)) {
+                if (!*abort_flag)
+                    atomicExch(fp.status, kStatusConsumerTimeout);
+                *abort_flag = 1;
+                return;
+            }
+            const uint16_t *sb = ring + size_t(stage) * W * FILL;
+            const int64_t nv = len >> 3;
+            for (int64_t v = ctid; v < nv; v += NCT) {
+                float acc[8];
+                unpack8(lds_v4(sb + v * 8), acc);
+#pragma unroll 8
+                for (int u = 1; u < (WT > 0 ? WT : W); ++u) {
+                    float f[8];
+                    unpack8(lds_v4(sb + size_t(u) * FILL + v * 8), f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        acc[e] = __fadd_rn(acc[e], f[e]);
+                }
+                store8<ACC>(dst + c + v * 8, acc, alpha, dst_vec);
+            }
+            for (int64_t e = nv * 8 + ctid; e < len; e += NCT)
+                fold_scalar_global<WT, ACC>(bp, W, seg.src_elem + item.begin + c + e, dst + c + e, alpha);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[stage]);
+            if (++stage == uint32_t(STAGES)) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
+template <bool ACC>
+FoldKernel pick_bulk(int world)
+{
+    switch (world) {
+    case 1: return fold_bulk_kernel<1, ACC>;
+    case 2: return fold_bulk_kernel<2, ACC>;
+    case 4: return fold_bulk_kernel<4, ACC>;
+    case 8: return fold_bulk_kernel<8, ACC>;
+    case 16: return fold_bulk_kernel<16, ACC>;
+    case 32: return fold_bulk_kernel<32, ACC>;
+    default: return fold_bulk_kernel<0, ACC>;
+    }
+}
+
 }  // namespace
 
-size_t fold_smem_bytes(int /*kernel*/, int world, int64_t /*chunk_elems*/) { return size_t(world) * sizeof(uint64_t); }
-
-cudaError_t fold_occupancy(int /*kernel*/, int world, int block, size_t smem, int *blocks_per_sm)
+BulkShape bulk_shape(int world)
 {
+    // Fills of >= 1 KB per rank while a stage stays within 32 KB; smaller
+    // fills only for very wide groups.
+    BulkShape b{};
+    int64_t fill = 8192 / world;
+    if (fill < 512)
+        fill = 512;
+    if (fill * world * 2 > 32768)
+        fill = 32768 / (2 * int64_t(world));
+    fill &= ~int64_t(7);
+    if (fill < 8)
+        fill = 8;
+    const int64_t stage_bytes = fill * world * 2;
+    int64_t stages = kBulkSmemTarget / stage_bytes;
+    if (stages > 8)
+        stages = 8;
+    if (stages < 2)
+        stages = 2;
+    b.fill_elems = int32_t(fill);
+    b.stages = int32_t(stages);
+    b.smem_bytes = size_t(((2 * stages * 8 + 8 + 127) / 128) * 128 + stages * stage_bytes);
+    return b;
+}
+
+size_t fold_smem_bytes(int kernel, int world, int64_t /*chunk_elems*/)
+{
+    if (kernel == TIDE_KERNEL_BULK)
+        return bulk_shape(world).smem_bytes;
+    return size_t(world) * sizeof(uint64_t);
+}
+
+cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *blocks_per_sm)
+{
+    if (kernel == TIDE_KERNEL_BULK) {
+        // Allow the device maximum once per kernel: the generic-world instance
+        // serves several stage sizes.
+        int dev = 0, optin = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess)
+            return e;
+        if (smem > size_t(optin))
+            return cudaErrorInvalidValue;
+        for (int acc = 0; acc < 2; ++acc) {
+            FoldKernel k = acc ? pick_bulk<true>(world) : pick_bulk<false>(world);
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+            if (e != cudaSuccess)
+                return e;
+        }
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, pick_bulk<false>(world), block, smem);
+    }
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, pick_direct<false>(world), block, smem);
 }
 
-cudaError_t launch_fold(const FoldParams &fp, int /*kernel*/, int accumulate, int grid, int block, size_t smem,
+cudaError_t launch_fold(const FoldParams &fp, int kernel, int accumulate, int grid, int block, size_t smem,
                         cudaStream_t stream)
 {
-    FoldKernel k = accumulate ? pick_direct<true>(fp.world) : pick_direct<false>(fp.world);
+    FoldKernel k;
+    if (kernel == TIDE_KERNEL_BULK)
+        k = accumulate ? pick_bulk<true>(fp.world) : pick_bulk<false>(fp.world);
+    else
+        k = accumulate ? pick_direct<true>(fp.world) : pick_direct<false>(fp.world);
     k<<<grid, block, smem, stream>>>(fp);
     return cudaGetLastError();
 }

@@ -15,6 +15,11 @@ namespace tide {
 
 constexpr int kMaxWorld = 1024;
 constexpr int kFoldThreads = 256;            // threads per fold CTA (direct kernel)
+constexpr int kBulkConsumerWarps = 4;        // bulk kernel: warp 0 produces, warps 1..4 consume
+constexpr int kBulkThreads = 32 * (1 + kBulkConsumerWarps);
+constexpr int kBulkSmemTarget = 96 * 1024;   // stage ring bytes per bulk CTA (two CTAs per SM)
+constexpr uint64_t kWaitBudgetNs = 4000000000ull;   // bounded mbarrier waits: 4 s
+constexpr uint64_t kShortWaitBudgetNs = 50000000ull; // with TIDE_DEBUG_SHORT_WAIT: 50 ms
 constexpr int kAgThreads = 256;              // threads per placement CTA
 constexpr int kAgParamsPerLaunch = 1024;     // full[] pointers passed by value per placement launch
 constexpr int64_t kDefaultChunkBytes = 16384;  // bf16 bytes per rank per fold work item
@@ -58,7 +63,19 @@ struct FoldParams {
     uint32_t *counters;    // [2] dynamic-schedule ticket and done counters
     int32_t *status;       // device status word
     uint32_t debug;
+    // bulk kernel only
+    uint64_t wait_budget_ns;  // bound on every mbarrier wait
+    int32_t fill_elems;       // elements per rank per stage fill (multiple of 8)
+    int32_t stages;           // ring depth
 };
+
+// Stage geometry of the bulk kernel for a world size.
+struct BulkShape {
+    int32_t fill_elems;
+    int32_t stages;
+    size_t smem_bytes;
+};
+BulkShape bulk_shape(int world);
 
 struct AgParams {
     const Seg *segs;

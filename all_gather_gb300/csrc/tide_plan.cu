@@ -85,8 +85,12 @@ tide_status_t check_flags(const tide_plan_flags_t &f)
         return fail(TIDE_ERR_INVALID_ARG, "flags.kernel %d", f.kernel);
     if (f.grad_dtype != TIDE_DTYPE_BF16)
         return fail(TIDE_ERR_UNSUPPORTED, "flags.grad_dtype %d is not implemented", f.grad_dtype);
-    if (f.debug & ~TIDE_DEBUG_HOST_ONLY)
+    if (f.debug & ~(TIDE_DEBUG_HOST_ONLY | TIDE_DEBUG_SHORT_WAIT | TIDE_DEBUG_SKIP_FILL))
         return fail(TIDE_ERR_INVALID_ARG, "unknown debug bits 0x%x", f.debug);
+    if (f.kernel == TIDE_KERNEL_BULK && f.sched == TIDE_SCHED_DYNAMIC)
+        return fail(TIDE_ERR_UNSUPPORTED, "the bulk-copy kernel schedules statically only");
+    if ((f.debug & TIDE_DEBUG_SKIP_FILL) && f.kernel != TIDE_KERNEL_BULK)
+        return fail(TIDE_ERR_INVALID_ARG, "TIDE_DEBUG_SKIP_FILL applies to the bulk-copy kernel only");
     return TIDE_OK;
 }
 
@@ -245,8 +249,6 @@ tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_para
     plan->host_only = (f.debug & TIDE_DEBUG_HOST_ONLY) != 0;
     plan->chunk_elems = (f.chunk_bytes ? f.chunk_bytes : tide::kDefaultChunkBytes) / 2;
     plan->kernel = f.kernel == TIDE_KERNEL_AUTO ? TIDE_KERNEL_DIRECT : f.kernel;
-    if (plan->kernel == TIDE_KERNEL_BULK)
-        return bail(fail(TIDE_ERR_UNSUPPORTED, "the bulk-copy kernel is not available in this build"));
 
     // --- geometry (Section 2.1): R_p = ceil(D_p / W), o_p, S -------------
     plan->dim0.resize(num_params);
@@ -335,7 +337,7 @@ tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_para
     if (plan->segs.size() > size_t(INT32_MAX) || plan->rs_items.size() > size_t(INT32_MAX))
         return bail(fail(TIDE_ERR_UNSUPPORTED, "too many work items; raise chunk_bytes"));
 
-    plan->block = tide::kFoldThreads;
+    plan->block = plan->kernel == TIDE_KERNEL_BULK ? tide::kBulkThreads : tide::kFoldThreads;
     plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, CH);
     if (plan->host_only) {
         plan->grid = f.cta_budget ? f.cta_budget : 0;
@@ -473,6 +475,10 @@ tide_status_t tide_rs_fold(tide_plan_t *plan, float *out_base, int64_t out_slot_
     fp.counters = plan->d_counters;
     fp.status = plan->d_status;
     fp.debug = plan->flags.debug;
+    fp.wait_budget_ns = (plan->flags.debug & TIDE_DEBUG_SHORT_WAIT) ? tide::kShortWaitBudgetNs : tide::kWaitBudgetNs;
+    const tide::BulkShape bs = tide::bulk_shape(plan->world);
+    fp.fill_elems = bs.fill_elems;
+    fp.stages = bs.stages;
     const int grid = int(std::min<int64_t>(plan->grid, fp.n_items));
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     cudaError_t e = tide::launch_fold(fp, plan->kernel, accumulate, grid, plan->block, plan->fold_smem, stream);

@@ -1,0 +1,153 @@
+"""Concurrent-compute interference of the reduce-scatter (measurement harness).
+
+Follows the method of the TIDE paper's Table 4 / Section 2.2: a victim kernel
+runs back to back on one stream while the reduce-scatter runs on another;
+the slowdown is the median duration of the victims that ran entirely inside
+the reduce-scatter window over the median duration of the victim alone,
+minus one.  Victims: a bf16 GEMM of 256 x 8192 x 8192 (the page's one-wave
+GEMM), a large 8192^3 bf16 GEMM, and a 256 MiB bf16 elementwise kernel.
+Arms: the fused fold at several CTA budgets and the two-pass stock-FSDP2
+baseline.  Set CUDA_DEVICE_MAX_CONNECTIONS=32 before CUDA starts (the page's
+setting) so the two streams get separate hardware queues.
+
+    python -m all_gather_gb300.interference [--workload NAME] [--budgets 0,16,64]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+from typing import Callable, Dict, List
+
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
+
+
+def _victims(dev) -> Dict[str, Callable[[], None]]:
+    import torch
+    g = torch.Generator(device=dev).manual_seed(1234)
+    a1 = torch.randn(256, 8192, device=dev, generator=g).to(torch.bfloat16)
+    b1 = torch.randn(8192, 8192, device=dev, generator=g).to(torch.bfloat16)
+    c1 = torch.empty(256, 8192, device=dev, dtype=torch.bfloat16)
+    a2 = torch.randn(8192, 8192, device=dev, generator=g).to(torch.bfloat16)
+    c2 = torch.empty(8192, 8192, device=dev, dtype=torch.bfloat16)
+    x = torch.randn(128 * 1024 * 1024, device=dev, generator=g).to(torch.bfloat16)  # 256 MiB
+    y = torch.empty_like(x)
+    return {
+        "gemm_256x8192x8192": lambda: torch.matmul(a1, b1, out=c1),
+        "gemm_8192x8192x8192": lambda: torch.matmul(a2, b1, out=c2),
+        "elementwise_256MiB": lambda: torch.mul(x, 1.0009765625, out=y),
+    }
+
+
+def _time_alone(fn, n: int, stream) -> float:
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fn()
+        for s, e in ev:
+            s.record(stream)
+            fn()
+            e.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(s.elapsed_time(e) for s, e in ev)
+
+
+def _co_run(rs_call: Callable[[], None], n_rs: int, victim, victim_ms: float, rs_ms_est: float) -> dict:
+    import torch
+    s_rs, s_v = torch.cuda.Stream(), torch.cuda.Stream()
+    n_v = int((rs_ms_est * n_rs) / max(victim_ms, 1e-3) * 1.5) + 20
+    n_v = min(n_v, 4000)
+    start = torch.cuda.Event(enable_timing=True)
+    rs0, rs1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_v)]
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    start.record(cur)
+    s_rs.wait_event(start)
+    s_v.wait_event(start)
+    with torch.cuda.stream(s_v):
+        for s, e in ev:
+            s.record(s_v)
+            victim()
+            e.record(s_v)
+    with torch.cuda.stream(s_rs):
+        rs0.record(s_rs)
+        for _ in range(n_rs):
+            rs_call()
+        rs1.record(s_rs)
+    torch.cuda.synchronize()
+    w0, w1 = start.elapsed_time(rs0), start.elapsed_time(rs1)
+    inside = [s.elapsed_time(e) for s, e in ev if start.elapsed_time(s) >= w0 and start.elapsed_time(e) <= w1]
+    return {"rs_window_ms": round(w1 - w0, 4), "rs_ms": round((w1 - w0) / n_rs, 4), "victims_inside": len(inside),
+            "victim_ms": round(statistics.median(inside), 5) if inside else None}
+
+
+def measure(workload: str = "llama3.1_8b_block", budgets=(0, 64, 16), n_rs: int = 20, device: int = 0,
+            grads=None) -> dict:
+    import torch
+
+    import all_gather_gb300 as tide
+    import workloads
+    from all_gather_gb300 import baselines
+
+    torch.cuda.set_device(device)
+    dev = torch.device("cuda", device)
+    w = workloads.get(workload)
+    gs = grads if grads is not None else workloads.make_grads(w, device=dev)
+    victims = _victims(dev)
+    plans = {}
+    for b in budgets:
+        plans[f"fused_cta{b}" if b else "fused_full_wave"] = tide.Plan(gs.views, tide.make_flags(cta_budget=b))
+    S = next(iter(plans.values())).slot_numel
+    out = torch.zeros(w.world, S, device=dev)
+    pack = torch.empty(w.world, w.world * S, device=dev)
+    arms = {name: (lambda p=p: p.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)) for name, p in plans.items()}
+    arms["two_pass_baseline"] = lambda: baselines.two_pass_rs(gs.views, pack, out, w.alpha, w.accumulate)
+
+    quiet = torch.cuda.Stream()
+    rs_alone = {name: _time_alone(fn, 10, quiet) for name, fn in arms.items()}
+    res = {"workload": w.name, "cuda_device_max_connections": os.environ.get("CUDA_DEVICE_MAX_CONNECTIONS"),
+           "rs_alone_ms": {k: round(v, 4) for k, v in rs_alone.items()}, "victims": {}}
+    for vname, vfn in victims.items():
+        alone = _time_alone(vfn, 50, quiet)
+        entry = {"alone_ms": round(alone, 5), "arms": {}}
+        for name, fn in arms.items():
+            r = _co_run(fn, n_rs, vfn, alone, rs_alone[name])
+            r["slowdown"] = round(r["victim_ms"] / alone - 1.0, 4) if r["victim_ms"] else None
+            entry["arms"][name] = r
+        res["victims"][vname] = entry
+    for p in plans.values():
+        p.close()
+    del pack, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def summarize(res: dict) -> dict:
+    """victim -> {arm: slowdown} plus the RS times per arm."""
+    return {"slowdown": {v: {a: r["slowdown"] for a, r in e["arms"].items()} for v, e in res["victims"].items()},
+            "victim_alone_ms": {v: e["alone_ms"] for v, e in res["victims"].items()},
+            "rs_alone_ms": res["rs_alone_ms"],
+            "rs_ms_while_corunning": {v: {a: r["rs_ms"] for a, r in e["arms"].items()}
+                                      for v, e in res["victims"].items()},
+            "method": "median victim duration fully inside the RS window / median alone - 1; "
+                      "CUDA_DEVICE_MAX_CONNECTIONS=" + str(res["cuda_device_max_connections"])}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="llama3.1_8b_block")
+    ap.add_argument("--budgets", default="0,64,16")
+    ap.add_argument("--n-rs", type=int, default=20)
+    a = ap.parse_args(argv)
+    res = measure(a.workload, tuple(int(x) for x in a.budgets.split(",")), a.n_rs)
+    print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    sys.exit(main())

@@ -22,6 +22,8 @@ from __future__ import annotations
 import argparse
 import json
 import os
+
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")  # before CUDA starts: separate queues per stream
 import subprocess
 import sys
 import threading
@@ -52,6 +54,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-baseline", action="store_true", help="skip the two-pass GPU baseline")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-interference", action="store_true", help="skip the concurrent-GEMM harness")
     return ap.parse_args()
 
 
@@ -63,6 +66,22 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The maximum of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Effective GB/s of the whole job: every rank's bytes over the slowest rank's time."""
+    return world * bytes_per_step_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def alg_bytes(w, numel: int):
     rs = w.world * numel * 2 + numel * 4 + (numel * 4 if w.accumulate else 0)
     ag = numel * 2 + numel * 2
@@ -70,76 +89,126 @@ def alg_bytes(w, numel: int):
 
 
 class ClockSampler:
-    """nvidia-smi samples (SM clock, max clock, throttle reasons) while running."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock, max clock, power and clock-event (throttle) reasons sampled
+    every ~2 ms while the timed region runs.  Reads NVML through ctypes (read
+    only: no setting is changed); falls back to `nvidia-smi -lms 100`."""
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index: int):
-        self.index = index
-        self.lines = []
-        self.proc = None
+    def __init__(self, cuda_index: int):
+        self.cuda_index = cuda_index
+        self.samples = []  # (time, sm_mhz, max_mhz, power_w, reasons_mask)
+        self.source = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._smi = None
+
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        count = ctypes.c_uint(0)
+        lib.nvmlDeviceGetCount_v2(ctypes.byref(count))
+        handle = ctypes.c_void_p()
+        want = ""
+        try:
+            import torch
+            want = str(torch.cuda.get_device_properties(self.cuda_index).uuid).lower().replace("gpu-", "")
+        except Exception:
+            pass
+        chosen = None
+        for i in range(count.value):
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(i, ctypes.byref(h)) != 0:
+                continue
+            buf = ctypes.create_string_buffer(96)
+            lib.nvmlDeviceGetUUID(h, buf, 96)
+            if want and want in buf.value.decode().lower():
+                chosen = h
+                break
+        if chosen is None:
+            if lib.nvmlDeviceGetHandleByIndex_v2(self.cuda_index, ctypes.byref(handle)) != 0:
+                raise OSError("no NVML handle")
+            chosen = handle
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, chosen, reasons_fn
 
     def start(self):
+        import ctypes
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+            lib, h, reasons_fn = self._nvml()
+        except (OSError, AttributeError):
+            return self._start_smi()
+        self.source = "nvml"
+        clk, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+
+        def loop():
+            while not self._stop.is_set():
+                lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk))
+                lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+                lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+                reasons_fn(h, ctypes.byref(rs))
+                self.samples.append((time.time(), clk.value, mx.value, pw.value / 1000.0, rs.value))
+                time.sleep(0.002)
+        self._thread = threading.Thread(target=loop, daemon=True)
+        self._thread.start()
+
+    def _start_smi(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self._smi = subprocess.Popen(["nvidia-smi", f"--id={self.cuda_index}", f"--query-gpu={q}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
-            self.proc = None
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
-        self.thread.start()
-        t0 = time.time()
-        while not self.lines and time.time() - t0 < 5:
-            time.sleep(0.05)
+        self.source = "nvidia-smi"
+        bits = [0x8, 0x40, 0x20, 0x4]
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append((time.time(), line.strip()))
-
-    def mark(self):
-        return time.time()
+        def loop():
+            for line in self._smi.stdout:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    mask = sum(b for b, v in zip(bits, parts[3:7]) if v.lower() == "active")
+                    self.samples.append((time.time(), float(parts[0]), float(parts[1]), float(parts[2]), mask))
+                except ValueError:
+                    continue
+        self._thread = threading.Thread(target=loop, daemon=True)
+        self._thread.start()
 
     def stop(self):
-        if self.proc:
-            self.proc.terminate()
+        self._stop.set()
+        if self._smi:
+            self._smi.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._smi.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
+                self._smi.kill()
+        if self._thread:
+            self._thread.join(timeout=5)
 
     def summary(self, t0, t1):
-        rows = []
-        for t, line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            rows.append((t, parts))
-        inside = [r for t, r in rows if t0 <= t <= t1]
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
         window = "timed"
-        if not inside:  # the timed region was shorter than the sampling period
-            inside = [r for t, r in rows if t0 - 1.0 <= t <= t1 + 1.0]
+        if not inside:
+            inside = [x for x in self.samples if t0 - 1.0 <= x[0] <= t1 + 1.0]
             window = "timed+-1s"
         if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-        sm = sorted(v for v in (num(r[1]) for r in inside) if v is not None)
-        mx = [v for v in (num(r[2]) for r in inside) if v is not None]
-        reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in inside:
-            for name, val in zip(names, r[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(inside), "window": window,
-                "power_w_max": max((num(r[3]) or 0.0) for r in inside)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
+        sm = sorted(x[1] for x in inside)
+        mask = 0
+        for x in inside:
+            mask |= int(x[4])
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(x[2] for x in inside),
+                "reasons": sorted(name for bit, name in self.REASONS.items() if mask & bit),
+                "samples": len(inside), "window": window, "source": self.source,
+                "power_w_max": round(max(x[3] for x in inside), 1)}
 
 
 def measured_peak_gbs():
@@ -327,12 +396,9 @@ def run_ours(args):
     total_ms = start.elapsed_time(end)
     rs_ms = [e[0].elapsed_time(e[1]) for e in ev]
     ag_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / K
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, world, ms_per_step)
     rs_mean = sum(rs_ms) / K
     ag_mean = sum(ag_ms) / K
     peak, peak_kind = measured_peak_gbs()
@@ -366,6 +432,12 @@ def run_ours(args):
         b = result["baseline_two_pass"]
         b["fused_speedup_rs"] = round(b["rs_ms"] / rs_mean, 3)
         b["fused_speedup_ag"] = round(b["ag_ms"] / ag_mean, 3)
+
+    # concurrent-compute interference (victim GEMMs / elementwise vs the RS arms)
+    if not args.no_interference and rank == 0:
+        from all_gather_gb300 import interference
+        result["interference"] = interference.summarize(
+            interference.measure(w.name, budgets=(0, 64, 16), n_rs=20, device=local, grads=gs))
 
     # end to end through the public API: pinned host inputs -> device -> fold + place -> host
     if not args.no_e2e:
@@ -423,12 +495,8 @@ def e2e(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world):
         one()
     e.record(stream)
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / K
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    ms = max_over_ranks(s.elapsed_time(e) / K, world, dev)
+    return {"value": round(whole_job_gbs(step_bytes, world, ms), 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "steps": K,
             "note": "pinned host grads+slots -> device, tide_rs_fold + tide_ag_place, shards+full params -> host"}
 

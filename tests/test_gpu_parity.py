@@ -61,11 +61,16 @@ def _check_canaries(buf, out, S):
     assert (tail == np.float32(CANARY)).all(), "wrote past S inside a slot"
 
 
+KERNELS = {"direct": dict(kernel=tide.TIDE_KERNEL_DIRECT),
+           "direct_dynamic": dict(kernel=tide.TIDE_KERNEL_DIRECT, sched=tide.TIDE_SCHED_DYNAMIC),
+           "bulk": dict(kernel=tide.TIDE_KERNEL_BULK)}
+
+
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("acc", [False, True])
 @pytest.mark.parametrize("alpha", ["1/W", 1.0])
-@pytest.mark.parametrize("sched", [tide.TIDE_SCHED_STATIC, tide.TIDE_SCHED_DYNAMIC])
-def test_toy_full_parity(acc, alpha, sched):
+@pytest.mark.parametrize("kname", sorted(KERNELS))
+def test_toy_full_parity(acc, alpha, kname):
     w = workloads.get(1)
     a = 1.0 / w.world if alpha == "1/W" else alpha
     dims = w.dim0_rownumel()
@@ -74,15 +79,16 @@ def test_toy_full_parity(acc, alpha, sched):
     init = workloads.make_out_init(w, S, device="cuda") if acc else None
     buf, out = _guarded_out(w.world, S, 5, init)
     before = out.clone()
-    _fold(w, gs.views, a, acc, out, sched=sched)
+    _fold(w, gs.views, a, acc, out, **KERNELS[kname])
     want = oracle_rs_full(w.world, dims, gs.views, a, acc, before)
-    assert_same_f32(out[:, :S].cpu().numpy(), want[:, :S], f"toy alpha={a} acc={acc} sched={sched}")
+    assert_same_f32(out[:, :S].cpu().numpy(), want[:, :S], f"toy alpha={a} acc={acc} {kname}")
     _check_canaries(buf, out, S)
 
 
 @pytest.mark.parametrize("world", [1, 2, 3, 5, 8, 16, 32])
 @pytest.mark.parametrize("chunk", [256, 0])
-def test_ragged_shapes(world, chunk):
+@pytest.mark.parametrize("kname", ["direct", "bulk"])
+def test_ragged_shapes(world, chunk, kname):
     rnd = random.Random(world * 101 + chunk)
     shapes = [(rnd.randint(1, 3 * world + 7), rnd.choice([1, 3, 8, 17, 64, 129])) for _ in range(5)]
     shapes += [(world * 37 + 5, 100), (rnd.randint(1, world), 7), (4099,)]
@@ -93,14 +99,15 @@ def test_ragged_shapes(world, chunk):
         init = torch.randn(world, S, device="cuda") if acc else None
         buf, out = _guarded_out(world, S, 3, init)
         before = out.clone()
-        _fold(w, gs.views, 1.0 / world, acc, out, chunk_bytes=chunk)
+        _fold(w, gs.views, 1.0 / world, acc, out, chunk_bytes=chunk, **KERNELS[kname])
         want = oracle_rs_full(world, dims, gs.views, 1.0 / world, acc, before)
-        assert_same_f32(out[:, :S].cpu().numpy(), want[:, :S], f"ragged W={world} chunk={chunk} acc={acc}")
+        assert_same_f32(out[:, :S].cpu().numpy(), want[:, :S], f"ragged W={world} chunk={chunk} acc={acc} {kname}")
         _check_canaries(buf, out, S)
 
 
 @pytest.mark.parametrize("case", ["uniform_phase", "mixed_phase", "odd_out", "odd_stride"])
-def test_misaligned(case):
+@pytest.mark.parametrize("kname", ["direct", "bulk"])
+def test_misaligned(case, kname):
     world, shapes = 4, [(67, 33), (9, 8), (130, 64), (5,)]
     rnd = random.Random(7)
     numels = [int(np.prod(s)) for s in shapes]
@@ -123,12 +130,13 @@ def test_misaligned(case):
     off = 1 if case == "odd_out" else 0
     out = base[off:off + world * stride].view(world, stride)
     before = out.clone()
-    _fold(None, views, 0.25, False, out)
+    _fold(None, views, 0.25, False, out, **KERNELS[kname])
     want = oracle_rs_full(world, dims, views, 0.25, False, before)
-    assert_same_f32(out[:, :S].cpu().numpy(), want[:, :S], case)
+    assert_same_f32(out[:, :S].cpu().numpy(), want[:, :S], f"{case} {kname}")
 
 
-def test_special_values():
+@pytest.mark.parametrize("kname", ["direct", "bulk"])
+def test_special_values(kname):
     world, shapes = 5, [(41, 24), (13,), (7, 9)]
     specials = np.array([np.nan, np.inf, -np.inf, -0.0, 0.0, 2.0 ** -133, -(2.0 ** -130), 3.3895e38, -3.3895e38,
                          1.0, 2.0 ** -24], dtype=np.float32)
@@ -148,13 +156,14 @@ def test_special_values():
         init = torch.from_numpy(rng.choice(specials, size=(world, S))).cuda() if acc else None
         buf, out = _guarded_out(world, S, 0, init)
         before = out.clone()
-        _fold(w, gs.views, 1.0, acc, out)
+        _fold(w, gs.views, 1.0, acc, out, **KERNELS[kname])
         want = oracle_rs_full(world, dims, gs.views, 1.0, acc, before)
-        assert_same_f32(out.cpu().numpy(), want, f"special values acc={acc}")
+        assert_same_f32(out.cpu().numpy(), want, f"special values acc={acc} {kname}")
 
 
 @pytest.mark.parametrize("world", [2, 3, 8, 32])
-def test_order_probe(world):
+@pytest.mark.parametrize("kname", ["direct", "bulk"])
+def test_order_probe(world, kname):
     """Closed form: 1.0 on rank 0 and 2^-24 elsewhere sums to exactly 1.0 in
     rank order; 1.0 on the last rank gives round(1 + (W-1) 2^-24)."""
     n = 4096 + 3
@@ -162,8 +171,7 @@ def test_order_probe(world):
         grads = [[torch.full((n,), 1.0 if u == big_rank else 2.0 ** -24, device="cuda").to(torch.bfloat16)]
                  for u in range(world)]
         out = torch.zeros(world, -(-n // world), device="cuda")
-        _fold(None, grads, 1.0, False, out)
-        R = -(-n // world)
+        _fold(None, grads, 1.0, False, out, **KERNELS[kname])
         flat = out.reshape(-1)[:n].cpu().numpy()
         assert_same_f32(flat, np.full(n, expect, np.float32), f"order probe W={world} big={big_rank}")
 
@@ -175,7 +183,9 @@ def test_determinism_across_launch_shapes():
     ref = None
     for kw in ({}, {"cta_budget": 1}, {"cta_budget": 3}, {"cta_budget": 152}, {"chunk_bytes": 256},
                {"chunk_bytes": 65536}, {"sched": tide.TIDE_SCHED_DYNAMIC, "cta_budget": 7},
-               {"sched": tide.TIDE_SCHED_DYNAMIC, "chunk_bytes": 512}):
+               {"sched": tide.TIDE_SCHED_DYNAMIC, "chunk_bytes": 512},
+               {"kernel": tide.TIDE_KERNEL_BULK}, {"kernel": tide.TIDE_KERNEL_BULK, "cta_budget": 5},
+               {"kernel": tide.TIDE_KERNEL_BULK, "chunk_bytes": 512}):
         out = torch.zeros(w.world, S, device="cuda")
         _fold(w, gs.views, 0.25, False, out, **kw)
         got = out.cpu().numpy()
@@ -183,6 +193,29 @@ def test_determinism_across_launch_shapes():
             ref = got
         else:
             assert_same_f32(got, ref, f"launch shape {kw}")
+
+
+def test_bulk_wait_timeout_reports_status():
+    """A bounded device-side wait that expires is reported as TIMEOUT and the
+    context stays usable: CTA 0 of the bulk kernel skips its first stage fill
+    (debug flag), its consumers give up after 50 ms, the producer drains the
+    copies it issued, and the kernel returns."""
+    w = workloads.get(1)
+    gs = workloads.make_grads(w, device="cuda")
+    _, _, S = oracle.geometry(w.world, w.dim0_rownumel())
+    flags = tide.make_flags(kernel=tide.TIDE_KERNEL_BULK,
+                            debug=tide.TIDE_DEBUG_SHORT_WAIT | tide.TIDE_DEBUG_SKIP_FILL)
+    out = torch.zeros(w.world, S, device="cuda")
+    with tide.Plan(gs.views, flags) as plan:
+        plan.rs_fold(out, alpha=0.25)
+        torch.cuda.synchronize()
+        assert plan.device_status() == tide.TIDE_ERR_TIMEOUT
+        assert plan.device_status() == tide.TIDE_OK  # reading clears the word
+    # the context is healthy: a normal fold still matches the oracle
+    out = torch.zeros(w.world, S, device="cuda")
+    _fold(w, gs.views, 0.25, False, out, kernel=tide.TIDE_KERNEL_BULK)
+    want = oracle_rs_full(w.world, w.dim0_rownumel(), gs.views, 0.25, False, torch.zeros(w.world, S))
+    assert_same_f32(out.cpu().numpy(), want, "after timeout")
 
 
 def test_repeated_calls_and_rebind():

@@ -135,13 +135,23 @@ WORKLOADS: Tuple[Workload, ...] = (
     _qwen3_moe_layer(),
 )
 
-BY_NAME = {w.name: w for w in WORKLOADS}
+# A reduced case of the Llama-3.1-8B block (its attention projections and
+# norms only, ~0.7 GB of gradients) for full-set profiler captures, which
+# replay a kernel dozens of times and so want a few GB on the device at most.
+PROFILE_CASES: Tuple[Workload, ...] = (
+    Workload(6, "llama3.1_8b_attn", 8,
+             ("q_proj", "k_proj", "v_proj", "o_proj", "input_layernorm", "post_attention_layernorm"),
+             ((4096, 4096), (1024, 4096), (1024, 4096), (4096, 4096), (4096,), (4096,)),
+             sigma=1e-3, outlier_rate=1e-3, outlier_scale=100.0),
+)
+
+BY_NAME = {w.name: w for w in WORKLOADS + PROFILE_CASES}
 
 
 def get(key) -> Workload:
     """Workload by 1-based index or by name."""
     if isinstance(key, int):
-        return WORKLOADS[key - 1]
+        return (WORKLOADS + PROFILE_CASES)[key - 1]
     return BY_NAME[key]
 
 
