@@ -327,13 +327,20 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)));
 }
 
 __device__ __forceinline__ uint4 lds_v4(const uint16_t *p)
 {
     return *reinterpret_cast<const uint4 *>(p);
+}
+
+// Shared-memory layout of the bulk kernel: STAGES full + STAGES empty
+// mbarriers, the abort flag, the producer's W source pointers, then the
+// 128-byte aligned stage ring.
+__host__ __device__ constexpr size_t bulk_ring_offset(int stages, int world)
+{
+    return ((size_t(2 * stages + 1) * 8 + size_t(world) * 8 + 127) / 128) * 128;
 }
 
 constexpr int32_t kStatusConsumerTimeout = 1;
@@ -363,7 +370,8 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + STAGES;
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(empty + STAGES);
-    uint16_t *ring = reinterpret_cast<uint16_t *>(smem + ((size_t(2 * STAGES) * 8 + 8 + 127) / 128) * 128);
+    const uint16_t **src_cache = reinterpret_cast<const uint16_t **>(empty + STAGES + 1);  // producer's W pointers
+    uint16_t *ring = reinterpret_cast<uint16_t *>(smem + bulk_ring_offset(STAGES, W));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float alpha = fp.alpha;
 
@@ -391,6 +399,9 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
                 continue;
             const int64_t count = int64_t(item.count_kind & ~kItemPad);
             const uint64_t *bp = fp.ptrs + int64_t(seg.param) * W;
+            const int64_t base = seg.src_elem + item.begin;
+            for (int u = 0; u < W; ++u)
+                src_cache[u] = reinterpret_cast<const uint16_t *>(bp[u]) + base;
             for (int64_t c = 0; c < count; c += FILL) {
                 const int64_t len = count - c < FILL ? count - c : FILL;
                 const uint32_t bytes = uint32_t(len & ~int64_t(7)) * 2u;
@@ -407,10 +418,9 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
                     mbar_arrive_expect_tx(&full[stage], uint32_t(W) * bytes);
                     if (bytes) {
                         uint16_t *dst = ring + size_t(stage) * W * FILL;
-                        const int64_t off = seg.src_elem + item.begin + c;
+#pragma unroll 4
                         for (int u = 0; u < W; ++u)
-                            bulk_copy_g2s(dst + size_t(u) * FILL, reinterpret_cast<const uint16_t *>(bp[u]) + off,
-                                          bytes, &full[stage]);
+                            bulk_copy_g2s(dst + size_t(u) * FILL, src_cache[u] + c, bytes, &full[stage]);
                     }
                 }
                 ++fills;
@@ -507,16 +517,20 @@ FoldKernel pick_bulk(int world)
 
 }  // namespace
 
-BulkShape bulk_shape(int world)
+BulkShape bulk_shape(int world, int64_t fill_elems)
 {
-    // Fills of >= 1 KB per rank while a stage stays within 32 KB; smaller
-    // fills only for very wide groups.
+    // Default: fills of >= 1 KB per rank while a stage stays within 32 KB;
+    // smaller fills only for very wide groups.
     BulkShape b{};
     int64_t fill = 8192 / world;
     if (fill < 512)
         fill = 512;
     if (fill * world * 2 > 32768)
         fill = 32768 / (2 * int64_t(world));
+    if (fill_elems > 0)
+        fill = fill_elems;
+    while (fill > 8 && fill * world * 2 * 2 > 200 * 1024)  // two stages must fit in shared memory
+        fill /= 2;
     fill &= ~int64_t(7);
     if (fill < 8)
         fill = 8;
@@ -528,14 +542,14 @@ BulkShape bulk_shape(int world)
         stages = 2;
     b.fill_elems = int32_t(fill);
     b.stages = int32_t(stages);
-    b.smem_bytes = size_t(((2 * stages * 8 + 8 + 127) / 128) * 128 + stages * stage_bytes);
+    b.smem_bytes = bulk_ring_offset(int(stages), world) + size_t(stages * stage_bytes);
     return b;
 }
 
-size_t fold_smem_bytes(int kernel, int world, int64_t /*chunk_elems*/)
+size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems)
 {
     if (kernel == TIDE_KERNEL_BULK)
-        return bulk_shape(world).smem_bytes;
+        return bulk_shape(world, fill_elems).smem_bytes;
     return size_t(world) * sizeof(uint64_t);
 }
 

@@ -75,7 +75,7 @@ struct BulkShape {
     int32_t stages;
     size_t smem_bytes;
 };
-BulkShape bulk_shape(int world);
+BulkShape bulk_shape(int world, int64_t fill_elems);  // fill_elems 0 = sized from the world
 
 struct AgParams {
     const Seg *segs;
@@ -92,7 +92,7 @@ struct AgParams {
 cudaError_t launch_fold(const FoldParams &fp, int kernel, int accumulate, int grid, int block, size_t smem,
                         cudaStream_t stream);
 cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *blocks_per_sm);
-size_t fold_smem_bytes(int kernel, int world, int64_t chunk_elems);
+size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems);
 cudaError_t launch_ag(const AgParams &ap, int grid, cudaStream_t stream);
 
 extern std::atomic<uint64_t> g_launches;

@@ -69,9 +69,12 @@ int32_t piece_phase(const uint64_t *ptrs_p, int32_t W, int64_t src_elem)
 
 tide_status_t check_flags(const tide_plan_flags_t &f)
 {
-    for (int i = 0; i < 5; ++i)
+    for (int i = 0; i < 4; ++i)
         if (f.reserved[i] != 0)
             return fail(TIDE_ERR_INVALID_ARG, "flags.reserved[%d] must be zero", i);
+    if (f.fill_bytes != 0 && (f.fill_bytes < 16 || f.fill_bytes % 16 != 0 || f.fill_bytes > 65536))
+        return fail(TIDE_ERR_INVALID_ARG, "flags.fill_bytes %d: need 0 or a multiple of 16 in [16, 65536]",
+                    f.fill_bytes);
     if (f.cta_budget < 0)
         return fail(TIDE_ERR_INVALID_ARG, "flags.cta_budget %d < 0", f.cta_budget);
     if (f.chunk_bytes != 0 && (f.chunk_bytes < 256 || f.chunk_bytes % 256 != 0 || f.chunk_bytes > (1 << 26)))
@@ -338,7 +341,7 @@ tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_para
         return bail(fail(TIDE_ERR_UNSUPPORTED, "too many work items; raise chunk_bytes"));
 
     plan->block = plan->kernel == TIDE_KERNEL_BULK ? tide::kBulkThreads : tide::kFoldThreads;
-    plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, CH);
+    plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, f.fill_bytes / 2);
     if (plan->host_only) {
         plan->grid = f.cta_budget ? f.cta_budget : 0;
         *plan_out = plan;
@@ -476,7 +479,7 @@ tide_status_t tide_rs_fold(tide_plan_t *plan, float *out_base, int64_t out_slot_
     fp.status = plan->d_status;
     fp.debug = plan->flags.debug;
     fp.wait_budget_ns = (plan->flags.debug & TIDE_DEBUG_SHORT_WAIT) ? tide::kShortWaitBudgetNs : tide::kWaitBudgetNs;
-    const tide::BulkShape bs = tide::bulk_shape(plan->world);
+    const tide::BulkShape bs = tide::bulk_shape(plan->world, plan->flags.fill_bytes / 2);
     fp.fill_elems = bs.fill_elems;
     fp.stages = bs.stages;
     const int grid = int(std::min<int64_t>(plan->grid, fp.n_items));

@@ -131,7 +131,9 @@ typedef struct {
     int32_t kernel;       /* TIDE_KERNEL_* */
     int32_t grad_dtype;   /* TIDE_DTYPE_* */
     uint32_t debug;       /* TIDE_DEBUG_* bits */
-    int32_t reserved[5];  /* must be zero */
+    int32_t fill_bytes;   /* bulk kernel: bf16 bytes per rank in one shared-memory stage fill
+                             (multiple of 16, at most 65536); 0 = sized from the world */
+    int32_t reserved[4];  /* must be zero */
 } tide_plan_flags_t;
 
 /* Read-only view of one (parameter, rank) shard piece of a plan. */

@@ -135,6 +135,8 @@ def test_empty_group(tide):
     ("chunk", "TIDE_ERR_INVALID_ARG"), ("order", "TIDE_ERR_UNSUPPORTED"),
     ("dtype", "TIDE_ERR_UNSUPPORTED"), ("overflow", "TIDE_ERR_INVALID_ARG"),
     ("neg_offset", "TIDE_ERR_INVALID_ARG"), ("sched", "TIDE_ERR_INVALID_ARG"),
+    ("fill", "TIDE_ERR_INVALID_ARG"), ("bulk_dynamic", "TIDE_ERR_UNSUPPORTED"),
+    ("skip_fill_direct", "TIDE_ERR_INVALID_ARG"), ("debug_bits", "TIDE_ERR_INVALID_ARG"),
 ])
 def test_build_validation(tide, case, status):
     W, dims = 4, [(8, 8), (5, 1)]
@@ -165,7 +167,18 @@ def test_build_validation(tide, case, status):
         offsets = [-2, -1]
     elif case == "sched":
         kw["sched"] = 9
-    flags = tide.make_flags(debug=tide.TIDE_DEBUG_HOST_ONLY, **kw)
+    elif case == "fill":
+        kw["fill_bytes"] = 24
+    elif case == "bulk_dynamic":
+        kw.update(kernel=tide.TIDE_KERNEL_BULK, sched=tide.TIDE_SCHED_DYNAMIC)
+    elif case == "skip_fill_direct":
+        kw.update(kernel=tide.TIDE_KERNEL_DIRECT)
+    flags_debug = tide.TIDE_DEBUG_HOST_ONLY
+    if case == "skip_fill_direct":
+        flags_debug |= tide.TIDE_DEBUG_SKIP_FILL
+    if case == "debug_bits":
+        flags_debug |= 0x100
+    flags = tide.make_flags(debug=flags_debug, **kw)
     if case == "reserved":
         flags.reserved[2] = 1
     params = [(ptrs[p], d, k, -1 if offsets is None else offsets[p]) for p, (d, k) in enumerate(dims)]
