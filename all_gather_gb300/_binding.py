@@ -52,7 +52,8 @@ class ParamDesc(ctypes.Structure):
 class PlanFlags(ctypes.Structure):
     _fields_ = [("cta_budget", ctypes.c_int32), ("chunk_bytes", ctypes.c_int32), ("order", ctypes.c_int32),
                 ("sched", ctypes.c_int32), ("kernel", ctypes.c_int32), ("grad_dtype", ctypes.c_int32),
-                ("debug", ctypes.c_uint32), ("fill_bytes", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+                ("debug", ctypes.c_uint32), ("fill_bytes", ctypes.c_int32), ("fill_ranks", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 3)]
 
 
 class Segment(ctypes.Structure):
@@ -130,10 +131,11 @@ def _descs(params: Sequence[Tuple[Sequence[int], int, int, int]]):
 
 
 def make_flags(cta_budget=0, chunk_bytes=0, order=TIDE_ORDER_RANK_ASC, sched=TIDE_SCHED_STATIC,
-               kernel=TIDE_KERNEL_AUTO, grad_dtype=TIDE_DTYPE_BF16, debug=0, fill_bytes=0) -> PlanFlags:
+               kernel=TIDE_KERNEL_AUTO, grad_dtype=TIDE_DTYPE_BF16, debug=0, fill_bytes=0,
+               fill_ranks=0) -> PlanFlags:
     f = PlanFlags()
     f.cta_budget, f.chunk_bytes, f.order, f.sched = cta_budget, chunk_bytes, order, sched
-    f.kernel, f.grad_dtype, f.debug, f.fill_bytes = kernel, grad_dtype, debug, fill_bytes
+    f.kernel, f.grad_dtype, f.debug, f.fill_bytes, f.fill_ranks = kernel, grad_dtype, debug, fill_bytes, fill_ranks
     return f
 
 

@@ -79,6 +79,43 @@ __device__ __forceinline__ void store8(float *d, const float (&acc)[8], float al
     }
 }
 
+__device__ __forceinline__ void load8(const float *d, float (&o)[8], bool vec)
+{
+    if (vec) {
+        const float4 a = __ldcs(reinterpret_cast<const float4 *>(d));
+        const float4 b = __ldcs(reinterpret_cast<const float4 *>(d) + 1);
+        o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+        o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            o[e] = __ldcs(d + e);
+    }
+}
+
+// y = alpha * acc, then old + y when accumulating (old already loaded).
+template <bool ACC>
+__device__ __forceinline__ void store8_onto(float *d, const float (&acc)[8], const float (&old)[8], float alpha,
+                                            bool vec)
+{
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        y[e] = __fmul_rn(alpha, acc[e]);
+        if (ACC)
+            y[e] = __fadd_rn(old[e], y[e]);
+    }
+    if (vec) {
+        float4 *d4 = reinterpret_cast<float4 *>(d);
+        __stcs(d4, make_float4(y[0], y[1], y[2], y[3]));
+        __stcs(d4 + 1, make_float4(y[4], y[5], y[6], y[7]));
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            __stcs(d + e, y[e]);
+    }
+}
+
 // One element by scalar loads (misaligned heads, tails and pieces).
 template <int WT, bool ACC>
 __device__ __forceinline__ void fold_scalar(const uint64_t *s_src, int W, int64_t e, float *dst, float alpha)
@@ -343,6 +380,9 @@ __host__ __device__ constexpr size_t bulk_ring_offset(int stages, int world)
     return ((size_t(2 * stages + 1) * 8 + size_t(world) * 8 + 127) / 128) * 128;
 }
 
+constexpr int kBulkMaxVec = 2;                               // vectors per consumer thread per chunk
+constexpr int64_t kBulkMaxFill = 8 * kBulkMaxVec * 32 * kBulkConsumerWarps;  // 2048 elements
+
 constexpr int32_t kStatusConsumerTimeout = 1;
 constexpr int32_t kStatusProducerTimeout = 2;
 constexpr int32_t kStatusDrainTimeout = 3;
@@ -365,6 +405,8 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
 {
     extern __shared__ __align__(128) unsigned char smem[];
     const int W = WT > 0 ? WT : fp.world;
+    const int RG = fp.fill_ranks;          // ranks per stage fill
+    const int NG = (W + RG - 1) / RG;      // fills per chunk of FILL elements
     const int STAGES = fp.stages;
     const int64_t FILL = fp.fill_elems;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -389,6 +431,8 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
         if (lane != 0)
             return;
         // ------------------------------------------------------------ producer
+        // For every chunk of FILL elements of a work item, NG stage fills of
+        // RG ranks each, in rank order.
         uint32_t stage = 0, phase = 0;
         int64_t fills = 0, skipped = -1;
         bool stop = false;
@@ -402,31 +446,35 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
             const int64_t base = seg.src_elem + item.begin;
             for (int u = 0; u < W; ++u)
                 src_cache[u] = reinterpret_cast<const uint16_t *>(bp[u]) + base;
-            for (int64_t c = 0; c < count; c += FILL) {
+            for (int64_t c = 0; c < count && !stop; c += FILL) {
                 const int64_t len = count - c < FILL ? count - c : FILL;
                 const uint32_t bytes = uint32_t(len & ~int64_t(7)) * 2u;
-                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, fp.wait_budget_ns, abort_flag)) {
-                    if (!*abort_flag)
-                        atomicExch(fp.status, kStatusProducerTimeout);
-                    *abort_flag = 1;
-                    stop = true;
-                    break;
-                }
-                if ((fp.debug & TIDE_DEBUG_SKIP_FILL) && blockIdx.x == 0 && fills == 0) {
-                    skipped = fills;  // leave this stage unfilled: its consumers' wait expires
-                } else {
-                    mbar_arrive_expect_tx(&full[stage], uint32_t(W) * bytes);
-                    if (bytes) {
-                        uint16_t *dst = ring + size_t(stage) * W * FILL;
-#pragma unroll 4
-                        for (int u = 0; u < W; ++u)
-                            bulk_copy_g2s(dst + size_t(u) * FILL, src_cache[u] + c, bytes, &full[stage]);
+                for (int g = 0; g < NG; ++g) {
+                    const int u0 = g * RG;
+                    const int nr = W - u0 < RG ? W - u0 : RG;
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, fp.wait_budget_ns, abort_flag)) {
+                        if (!*abort_flag)
+                            atomicExch(fp.status, kStatusProducerTimeout);
+                        *abort_flag = 1;
+                        stop = true;
+                        break;
                     }
-                }
-                ++fills;
-                if (++stage == uint32_t(STAGES)) {
-                    stage = 0;
-                    phase ^= 1u;
+                    if ((fp.debug & TIDE_DEBUG_SKIP_FILL) && blockIdx.x == 0 && fills == 0) {
+                        skipped = fills;  // leave this stage unfilled: its consumers' wait expires
+                    } else {
+                        mbar_arrive_expect_tx(&full[stage], uint32_t(nr) * bytes);
+                        if (bytes) {
+                            uint16_t *dst = ring + size_t(stage) * RG * FILL;
+#pragma unroll 4
+                            for (int j = 0; j < nr; ++j)
+                                bulk_copy_g2s(dst + size_t(j) * FILL, src_cache[u0 + j] + c, bytes, &full[stage]);
+                        }
+                    }
+                    ++fills;
+                    if (++stage == uint32_t(STAGES)) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
         }
@@ -443,6 +491,9 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
     }
 
     // ---------------------------------------------------------------- consumers
+    // Each consumer thread owns up to kBulkMaxVec 8-element vectors of a
+    // chunk and keeps their fp32 sums in registers across the chunk's NG
+    // fills, so the ranks are added in order 0, 1, ..., W-1.
     const int ctid = threadIdx.x - 32;
     constexpr int NCT = 32 * kBulkConsumerWarps;
     uint32_t stage = 0, phase = 0;
@@ -467,36 +518,64 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
         const bool dst_vec = (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
         for (int64_t c = 0; c < count; c += FILL) {
             const int64_t len = count - c < FILL ? count - c : FILL;
-            if (!mbar_wait_bounded(&full[stage], phase, fp.wait_budget_ns, abort_flag)) {
-                if (!*abort_flag)
-                    atomicExch(fp.status, kStatusConsumerTimeout);
-                *abort_flag = 1;
-                return;
-            }
-            const uint16_t *sb = ring + size_t(stage) * W * FILL;
             const int64_t nv = len >> 3;
-            for (int64_t v = ctid; v < nv; v += NCT) {
-                float acc[8];
-                unpack8(lds_v4(sb + v * 8), acc);
-#pragma unroll 8
-                for (int u = 1; u < (WT > 0 ? WT : W); ++u) {
-                    float f[8];
-                    unpack8(lds_v4(sb + size_t(u) * FILL + v * 8), f);
+            float acc[kBulkMaxVec][8];
+            float old[kBulkMaxVec][8];
+            if (ACC) {
+                // Issue the loads of the existing shard values before waiting
+                // for the chunk's fills, so their latency overlaps the copies.
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        acc[e] = __fadd_rn(acc[e], f[e]);
+                for (int k = 0; k < kBulkMaxVec; ++k) {
+                    const int64_t v = ctid + int64_t(k) * NCT;
+                    if (v < nv)
+                        load8(dst + c + v * 8, old[k], dst_vec);
                 }
-                store8<ACC>(dst + c + v * 8, acc, alpha, dst_vec);
+            }
+            for (int g = 0; g < NG; ++g) {
+                const int u0 = g * RG;
+                const int nr = W - u0 < RG ? W - u0 : RG;
+                if (!mbar_wait_bounded(&full[stage], phase, fp.wait_budget_ns, abort_flag)) {
+                    if (!*abort_flag)
+                        atomicExch(fp.status, kStatusConsumerTimeout);
+                    *abort_flag = 1;
+                    return;
+                }
+                const uint16_t *sb = ring + size_t(stage) * RG * FILL;
+#pragma unroll
+                for (int k = 0; k < kBulkMaxVec; ++k) {
+                    const int64_t v = ctid + int64_t(k) * NCT;
+                    if (v < nv) {
+                        int j0 = 0;
+                        if (g == 0) {
+                            unpack8(lds_v4(sb + v * 8), acc[k]);
+                            j0 = 1;
+                        }
+#pragma unroll 4
+                        for (int j = j0; j < nr; ++j) {
+                            float f[8];
+                            unpack8(lds_v4(sb + size_t(j) * FILL + v * 8), f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                acc[k][e] = __fadd_rn(acc[k][e], f[e]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&empty[stage]);
+                if (++stage == uint32_t(STAGES)) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kBulkMaxVec; ++k) {
+                const int64_t v = ctid + int64_t(k) * NCT;
+                if (v < nv)
+                    store8_onto<ACC>(dst + c + v * 8, acc[k], old[k], alpha, dst_vec);
             }
             for (int64_t e = nv * 8 + ctid; e < len; e += NCT)
                 fold_scalar_global<WT, ACC>(bp, W, seg.src_elem + item.begin + c + e, dst + c + e, alpha);
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&empty[stage]);
-            if (++stage == uint32_t(STAGES)) {
-                stage = 0;
-                phase ^= 1u;
-            }
         }
     }
 }
@@ -517,39 +596,41 @@ FoldKernel pick_bulk(int world)
 
 }  // namespace
 
-BulkShape bulk_shape(int world, int64_t fill_elems)
+BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_sm)
 {
-    // Default: fills of >= 1 KB per rank while a stage stays within 32 KB;
-    // smaller fills only for very wide groups.
+    // Default: 4 KB of each of up to 8 ranks per stage fill (32 KB stages),
+    // three stages per CTA, two CTAs per SM.  Wider groups take several fills
+    // per chunk; the consumers keep the partial sums in registers meanwhile.
     BulkShape b{};
-    int64_t fill = 8192 / world;
-    if (fill < 512)
-        fill = 512;
-    if (fill * world * 2 > 32768)
-        fill = 32768 / (2 * int64_t(world));
-    if (fill_elems > 0)
-        fill = fill_elems;
-    while (fill > 8 && fill * world * 2 * 2 > 200 * 1024)  // two stages must fit in shared memory
-        fill /= 2;
+    int64_t fill = fill_elems > 0 ? fill_elems : 2048;
+    if (fill > kBulkMaxFill)
+        fill = kBulkMaxFill;
     fill &= ~int64_t(7);
     if (fill < 8)
         fill = 8;
-    const int64_t stage_bytes = fill * world * 2;
-    int64_t stages = kBulkSmemTarget / stage_bytes;
-    if (stages > 8)
-        stages = 8;
+    int rg = fill_ranks > 0 ? fill_ranks : 8;
+    if (rg > world)
+        rg = world;
+    while (fill > 8 && fill * rg * 2 * 2 > 200 * 1024)  // two stages must fit in shared memory
+        fill = (fill / 2) & ~int64_t(7);
+    const int64_t stage_bytes = fill * rg * 2;
+    // A CTA that has an SM to itself (small CTA budgets) takes twice the ring.
+    int64_t stages = (whole_sm ? 2 * kBulkSmemTarget : kBulkSmemTarget) / stage_bytes;
+    if (stages > 16)
+        stages = 16;
     if (stages < 2)
         stages = 2;
     b.fill_elems = int32_t(fill);
+    b.fill_ranks = rg;
     b.stages = int32_t(stages);
     b.smem_bytes = bulk_ring_offset(int(stages), world) + size_t(stages * stage_bytes);
     return b;
 }
 
-size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems)
+size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems, int fill_ranks, bool whole_sm)
 {
     if (kernel == TIDE_KERNEL_BULK)
-        return bulk_shape(world, fill_elems).smem_bytes;
+        return bulk_shape(world, fill_elems, fill_ranks, whole_sm).smem_bytes;
     return size_t(world) * sizeof(uint64_t);
 }
 

@@ -66,16 +66,19 @@ struct FoldParams {
     // bulk kernel only
     uint64_t wait_budget_ns;  // bound on every mbarrier wait
     int32_t fill_elems;       // elements per rank per stage fill (multiple of 8)
+    int32_t fill_ranks;       // ranks per stage fill
     int32_t stages;           // ring depth
 };
 
 // Stage geometry of the bulk kernel for a world size.
 struct BulkShape {
     int32_t fill_elems;
+    int32_t fill_ranks;
     int32_t stages;
     size_t smem_bytes;
 };
-BulkShape bulk_shape(int world, int64_t fill_elems);  // fill_elems 0 = sized from the world
+// fill_elems / fill_ranks 0 = default; whole_sm: the grid has at most one CTA per SM
+BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_sm);
 
 struct AgParams {
     const Seg *segs;
@@ -92,7 +95,7 @@ struct AgParams {
 cudaError_t launch_fold(const FoldParams &fp, int kernel, int accumulate, int grid, int block, size_t smem,
                         cudaStream_t stream);
 cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *blocks_per_sm);
-size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems);
+size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems, int fill_ranks, bool whole_sm);
 cudaError_t launch_ag(const AgParams &ap, int grid, cudaStream_t stream);
 
 extern std::atomic<uint64_t> g_launches;
@@ -114,6 +117,7 @@ struct tide_plan {
     int32_t grid = 0, block = 0, sms = 0;
     size_t fold_smem = 0;
     int kernel = TIDE_KERNEL_DIRECT;
+    bool whole_sm = false;               // bulk kernel: at most one CTA per SM (deeper ring)
     bool host_only = false;
     int device = -1;
     uintptr_t src_lo = 0, src_hi = 0;    // hull of all gradient ranges

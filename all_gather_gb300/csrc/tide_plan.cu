@@ -69,12 +69,14 @@ int32_t piece_phase(const uint64_t *ptrs_p, int32_t W, int64_t src_elem)
 
 tide_status_t check_flags(const tide_plan_flags_t &f)
 {
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 3; ++i)
         if (f.reserved[i] != 0)
             return fail(TIDE_ERR_INVALID_ARG, "flags.reserved[%d] must be zero", i);
-    if (f.fill_bytes != 0 && (f.fill_bytes < 16 || f.fill_bytes % 16 != 0 || f.fill_bytes > 65536))
-        return fail(TIDE_ERR_INVALID_ARG, "flags.fill_bytes %d: need 0 or a multiple of 16 in [16, 65536]",
+    if (f.fill_bytes != 0 && (f.fill_bytes < 16 || f.fill_bytes % 16 != 0 || f.fill_bytes > 4096))
+        return fail(TIDE_ERR_INVALID_ARG, "flags.fill_bytes %d: need 0 or a multiple of 16 in [16, 4096]",
                     f.fill_bytes);
+    if (f.fill_ranks < 0 || f.fill_ranks > tide::kMaxWorld)
+        return fail(TIDE_ERR_INVALID_ARG, "flags.fill_ranks %d", f.fill_ranks);
     if (f.cta_budget < 0)
         return fail(TIDE_ERR_INVALID_ARG, "flags.cta_budget %d < 0", f.cta_budget);
     if (f.chunk_bytes != 0 && (f.chunk_bytes < 256 || f.chunk_bytes % 256 != 0 || f.chunk_bytes > (1 << 26)))
@@ -251,7 +253,9 @@ tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_para
     plan->flags = f;
     plan->host_only = (f.debug & TIDE_DEBUG_HOST_ONLY) != 0;
     plan->chunk_elems = (f.chunk_bytes ? f.chunk_bytes : tide::kDefaultChunkBytes) / 2;
-    plan->kernel = f.kernel == TIDE_KERNEL_AUTO ? TIDE_KERNEL_DIRECT : f.kernel;
+    plan->kernel = f.kernel == TIDE_KERNEL_AUTO ? TIDE_KERNEL_BULK : f.kernel;
+    if (f.kernel == TIDE_KERNEL_AUTO && f.sched == TIDE_SCHED_DYNAMIC)
+        plan->kernel = TIDE_KERNEL_DIRECT;  // only the direct kernel claims items dynamically
 
     // --- geometry (Section 2.1): R_p = ceil(D_p / W), o_p, S -------------
     plan->dim0.resize(num_params);
@@ -341,7 +345,7 @@ tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_para
         return bail(fail(TIDE_ERR_UNSUPPORTED, "too many work items; raise chunk_bytes"));
 
     plan->block = plan->kernel == TIDE_KERNEL_BULK ? tide::kBulkThreads : tide::kFoldThreads;
-    plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, f.fill_bytes / 2);
+    plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, f.fill_bytes / 2, f.fill_ranks, false);
     if (plan->host_only) {
         plan->grid = f.cta_budget ? f.cta_budget : 0;
         *plan_out = plan;
@@ -356,6 +360,10 @@ tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_para
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, plan->device);
     if (e != cudaSuccess)
         return bail(cuda_fail(e, "query SM count"));
+    plan->sms = sms;
+    plan->whole_sm = plan->kernel == TIDE_KERNEL_BULK && f.cta_budget > 0 && f.cta_budget <= sms;
+    if (plan->whole_sm)
+        plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, f.fill_bytes / 2, f.fill_ranks, true);
     int per_sm = 0;
     e = tide::fold_occupancy(plan->kernel, world, plan->block, plan->fold_smem, &per_sm);
     if (e != cudaSuccess)
@@ -363,7 +371,6 @@ tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_para
     if (per_sm < 1)
         return bail(fail(TIDE_ERR_UNSUPPORTED, "fold kernel does not fit on an SM (world %d)", world));
     plan->grid = f.cta_budget ? f.cta_budget : sms * per_sm;
-    plan->sms = sms;
 
     size_t off = 0;
     auto carve = [&](size_t bytes) {
@@ -479,8 +486,10 @@ tide_status_t tide_rs_fold(tide_plan_t *plan, float *out_base, int64_t out_slot_
     fp.status = plan->d_status;
     fp.debug = plan->flags.debug;
     fp.wait_budget_ns = (plan->flags.debug & TIDE_DEBUG_SHORT_WAIT) ? tide::kShortWaitBudgetNs : tide::kWaitBudgetNs;
-    const tide::BulkShape bs = tide::bulk_shape(plan->world, plan->flags.fill_bytes / 2);
+    const tide::BulkShape bs =
+        tide::bulk_shape(plan->world, plan->flags.fill_bytes / 2, plan->flags.fill_ranks, plan->whole_sm);
     fp.fill_elems = bs.fill_elems;
+    fp.fill_ranks = bs.fill_ranks;
     fp.stages = bs.stages;
     const int grid = int(std::min<int64_t>(plan->grid, fp.n_items));
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);

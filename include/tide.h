@@ -96,7 +96,7 @@ enum {
 
 /* Reduce-scatter kernel family. */
 enum {
-    TIDE_KERNEL_AUTO = 0,    /* the library's default */
+    TIDE_KERNEL_AUTO = 0,    /* the library's default: BULK (DIRECT when sched is DYNAMIC) */
     TIDE_KERNEL_DIRECT = 1,  /* 16-byte vector loads of the W rank rows straight into registers */
     TIDE_KERNEL_BULK = 2     /* warp-specialised: bulk async copies (cp.async.bulk + mbarrier)
                                 stage the W rank rows in shared memory */
@@ -132,8 +132,10 @@ typedef struct {
     int32_t grad_dtype;   /* TIDE_DTYPE_* */
     uint32_t debug;       /* TIDE_DEBUG_* bits */
     int32_t fill_bytes;   /* bulk kernel: bf16 bytes per rank in one shared-memory stage fill
-                             (multiple of 16, at most 65536); 0 = sized from the world */
-    int32_t reserved[4];  /* must be zero */
+                             (multiple of 16, at most 4096); 0 = 4096 */
+    int32_t fill_ranks;   /* bulk kernel: ranks per stage fill (0 = min(W, 8)); wider groups take
+                             several fills per chunk, summed in registers in rank order */
+    int32_t reserved[3];  /* must be zero */
 } tide_plan_flags_t;
 
 /* Read-only view of one (parameter, rank) shard piece of a plan. */

@@ -63,7 +63,9 @@ def _check_canaries(buf, out, S):
 
 KERNELS = {"direct": dict(kernel=tide.TIDE_KERNEL_DIRECT),
            "direct_dynamic": dict(kernel=tide.TIDE_KERNEL_DIRECT, sched=tide.TIDE_SCHED_DYNAMIC),
-           "bulk": dict(kernel=tide.TIDE_KERNEL_BULK)}
+           "bulk": dict(kernel=tide.TIDE_KERNEL_BULK),
+           # tiny fills and odd rank groups: many stage fills per chunk, groups of 3, 3, ..., remainder
+           "bulk_groups": dict(kernel=tide.TIDE_KERNEL_BULK, fill_bytes=64, fill_ranks=3)}
 
 
 # ---------------------------------------------------------------------------
@@ -87,7 +89,7 @@ def test_toy_full_parity(acc, alpha, kname):
 
 @pytest.mark.parametrize("world", [1, 2, 3, 5, 8, 16, 32])
 @pytest.mark.parametrize("chunk", [256, 0])
-@pytest.mark.parametrize("kname", ["direct", "bulk"])
+@pytest.mark.parametrize("kname", ["direct", "bulk", "bulk_groups"])
 def test_ragged_shapes(world, chunk, kname):
     rnd = random.Random(world * 101 + chunk)
     shapes = [(rnd.randint(1, 3 * world + 7), rnd.choice([1, 3, 8, 17, 64, 129])) for _ in range(5)]
@@ -106,7 +108,7 @@ def test_ragged_shapes(world, chunk, kname):
 
 
 @pytest.mark.parametrize("case", ["uniform_phase", "mixed_phase", "odd_out", "odd_stride"])
-@pytest.mark.parametrize("kname", ["direct", "bulk"])
+@pytest.mark.parametrize("kname", ["direct", "bulk", "bulk_groups"])
 def test_misaligned(case, kname):
     world, shapes = 4, [(67, 33), (9, 8), (130, 64), (5,)]
     rnd = random.Random(7)
@@ -135,7 +137,7 @@ def test_misaligned(case, kname):
     assert_same_f32(out[:, :S].cpu().numpy(), want[:, :S], f"{case} {kname}")
 
 
-@pytest.mark.parametrize("kname", ["direct", "bulk"])
+@pytest.mark.parametrize("kname", ["direct", "bulk", "bulk_groups"])
 def test_special_values(kname):
     world, shapes = 5, [(41, 24), (13,), (7, 9)]
     specials = np.array([np.nan, np.inf, -np.inf, -0.0, 0.0, 2.0 ** -133, -(2.0 ** -130), 3.3895e38, -3.3895e38,
@@ -162,7 +164,7 @@ def test_special_values(kname):
 
 
 @pytest.mark.parametrize("world", [2, 3, 8, 32])
-@pytest.mark.parametrize("kname", ["direct", "bulk"])
+@pytest.mark.parametrize("kname", ["direct", "bulk", "bulk_groups"])
 def test_order_probe(world, kname):
     """Closed form: 1.0 on rank 0 and 2^-24 elsewhere sums to exactly 1.0 in
     rank order; 1.0 on the last rank gives round(1 + (W-1) 2^-24)."""
@@ -185,7 +187,10 @@ def test_determinism_across_launch_shapes():
                {"chunk_bytes": 65536}, {"sched": tide.TIDE_SCHED_DYNAMIC, "cta_budget": 7},
                {"sched": tide.TIDE_SCHED_DYNAMIC, "chunk_bytes": 512},
                {"kernel": tide.TIDE_KERNEL_BULK}, {"kernel": tide.TIDE_KERNEL_BULK, "cta_budget": 5},
-               {"kernel": tide.TIDE_KERNEL_BULK, "chunk_bytes": 512}):
+               {"kernel": tide.TIDE_KERNEL_BULK, "chunk_bytes": 512},
+               {"kernel": tide.TIDE_KERNEL_BULK, "fill_bytes": 16, "fill_ranks": 1},
+               {"kernel": tide.TIDE_KERNEL_BULK, "fill_bytes": 4096, "fill_ranks": 4},
+               {"kernel": tide.TIDE_KERNEL_BULK, "cta_budget": 9}):
         out = torch.zeros(w.world, S, device="cuda")
         _fold(w, gs.views, 0.25, False, out, **kw)
         got = out.cpu().numpy()
