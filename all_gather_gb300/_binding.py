@@ -34,7 +34,8 @@ TIDE_DEBUG_SKIP_FILL = 0x4
 
 EXPORTED = ("tide_plan_build", "tide_plan_rebind", "tide_rs_fold", "tide_ag_place", "tide_plan_destroy",
             "tide_plan_slot_numel", "tide_plan_num_segments", "tide_plan_segment", "tide_plan_fold_config",
-            "tide_last_device_status", "tide_launch_count", "tide_status_string", "tide_last_error")
+            "tide_last_device_status", "tide_launch_count", "tide_status_string", "tide_last_error",
+            "tide_rs_fold_noalloc")
 
 
 class TideError(RuntimeError):
@@ -102,6 +103,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tide_status_string.restype = ctypes.c_char_p
     lib.tide_last_error.argtypes = []
     lib.tide_last_error.restype = ctypes.c_char_p
+    lib.tide_rs_fold_noalloc.argtypes = [i32, i32, ctypes.POINTER(ParamDesc), vp, i64, ctypes.c_float, i32, vp]
+    lib.tide_rs_fold_noalloc.restype = st
     _lib = lib
     return lib
 
@@ -213,3 +216,12 @@ def tide_status_string(status: int) -> str:
 
 def tide_last_error() -> str:
     return load_library().tide_last_error().decode()
+
+
+def tide_rs_fold_noalloc(world: int, params, out_base: int, out_slot_stride: int, alpha: float, accumulate: int,
+                         stream: int = 0) -> None:
+    """The allocation-free fold: same arguments as tide_plan_build + tide_rs_fold, no plan."""
+    arr, _keep = _descs(params)
+    _check(load_library().tide_rs_fold_noalloc(world, len(params), arr, ctypes.c_void_p(out_base or None),
+                                               out_slot_stride, ctypes.c_float(alpha), int(accumulate),
+                                               ctypes.c_void_p(stream or None)), "tide_rs_fold_noalloc")

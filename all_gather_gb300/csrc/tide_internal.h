@@ -100,6 +100,11 @@ cudaError_t launch_ag(const AgParams &ap, int grid, cudaStream_t stream);
 
 extern std::atomic<uint64_t> g_launches;
 
+// Set the detail message tide_last_error() returns on this thread.  The
+// message is copied into a fixed per-thread buffer, so callers may rely on
+// it not allocating once the thread's buffer exists.
+void record_error(const char *msg);
+
 }  // namespace tide
 
 struct tide_plan {

@@ -685,3 +685,7 @@ tide_status_t tide_last_device_status(tide_plan_t *plan, void *stream_)
 }
 
 }  // extern "C"
+
+namespace tide {
+void record_error(const char *msg) { t_last_error = msg; }
+}  // namespace tide

@@ -44,6 +44,7 @@
 #ifndef TIDE_H
 #define TIDE_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -227,6 +228,41 @@ TIDE_API tide_status_t tide_last_device_status(tide_plan_t *plan, void *stream);
 
 /* Kernels this library has launched in this process (all plans, all calls). */
 TIDE_API uint64_t tide_launch_count(void);
+
+/*
+ * Allocation-free reduce-scatter fold, for callers that cannot allocate GPU
+ * memory.  The paper has no counterpart to this entry point.
+ *
+ * tide_plan_build allocates device tables with cudaMalloc.  Callers that run
+ * inside an allocator (an allocation hook or an out-of-memory handler), under
+ * a memory pool or cap that forbids new device allocations, or that must not
+ * leave allocations behind can use this call instead: it computes the same
+ * result as tide_plan_build + tide_rs_fold + tide_plan_destroy with default
+ * flags (bit for bit), but keeps its tables in one fixed device array owned
+ * by the library and calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ *   Arguments: as tide_plan_build's (world, num_params, params) followed by
+ *   tide_rs_fold's (out_base, out_slot_stride, alpha, accumulate, stream);
+ *   S is computed from params the same way; explicit shard offsets must be
+ *   given in increasing order (each at least the previous shard's end).
+ *   Limit: the call's tables (8 bytes per gradient pointer, 48 per
+ *   (parameter, rank) piece, 16 per work item of 8,192 elements, plus
+ *   alignment) must fit in TIDE_NOALLOC_SCRATCH_BYTES; larger requests return
+ *   TIDE_ERR_INVALID_ARG without doing anything.  All five of this library's
+ *   benchmark workloads fit (the largest needs about 2 MB).
+ *   Memory: the array occupies TIDE_NOALLOC_SCRATCH_BYTES on each GPU where
+ *   the library is used, until the process exits.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   with that device current; make that first call before any stream capture.
+ *   Sharing: every call uses the same array, which keeps the last call's
+ *   tables.  Calls that overlap on the GPU (different streams without an
+ *   ordering between them) race; calls on one stream are ordered.  Calls from
+ *   several host threads are serialised by a lock.
+ */
+#define TIDE_NOALLOC_SCRATCH_BYTES ((size_t)4 * 1024 * 1024)
+TIDE_API tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params, const tide_param_desc_t *params,
+                                            float *out_base, int64_t out_slot_stride, float alpha,
+                                            int32_t accumulate, void *stream);
 
 /* Human-readable name of a status code. */
 TIDE_API const char *tide_status_string(tide_status_t status);
