@@ -21,6 +21,9 @@ What each function follows (TIDE paper, "The Endgame of FSDP Communication"):
   optional accumulate), Section 4.
 * :func:`ag` -- Section 2.1, Equation (2): rank-major slots placed into
   per-parameter full tensors, padding dropped.
+* :func:`f32_to_bf16`, :func:`ag_cast` -- Section 3.1 (mixed-precision
+  groups cast fp32 master shards to bf16 for the all-gather): the same
+  placement from fp32 slots, each element rounded to nearest even.
 """
 from __future__ import annotations
 
@@ -75,6 +78,11 @@ class Oracle:
         lib.oracle_ag.argtypes = [ctypes.c_int32, ctypes.c_int32, _i64p, _i64p, _u16p, ctypes.c_int64,
                                   ctypes.POINTER(_u16p)]
         lib.oracle_ag.restype = ctypes.c_int
+        lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+        lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_ag_cast.argtypes = [ctypes.c_int32, ctypes.c_int32, _i64p, _i64p, _f32p, ctypes.c_int64,
+                                       ctypes.POINTER(_u16p)]
+        lib.oracle_ag_cast.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
 
@@ -162,6 +170,28 @@ class Oracle:
         return list(full)
 
 
+    def f32_to_bf16(self, x: float) -> int:
+        """Round-to-nearest-even binary32 -> bf16 bit pattern (one value)."""
+        return int(self.lib.oracle_f32_to_bf16(ctypes.c_float(x)))
+
+    def ag_cast(self, world: int, dims: Sequence[Tuple[int, int]], slots: np.ndarray,
+                full: Optional[Sequence[np.ndarray]] = None) -> List[np.ndarray]:
+        """Mixed-precision placement: slots float32 [W, stride] -> P flat uint16 bf16 tensors."""
+        P = len(dims)
+        slots = np.ascontiguousarray(slots, dtype=np.float32)
+        assert slots.ndim == 2 and slots.shape[0] == world
+        if full is None:
+            full = [np.zeros(d * k, dtype=np.uint16) for d, k in dims]
+        ptrs = (_u16p * max(P, 1))(*[f.ctypes.data_as(_u16p) for f in full])
+        d0 = np.array([d for d, _ in dims] or [0], dtype=np.int64)
+        kk = np.array([k for _, k in dims] or [0], dtype=np.int64)
+        rc = self.lib.oracle_ag_cast(world, P, d0.ctypes.data_as(_i64p), kk.ctypes.data_as(_i64p),
+                                     slots.ctypes.data_as(_f32p), slots.shape[1], ptrs)
+        if rc != 0:
+            raise ValueError(f"oracle_ag_cast failed ({rc})")
+        return list(full)
+
+
 _default: Optional[Oracle] = None
 
 
@@ -197,3 +227,11 @@ def rs(world, dims, grads, alpha, accumulate, out):
 
 def ag(world, dims, slots, full=None):
     return load().ag(world, dims, slots, full)
+
+
+def f32_to_bf16(x):
+    return load().f32_to_bf16(x)
+
+
+def ag_cast(world, dims, slots, full=None):
+    return load().ag_cast(world, dims, slots, full)

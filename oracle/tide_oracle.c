@@ -211,3 +211,67 @@ done:
     free(o);
     return rc;
 }
+
+/*
+ * Round-to-nearest-even narrowing of a binary32 value to bf16 (8 significant
+ * bits), written from the definition: keep the upper 16 bits, then look at
+ * the 16 discarded bits -- above one half of the last kept place round up,
+ * below it truncate, exactly one half round to the even neighbour.  A carry
+ * out of the mantissa moves into the exponent, which turns the largest finite
+ * values into infinity as IEEE rounding requires.  NaN stays NaN (quiet, same
+ * sign).
+ */
+uint16_t oracle_f32_to_bf16(float x)
+{
+    uint32_t w;
+    memcpy(&w, &x, sizeof w);
+    if ((w & 0x7F800000u) == 0x7F800000u && (w & 0x007FFFFFu) != 0)
+        return (uint16_t)((w >> 16) | 0x0040u);
+    uint32_t kept = w >> 16;
+    uint32_t dropped = w & 0xFFFFu;
+    if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))
+        kept += 1u;
+    return (uint16_t)kept;
+}
+
+/*
+ * Mixed-precision all-gather placement (Section 3.1: mixed-precision groups
+ * keep fp32 master shards and cast them to bf16 for the all-gather): the
+ * placement of Eq. (2) reading fp32 rank slots and writing each element
+ * rounded to bf16.  slots is W rank slots of `stride` fp32 elements.
+ */
+int oracle_ag_cast(int32_t world, int32_t nparams, const int64_t *dim0, const int64_t *row_numel,
+                   const float *slots, int64_t stride, uint16_t *const *full)
+{
+    int64_t *R = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nparams > 0 ? nparams : 1));
+    int64_t *o = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nparams > 0 ? nparams : 1));
+    int64_t S = 0;
+    int rc = ORACLE_OK;
+    if (!R || !o) {
+        rc = ORACLE_ENOMEM;
+        goto done;
+    }
+    rc = oracle_geometry(world, nparams, dim0, row_numel, R, o, &S);
+    if (rc != ORACLE_OK)
+        goto done;
+    if (stride < S) {
+        rc = ORACLE_EINVAL;
+        goto done;
+    }
+    for (int32_t p = 0; p < nparams; ++p) {
+        int64_t K = row_numel[p];
+        for (int32_t r = 0; r < world; ++r) {
+            int64_t v = oracle_valid_rows(dim0[p], R[p], r);
+            for (int64_t i = 0; i < v; ++i) {
+                const float *src_row = slots + (size_t)r * (size_t)stride + (size_t)o[p] + (size_t)(i * K);
+                uint16_t *dst_row = full[p] + (size_t)((r * R[p] + i) * K);
+                for (int64_t k = 0; k < K; ++k)
+                    dst_row[k] = oracle_f32_to_bf16(src_row[k]);
+            }
+        }
+    }
+done:
+    free(R);
+    free(o);
+    return rc;
+}

@@ -318,5 +318,56 @@ def pin_window_matches_full(orc, seed=17):
                     assert_same_f32(win, full[r, o[p] + lo:o[p] + hi], f"window p={p} r={r} [{i0},{i1})")
 
 
+def _cast_patterns(rng) -> np.ndarray:
+    """binary32 bit patterns: every sign and exponent with the mantissas that
+    decide a rounding (0, ties with even and odd kept part, one below and one
+    above a tie, all ones), plus random patterns."""
+    mants = np.array([0x000000, 0x000001, 0x007FFF, 0x008000, 0x008001, 0x00FFFF, 0x010000, 0x017FFF, 0x018000,
+                      0x018001, 0x3F8000, 0x7F8000, 0x7FFFFF, 0x7F7FFF, 0x400000, 0x408000, 0x7E8000, 0x7F0000],
+                     dtype=np.uint32)
+    se = np.arange(512, dtype=np.uint32) << np.uint32(23)
+    structured = (se[:, None] | mants[None, :]).reshape(-1)
+    randoms = rng.integers(0, 2 ** 32, size=200_000, dtype=np.uint64).astype(np.uint32)
+    return np.concatenate([structured, randoms])
+
+
+def pin_cast_vs_torch(orc, seed=19):
+    """The fp32 -> bf16 rounding against torch's round-to-nearest-even cast,
+    bit for bit (NaN by class)."""
+    bits = _cast_patterns(np.random.default_rng(seed))
+    x = bits.view(np.float32)
+    got = np.concatenate(orc.ag_cast(1, [(x.size, 1)], x.reshape(1, -1)))
+    want = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    gnan = (got & 0x7F80) == 0x7F80
+    gnan &= (got & 0x7F) != 0
+    wnan = ((want & 0x7F80) == 0x7F80) & ((want & 0x7F) != 0)
+    assert (gnan == wnan).all(), "NaN class differs"
+    bad = (got != want) & ~wnan
+    assert not bad.any(), f"{int(bad.sum())} casts differ; first input 0x{bits[bad][0]:08x}"
+    for v, w in ((1.0, 0x3F80), (-2.0, 0xC000), (float("inf"), 0x7F80), (0.0, 0x0000), (-0.0, 0x8000)):
+        assert orc.f32_to_bf16(v) == w, v
+
+
+def pin_ag_cast_identity(orc, seed=23):
+    """Mixed-precision placement: AG_cast(shard(x)) == bf16(x) for x in fp32,
+    shards built by torch.chunk, NaN in every padding position."""
+    rng = np.random.default_rng(seed)
+    for W, dims in ((4, [(1000, 64), (64, 1), (333, 17), (7, 5), (129, 128)]), (3, [(1, 1), (5, 3)]),
+                    (8, [(9, 9), (3, 2)])):
+        R, o, S = orc.geometry(W, dims)
+        xs = [rng.standard_normal((d, k)).astype(np.float32) * np.float32(10.0 ** rng.integers(-3, 3))
+              for d, k in dims]
+        slots = np.full((W, S + 3), np.nan, dtype=np.float32)
+        for p, x in enumerate(xs):
+            for r, ch in enumerate(torch.chunk(torch.from_numpy(x), W)):
+                flat = ch.numpy().reshape(-1)
+                slots[r, o[p]:o[p] + flat.size] = flat
+        full = orc.ag_cast(W, dims, slots)
+        for p, x in enumerate(xs):
+            want = torch.from_numpy(x.reshape(-1).copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            assert_same_u16(full[p], want, f"AG_cast(shard(x)) W={W} p={p}")
+
+
 ALL_PINS = [pin_golden, pin_slot_sizes, pin_torch_chunk, pin_chunk_cat, pin_brute_force, pin_integer_exact,
-            pin_order_probe, pin_fp64_bound, pin_special_values, pin_ag_identity, pin_window_matches_full]
+            pin_order_probe, pin_fp64_bound, pin_special_values, pin_ag_identity, pin_window_matches_full,
+            pin_cast_vs_torch, pin_ag_cast_identity]

@@ -38,6 +38,13 @@ MUTANTS = {
     "ag_transposed_rank": [("uint16_t *to = full[p] + (size_t)((r * R[p] + i) * K);",
                             "uint16_t *to = full[p] + (size_t)((i * (int64_t)world + r) * K);")],
     "offset_without_padding": [("off += R * row_numel[p];", "off += (dim0[p] * row_numel[p] + world - 1) / world;")],
+    "cast_truncates": [("if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))", "if (0)")],
+    "cast_ties_away": [("(dropped == 0x8000u && (kept & 1u))", "(dropped == 0x8000u)")],
+    "cast_drops_nan": [("        return (uint16_t)((w >> 16) | 0x0040u);", "        return (uint16_t)0x7F80u;")],
+    "ag_cast_drops_offset": [("const float *src_row = slots + (size_t)r * (size_t)stride + (size_t)o[p] +",
+                              "const float *src_row = slots + (size_t)r * (size_t)stride +")],
+    "ag_cast_transposed_rank": [("uint16_t *dst_row = full[p] + (size_t)((r * R[p] + i) * K);",
+                                 "uint16_t *dst_row = full[p] + (size_t)((i * (int64_t)world + r) * K);")],
 }
 
 RUNNER = textwrap.dedent("""
