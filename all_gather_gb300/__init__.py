@@ -21,7 +21,8 @@ from ._binding import (  # noqa: F401  (re-exported C-ABI names)
     TIDE_DEBUG_SKIP_FILL, TIDE_DTYPE_BF16,
     TIDE_ERR_ALIGNMENT, TIDE_ERR_CUDA, TIDE_ERR_INVALID_ARG, TIDE_ERR_OOM, TIDE_ERR_TIMEOUT, TIDE_ERR_UNSUPPORTED,
     TIDE_KERNEL_AUTO, TIDE_KERNEL_BULK, TIDE_KERNEL_DIRECT, TIDE_OK, TIDE_ORDER_RANK_ASC, TIDE_SCHED_DYNAMIC,
-    TIDE_SCHED_STATIC, PlanFlags, TideError, load_library, make_flags, tide_ag_place, tide_last_device_status,
+    TIDE_SCHED_STATIC, PlanFlags, TideError, load_library, make_flags, tide_ag_place, tide_ag_place_f32,
+    tide_last_device_status,
     tide_last_error, tide_launch_count, tide_plan_build, tide_plan_destroy, tide_plan_fold_config,
     tide_plan_num_segments, tide_plan_rebind, tide_plan_segment, tide_plan_slot_numel, tide_rs_fold,
     tide_rs_fold_noalloc, tide_status_string)
@@ -109,6 +110,18 @@ class Plan:
                 raise ValueError(f"full[{p}] must be a contiguous bfloat16 tensor of shape {self.shapes[p]}")
         tide_ag_place(self.handle, slots.data_ptr(), slots.stride(0) if self.world > 1 else slots.shape[1],
                       [f.data_ptr() for f in full], AG_MODES[mode], _stream_handle(stream))
+        return full
+
+    def ag_place_f32(self, slots, full: List, stream=None):
+        """Mixed-precision placement: slots fp32 CUDA tensor [W, stride]; full[p] bf16 of parameter p's shape."""
+        import torch
+        if slots.dtype != torch.float32 or slots.dim() != 2 or slots.shape[0] != self.world or slots.stride(1) != 1:
+            raise ValueError("slots must be float32 [W, stride] with unit inner stride")
+        for p, f in enumerate(full):
+            if f.dtype != torch.bfloat16 or not f.is_contiguous() or tuple(f.shape) != self.shapes[p]:
+                raise ValueError(f"full[{p}] must be a contiguous bfloat16 tensor of shape {self.shapes[p]}")
+        tide_ag_place_f32(self.handle, slots.data_ptr(), slots.stride(0) if self.world > 1 else slots.shape[1],
+                          [f.data_ptr() for f in full], _stream_handle(stream))
         return full
 
     def fold_config(self) -> dict:

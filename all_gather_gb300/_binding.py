@@ -35,7 +35,7 @@ TIDE_DEBUG_SKIP_FILL = 0x4
 EXPORTED = ("tide_plan_build", "tide_plan_rebind", "tide_rs_fold", "tide_ag_place", "tide_plan_destroy",
             "tide_plan_slot_numel", "tide_plan_num_segments", "tide_plan_segment", "tide_plan_fold_config",
             "tide_last_device_status", "tide_launch_count", "tide_status_string", "tide_last_error",
-            "tide_rs_fold_noalloc")
+            "tide_rs_fold_noalloc", "tide_ag_place_f32")
 
 
 class TideError(RuntimeError):
@@ -105,6 +105,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tide_last_error.restype = ctypes.c_char_p
     lib.tide_rs_fold_noalloc.argtypes = [i32, i32, ctypes.POINTER(ParamDesc), vp, i64, ctypes.c_float, i32, vp]
     lib.tide_rs_fold_noalloc.restype = st
+    lib.tide_ag_place_f32.argtypes = [vp, vp, i64, ctypes.POINTER(vp), vp]
+    lib.tide_ag_place_f32.restype = st
     _lib = lib
     return lib
 
@@ -170,6 +172,12 @@ def tide_ag_place(plan: int, slots_base: int, slot_stride: int, full: Sequence[i
     arr = (ctypes.c_void_p * max(len(full), 1))(*[ctypes.c_void_p(int(x) or None) for x in full])
     _check(load_library().tide_ag_place(ctypes.c_void_p(plan), ctypes.c_void_p(slots_base or None), slot_stride,
                                         arr, mode, ctypes.c_void_p(stream or None)), "tide_ag_place")
+
+
+def tide_ag_place_f32(plan: int, slots_base: int, slot_stride: int, full: Sequence[int], stream: int = 0) -> None:
+    arr = (ctypes.c_void_p * max(len(full), 1))(*[ctypes.c_void_p(int(x) or None) for x in full])
+    _check(load_library().tide_ag_place_f32(ctypes.c_void_p(plan), ctypes.c_void_p(slots_base or None), slot_stride,
+                                            arr, ctypes.c_void_p(stream or None)), "tide_ag_place_f32")
 
 
 def tide_plan_destroy(plan: int) -> None:

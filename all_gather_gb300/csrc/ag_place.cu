@@ -5,6 +5,7 @@
 // are never read.  A pure HBM copy: one persistent grid walks (piece, chunk)
 // work items and moves 16-byte vectors when source and destination share
 // their alignment phase.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "tide_internal.h"
@@ -67,11 +68,80 @@ __global__ void __launch_bounds__(kAgThreads) ag_place_kernel(const __grid_const
     }
 }
 
+// Two fp32 values rounded to nearest even and packed as a bf16 pair (low half first).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint16_t to_bf16_bits(float x)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// Mixed-precision placement (fp32 master shards -> bf16 full tensors): the
+// same walk as ag_place_kernel, reading 32 bytes of fp32 and writing 16 bytes
+// of bf16 per vector when, after a common head, both sides are 16-byte aligned.
+__global__ void __launch_bounds__(kAgThreads) ag_cast_kernel(const __grid_constant__ AgParams ap)
+{
+    constexpr int NT = kAgThreads;
+    constexpr int U = 2;
+    const int tid = threadIdx.x;
+    for (int64_t i = ap.item_begin + blockIdx.x; i < ap.item_end; i += gridDim.x) {
+        const Item item = ap.items[i];
+        const Seg seg = ap.segs[item.seg];
+        const int64_t count = int64_t(item.count_kind & ~kItemPad);
+        const float *src = ap.slots_f32 + int64_t(seg.rank) * ap.stride + seg.dst_elem + item.begin;
+        uint16_t *dst = ap.full[seg.param - ap.param_base] + seg.src_elem + item.begin;
+        const uintptr_t sa = reinterpret_cast<uintptr_t>(src), da = reinterpret_cast<uintptr_t>(dst);
+        int64_t h = int64_t(((16u - (da & 15u)) & 15u) >> 1);
+        if (h > count)
+            h = count;
+        if (((sa + uintptr_t(h) * 4u) & 15u) == 0) {
+            const int64_t nv = (count - h) >> 3;
+            const float4 *s4 = reinterpret_cast<const float4 *>(src + h);
+            uint4 *d8 = reinterpret_cast<uint4 *>(dst + h);
+            for (int64_t v = tid; v < nv; v += int64_t(NT) * U) {
+                float4 a[U], b[U];
+#pragma unroll
+                for (int j = 0; j < U; ++j) {
+                    const int64_t vj = v + int64_t(j) * NT;
+                    if (vj < nv) {
+                        a[j] = __ldcs(s4 + 2 * vj);
+                        b[j] = __ldcs(s4 + 2 * vj + 1);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < U; ++j) {
+                    const int64_t vj = v + int64_t(j) * NT;
+                    if (vj < nv)
+                        d8[vj] = make_uint4(pack_bf16x2(a[j].x, a[j].y), pack_bf16x2(a[j].z, a[j].w),
+                                            pack_bf16x2(b[j].x, b[j].y), pack_bf16x2(b[j].z, b[j].w));
+                }
+            }
+            for (int64_t e = tid; e < h; e += NT)
+                dst[e] = to_bf16_bits(src[e]);
+            for (int64_t e = h + nv * 8 + tid; e < count; e += NT)
+                dst[e] = to_bf16_bits(src[e]);
+        } else {
+            for (int64_t e = tid; e < count; e += NT)
+                dst[e] = to_bf16_bits(src[e]);
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_ag(const AgParams &ap, int grid, cudaStream_t stream)
 {
     ag_place_kernel<<<grid, kAgThreads, 0, stream>>>(ap);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ag_f32(const AgParams &ap, int grid, cudaStream_t stream)
+{
+    ag_cast_kernel<<<grid, kAgThreads, 0, stream>>>(ap);
     return cudaGetLastError();
 }
 

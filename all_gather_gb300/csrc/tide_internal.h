@@ -85,6 +85,7 @@ struct AgParams {
     const Item *items;
     int64_t item_begin, item_end;  // this launch's item range
     const uint16_t *slots;
+    const float *slots_f32;        // mixed-precision placement: fp32 slots (slots unused)
     int64_t stride;
     int32_t param_base;            // full[0] is parameter param_base
     int32_t n_full;
@@ -97,6 +98,7 @@ cudaError_t launch_fold(const FoldParams &fp, int kernel, int accumulate, int gr
 cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *blocks_per_sm);
 size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems, int fill_ranks, bool whole_sm);
 cudaError_t launch_ag(const AgParams &ap, int grid, cudaStream_t stream);
+cudaError_t launch_ag_f32(const AgParams &ap, int grid, cudaStream_t stream);
 
 extern std::atomic<uint64_t> g_launches;
 

@@ -503,16 +503,20 @@ tide_status_t tide_rs_fold(tide_plan_t *plan, float *out_base, int64_t out_slot_
     return TIDE_OK;
 }
 
-tide_status_t tide_ag_place(tide_plan_t *plan, const void *slots_base, int64_t slot_stride, void *const *full,
-                            int32_t mode, void *stream_)
+}  // extern "C"
+
+namespace {
+
+// Common checks of both placements: plan, mode-independent sizes, the slot
+// range [s_lo, s_hi) and the full[] tensors (non-null, aligned, disjoint from
+// the slots and from each other).
+tide_status_t check_placement(tide_plan_t *plan, const void *slots_base, int64_t slot_stride, size_t elem_bytes,
+                              void *const *full)
 {
-    t_last_error.clear();
     if (!plan)
         return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
     if (plan->host_only)
         return fail(TIDE_ERR_INVALID_ARG, "plan was built host-only and cannot be launched");
-    if (mode != TIDE_AG_SM && mode != TIDE_AG_CE_2D && mode != TIDE_AG_CE_1D)
-        return fail(TIDE_ERR_INVALID_ARG, "unknown placement mode %d", mode);
     if (slot_stride < plan->slot_numel)
         return fail(TIDE_ERR_INVALID_ARG, "slot_stride %lld < S %lld", (long long)slot_stride,
                     (long long)plan->slot_numel);
@@ -520,13 +524,13 @@ tide_status_t tide_ag_place(tide_plan_t *plan, const void *slots_base, int64_t s
         return TIDE_OK;
     if (!slots_base || !full)
         return fail(TIDE_ERR_INVALID_ARG, "slots_base or full is NULL");
-    if (reinterpret_cast<uintptr_t>(slots_base) & 1u)
-        return fail(TIDE_ERR_ALIGNMENT, "slots_base is not 2-byte aligned");
+    if (reinterpret_cast<uintptr_t>(slots_base) & (elem_bytes - 1))
+        return fail(TIDE_ERR_ALIGNMENT, "slots_base is not %zu-byte aligned", elem_bytes);
     int64_t span;
     if (!mul_ok(slot_stride, plan->world - 1, &span) || span > kMaxElems - plan->slot_numel)
         return fail(TIDE_ERR_INVALID_ARG, "slot extent overflows");
     const uintptr_t s_lo = reinterpret_cast<uintptr_t>(slots_base);
-    const uintptr_t s_hi = s_lo + uintptr_t(span + plan->slot_numel) * 2u;
+    const uintptr_t s_hi = s_lo + uintptr_t(span + plan->slot_numel) * elem_bytes;
     std::vector<std::pair<uintptr_t, uintptr_t>> iv;
     iv.reserve(plan->nparams);
     for (int32_t p = 0; p < plan->nparams; ++p) {
@@ -546,36 +550,60 @@ tide_status_t tide_ag_place(tide_plan_t *plan, const void *slots_base, int64_t s
     for (size_t i = 1; i < iv.size(); ++i)
         if (iv[i].first < iv[i - 1].second)
             return fail(TIDE_ERR_INVALID_ARG, "two full[] tensors overlap");
-    tide_status_t st = check_device(plan);
-    if (st != TIDE_OK)
+    return check_device(plan);
+}
+
+// Placement kernel launches, at most kAgParamsPerLaunch destination pointers each.
+tide_status_t launch_placement(tide_plan_t *plan, const uint16_t *slots, const float *slots_f32,
+                               int64_t slot_stride, void *const *full, cudaStream_t stream)
+{
+    static thread_local tide::AgParams ap;  // ~8 KB: keep it off the stack
+    for (int32_t p0 = 0; p0 < plan->nparams; p0 += tide::kAgParamsPerLaunch) {
+        const int32_t p1 = std::min(plan->nparams, p0 + tide::kAgParamsPerLaunch);
+        ap.segs = plan->d_segs;
+        ap.items = plan->d_ag_items;
+        ap.item_begin = plan->ag_param_item_begin[p0];
+        ap.item_end = plan->ag_param_item_begin[p1];
+        if (ap.item_end == ap.item_begin)
+            continue;
+        ap.slots = slots;
+        ap.slots_f32 = slots_f32;
+        ap.stride = slot_stride;
+        ap.param_base = p0;
+        ap.n_full = p1 - p0;
+        for (int32_t p = p0; p < p1; ++p)
+            ap.full[p - p0] = static_cast<uint16_t *>(full[p]);
+        const int64_t n = ap.item_end - ap.item_begin;
+        const int grid = int(std::min<int64_t>(n, int64_t(plan->sms) * 8));
+        cudaError_t e = slots_f32 ? tide::launch_ag_f32(ap, grid, stream) : tide::launch_ag(ap, grid, stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "placement launch");
+        tide::g_launches.fetch_add(1);
+    }
+    return TIDE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tide_status_t tide_ag_place(tide_plan_t *plan, const void *slots_base, int64_t slot_stride, void *const *full,
+                            int32_t mode, void *stream_)
+{
+    t_last_error.clear();
+    if (mode != TIDE_AG_SM && mode != TIDE_AG_CE_2D && mode != TIDE_AG_CE_1D)
+        return fail(TIDE_ERR_INVALID_ARG, "unknown placement mode %d", mode);
+    tide_status_t st = check_placement(plan, slots_base, slot_stride, 2, full);
+    if (st != TIDE_OK || plan->ag_items.empty())
         return st;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     const auto *slots = static_cast<const uint16_t *>(slots_base);
     cudaError_t e = cudaSuccess;
 
     if (mode == TIDE_AG_SM) {
-        static thread_local tide::AgParams ap;  // ~8 KB: keep it off the stack
-        for (int32_t p0 = 0; p0 < plan->nparams; p0 += tide::kAgParamsPerLaunch) {
-            const int32_t p1 = std::min(plan->nparams, p0 + tide::kAgParamsPerLaunch);
-            ap.segs = plan->d_segs;
-            ap.items = plan->d_ag_items;
-            ap.item_begin = plan->ag_param_item_begin[p0];
-            ap.item_end = plan->ag_param_item_begin[p1];
-            if (ap.item_end == ap.item_begin)
-                continue;
-            ap.slots = slots;
-            ap.stride = slot_stride;
-            ap.param_base = p0;
-            ap.n_full = p1 - p0;
-            for (int32_t p = p0; p < p1; ++p)
-                ap.full[p - p0] = static_cast<uint16_t *>(full[p]);
-            const int64_t n = ap.item_end - ap.item_begin;
-            const int grid = int(std::min<int64_t>(n, int64_t(plan->sms) * 8));
-            e = tide::launch_ag(ap, grid, stream);
-            if (e != cudaSuccess)
-                return cuda_fail(e, "placement launch");
-            tide::g_launches.fetch_add(1);
-        }
+        st = launch_placement(plan, slots, nullptr, slot_stride, full, stream);
+        if (st != TIDE_OK)
+            return st;
     } else {
         // Copy engines.  Rank r's piece of p: slot r at o_p -> full_p rows [r R, r R + v).
         for (int32_t p = 0; p < plan->nparams; ++p) {
@@ -609,6 +637,23 @@ tide_status_t tide_ag_place(tide_plan_t *plan, const void *slots_base, int64_t s
         }
     }
     e = cudaEventRecord(plan->last_use, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "record plan event");
+    return TIDE_OK;
+}
+
+tide_status_t tide_ag_place_f32(tide_plan_t *plan, const float *slots_base, int64_t slot_stride, void *const *full,
+                                void *stream_)
+{
+    t_last_error.clear();
+    tide_status_t st = check_placement(plan, slots_base, slot_stride, 4, full);
+    if (st != TIDE_OK || plan->ag_items.empty())
+        return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    st = launch_placement(plan, nullptr, slots_base, slot_stride, full, stream);
+    if (st != TIDE_OK)
+        return st;
+    cudaError_t e = cudaEventRecord(plan->last_use, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "record plan event");
     return TIDE_OK;

@@ -57,6 +57,7 @@ def parse():
     ap.add_argument("--no-baseline", action="store_true", help="skip the two-pass GPU baseline")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-interference", action="store_true", help="skip the concurrent-GEMM harness")
+    ap.add_argument("--no-variants", action="store_true", help="skip timing the other placement variants")
     return ap.parse_args()
 
 
@@ -432,6 +433,10 @@ def run_ours(args):
         "clocks": clk,
     }
 
+    # the other placement engines and the mixed-precision placement, timed alone after the step
+    if rank == 0 and not args.no_variants:
+        result["variants"] = time_variants(plan, w, S, slots, full, dev, steps=min(K, 20))
+
     # two-pass stock-FSDP2-style baseline (chunk_cat pack to fp32, then reduce), timed alone
     if not args.no_baseline and rank == 0:
         result["baseline_two_pass"] = baselines.time_two_pass(w, gs.views, S, out, slots, full, steps=min(K, 10))
@@ -463,6 +468,36 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def time_variants(plan, w, S, slots, full, dev, steps: int = 20) -> dict:
+    """Mean event time of each placement variant over `steps` launches."""
+    import torch
+
+    import workloads
+    N = w.total_numel()
+    slots32 = torch.stack([workloads.normal_fp32(S, workloads.slot_seed(w, r), 0.02, dev) for r in range(w.world)])
+    stream = torch.cuda.current_stream()
+    calls = {
+        "ag_place_f32 (fp32 master shards -> bf16, fused cast)": (lambda: plan.ag_place_f32(slots32, full), 6 * N),
+        "ag_place ce2d (copy engines, one 2D copy per parameter)": (lambda: plan.ag_place(slots, full, "ce2d"), 4 * N),
+        "ag_place ce1d (copy engines, one copy per piece)": (lambda: plan.ag_place(slots, full, "ce1d"), 4 * N),
+    }
+    res = {}
+    for name, (fn, nbytes) in calls.items():
+        for _ in range(3):
+            fn()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s.record(stream)
+        for _ in range(steps):
+            fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(e) / steps
+        res[name] = {"ms": round(ms, 4), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "alg_bytes": nbytes}
+    del slots32
+    return res
 
 
 def e2e(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world):

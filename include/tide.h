@@ -202,6 +202,19 @@ TIDE_API tide_status_t tide_rs_fold(tide_plan_t *plan, float *out_base, int64_t 
 TIDE_API tide_status_t tide_ag_place(tide_plan_t *plan, const void *slots_base, int64_t slot_stride, void *const *full,
                             int32_t mode, void *stream);
 
+/*
+ * Mixed-precision all-gather placement (Section 3.1: groups that keep fp32
+ * master shards cast them to bf16 for the all-gather; here the cast is fused
+ * into the placement of Eq. (2)).
+ *   slots_base: device fp32, W rank slots of `slot_stride` elements (>= S);
+ *               4-byte aligned.  Padding is never read.
+ *   full: as tide_ag_place; each element is the fp32 value rounded to the
+ *         nearest bf16 (ties to even; NaN stays NaN, overflow gives +-inf).
+ * SM kernel only (copy engines cannot convert).  Enqueued on `stream`.
+ */
+TIDE_API tide_status_t tide_ag_place_f32(tide_plan_t *plan, const float *slots_base, int64_t slot_stride,
+                                         void *const *full, void *stream);
+
 /* Free the plan's device tables after synchronising the stream of its last use. */
 TIDE_API tide_status_t tide_plan_destroy(tide_plan_t *plan);
 

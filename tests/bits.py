@@ -51,6 +51,19 @@ def assert_same_u16(actual, expected, what=""):
         raise AssertionError(f"{what}: {int(bad.sum())} of {a.size} differ; first at {i}: 0x{a[i]:04x} vs 0x{e[i]:04x}")
 
 
+def assert_same_bf16(actual, expected, what=""):
+    """Bitwise equality of bf16 bit patterns; any NaN matches any NaN."""
+    a = np.asarray(actual, dtype=np.uint16).reshape(-1)
+    e = np.asarray(expected, dtype=np.uint16).reshape(-1)
+    assert a.shape == e.shape, f"{what}: shape {a.shape} != {e.shape}"
+    an = ((a & 0x7F80) == 0x7F80) & ((a & 0x7F) != 0)
+    en = ((e & 0x7F80) == 0x7F80) & ((e & 0x7F) != 0)
+    bad = (a != e) & ~(an & en)
+    if bad.any():
+        i = int(np.flatnonzero(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} of {a.size} differ; first at {i}: 0x{a[i]:04x} vs 0x{e[i]:04x}")
+
+
 def parse_golden(name: str) -> Dict:
     """Parse a hand-written fixture under tests/golden/."""
     out: Dict = {"params": [], "grad": {}, "expect": {}, "old": {}, "expect_acc": {}, "slot": {}, "full": {}}

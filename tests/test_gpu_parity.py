@@ -13,7 +13,7 @@ import torch
 import all_gather_gb300 as tide
 import oracle
 import workloads
-from bits import assert_same_f32, assert_same_u16, f32_to_bf16_bits
+from bits import assert_same_bf16, assert_same_f32, assert_same_u16, f32_to_bf16_bits
 from gpu_helpers import (ag_expected, bits16, oracle_rs_full, sampled_rs_check, sentinel_slots)
 
 pytestmark = pytest.mark.gpu
@@ -324,6 +324,45 @@ def test_ag_toy_and_ragged(mode):
         assert (host[cur:] == guard_bits).all()
 
 
+@pytest.mark.parametrize("case", ["aligned", "odd_slots", "odd_full"])
+def test_ag_f32_mixed_precision(case):
+    """fp32 master-shard slots -> bf16 full tensors, against the oracle's
+    round-to-nearest-even placement; rounding-critical values and NaN padding."""
+    rnd = random.Random(31)
+    specials = np.array([np.nan, np.inf, -np.inf, -0.0, 3.4e38, -3.4e38, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8,
+                         1.0 + 2.0 ** -8 + 2.0 ** -20, 2.0 ** -130, 1e-40], dtype=np.float32)
+    for world in (1, 3, 4, 8):
+        shapes = [(rnd.randint(1, 4 * world + 3), rnd.choice([1, 5, 8, 64])) for _ in range(4)] + [(world * 100 + 1,)]
+        w = workloads.custom(world, shapes, index=80 + world)
+        dims = w.dim0_rownumel()
+        R, o, S = oracle.geometry(world, dims)
+        rng = np.random.default_rng(world)
+        host = rng.standard_normal((world, S + 5)).astype(np.float32)
+        m = rng.random(host.shape) < 0.2
+        host[m] = rng.choice(specials, size=int(m.sum()))
+        mask = np.ones(host.shape, dtype=bool)
+        for p, (d, k) in enumerate(dims):
+            for r in range(world):
+                mask[r, o[p]:o[p] + oracle.valid_rows(d, R[p], r) * k] = False
+        host[mask] = np.nan
+        off = 1 if case == "odd_slots" else 0
+        buf = torch.from_numpy(np.concatenate([np.zeros(off, np.float32), host.reshape(-1)])).cuda()
+        slots = buf[off:].view(world, S + 5)
+        grads = workloads.make_grads(w, device="cuda")
+        foff = 3 if case == "odd_full" else 0
+        fbuf = torch.zeros(sum(d * k for d, k in dims) + foff + 8 * len(dims), dtype=torch.bfloat16, device="cuda")
+        full, cur = [], foff
+        for s_, (d, k) in zip(w.shapes, dims):
+            full.append(fbuf[cur:cur + d * k].view(s_))
+            cur += d * k + 8
+        with tide.Plan(grads.views) as plan:
+            plan.ag_place_f32(slots, full)
+            torch.cuda.synchronize()
+        want = oracle.ag_cast(world, dims, host)
+        for p, f in enumerate(full):
+            assert_same_bf16(bits16(f), want[p], f"ag_f32 {case} W={world} p={p}")
+
+
 def test_ag_shard_roundtrip_identity():
     """AG(shard(x)) == x for full-size-like shapes with misaligned offsets."""
     world = 8
@@ -372,5 +411,14 @@ def test_full_size_sampled(index):
         want = ag_expected(w.world, dims, slots)
         for p, f in enumerate(full):
             assert_same_u16(bits16(f), want[p], f"{w.name} ag p={p}")
+        # mixed-precision placement from fp32 master shards, every element
+        del slots
+        slots32 = torch.stack([workloads.normal_fp32(S, workloads.slot_seed(w, r), 0.02, "cuda")
+                               for r in range(w.world)])
+        plan.ag_place_f32(slots32, full)
+        torch.cuda.synchronize()
+        want = oracle.ag_cast(w.world, dims, slots32.cpu().numpy())
+        for p, f in enumerate(full):
+            assert_same_bf16(bits16(f), want[p], f"{w.name} ag_f32 p={p}")
     del gs
     torch.cuda.empty_cache()
