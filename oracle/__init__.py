@@ -21,6 +21,10 @@ What each function follows (TIDE paper, "The Endgame of FSDP Communication"):
   optional accumulate), Section 4.
 * :func:`ag` -- Section 2.1, Equation (2): rank-major slots placed into
   per-parameter full tensors, padding dropped.
+* :func:`rs_ex`, ``Oracle.rs_window_ex`` -- Section 4.3's orders: rank
+  order, the one-node Level 1 order (other ranks in local-rank order, then
+  the destination's own contribution) and the two-level order (per-node
+  Level 1 partials, then the node partials), for bf16 or fp32 gradients.
 * :func:`f32_to_bf16`, :func:`ag_cast` -- Section 3.1 (mixed-precision
   groups cast fp32 master shards to bf16 for the all-gather): the same
   placement from fp32 slots, each element rounded to nearest even.
@@ -83,6 +87,15 @@ class Oracle:
         lib.oracle_ag_cast.argtypes = [ctypes.c_int32, ctypes.c_int32, _i64p, _i64p, _f32p, ctypes.c_int64,
                                        ctypes.POINTER(_u16p)]
         lib.oracle_ag_cast.restype = ctypes.c_int
+        lib.oracle_rs_window_ex.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
+                                            ctypes.POINTER(ctypes.c_void_p), ctypes.c_float, ctypes.c_int32,
+                                            _f32p, _f32p]
+        lib.oracle_rs_window_ex.restype = ctypes.c_int
+        lib.oracle_rs_ex.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                     _i64p, _i64p, ctypes.POINTER(ctypes.c_void_p), ctypes.c_float, ctypes.c_int32,
+                                     _f32p, ctypes.c_int64]
+        lib.oracle_rs_ex.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
 
@@ -192,6 +205,49 @@ class Oracle:
         return list(full)
 
 
+    # -- other summation orders, fp32 gradients ----------------------------
+    ORDERS = {"rank": 0, "staged": 1, "nodes": 2}
+
+    def rs_ex(self, world: int, dims, grads, alpha: float, accumulate: bool, out: np.ndarray,
+              order: str = "rank", node_size: int = 0) -> np.ndarray:
+        """Reduce-scatter in a given order.  grads[p][u]: uint16 (bf16 bits) or float32 arrays."""
+        P = len(dims)
+        assert out.dtype == np.float32 and out.ndim == 2 and out.shape[0] == world and out.flags.c_contiguous
+        dtype = 1 if (P and np.asarray(grads[0][0]).dtype == np.float32) else 0
+        keep = []
+        ptrs = (ctypes.c_void_p * max(P * world, 1))()
+        for p in range(P):
+            for u in range(world):
+                g = np.ascontiguousarray(grads[p][u], dtype=np.float32 if dtype else np.uint16).reshape(-1)
+                assert g.size == dims[p][0] * dims[p][1]
+                keep.append(g)
+                ptrs[p * world + u] = g.ctypes.data
+        d0 = np.array([d for d, _ in dims] or [0], dtype=np.int64)
+        kk = np.array([k for _, k in dims] or [0], dtype=np.int64)
+        rc = self.lib.oracle_rs_ex(world, dtype, self.ORDERS[order], node_size, P, d0.ctypes.data_as(_i64p),
+                                   kk.ctypes.data_as(_i64p), ptrs, ctypes.c_float(alpha), int(bool(accumulate)),
+                                   out.ctypes.data_as(_f32p), out.shape[1])
+        if rc != 0:
+            raise ValueError(f"oracle_rs_ex failed ({rc})")
+        return out
+
+    def rs_window_ex(self, srcs, n_valid: int, n_pad: int, alpha: float, accumulate: bool, dest: int,
+                     order: str = "rank", node_size: int = 0, old=None) -> np.ndarray:
+        W = len(srcs)
+        dtype = 1 if np.asarray(srcs[0]).dtype == np.float32 else 0
+        srcs = [np.ascontiguousarray(x, dtype=np.float32 if dtype else np.uint16) for x in srcs]
+        n = n_valid + n_pad
+        out = np.empty(n, dtype=np.float32)
+        old = np.ascontiguousarray(old, dtype=np.float32) if accumulate else out
+        arr = (ctypes.c_void_p * W)(*[x.ctypes.data for x in srcs])
+        rc = self.lib.oracle_rs_window_ex(W, dtype, self.ORDERS[order], node_size, dest, n_valid, n_pad, arr,
+                                          ctypes.c_float(alpha), int(bool(accumulate)), old.ctypes.data_as(_f32p),
+                                          out.ctypes.data_as(_f32p))
+        if rc != 0:
+            raise ValueError(f"oracle_rs_window_ex failed ({rc})")
+        return out
+
+
 _default: Optional[Oracle] = None
 
 
@@ -227,6 +283,10 @@ def rs(world, dims, grads, alpha, accumulate, out):
 
 def ag(world, dims, slots, full=None):
     return load().ag(world, dims, slots, full)
+
+
+def rs_ex(world, dims, grads, alpha, accumulate, out, order="rank", node_size=0):
+    return load().rs_ex(world, dims, grads, alpha, accumulate, out, order, node_size)
 
 
 def f32_to_bf16(x):

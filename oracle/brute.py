@@ -88,3 +88,51 @@ def all_gather(world: int, shapes: Sequence[Tuple[int, int]], slots: np.ndarray)
                 t[row * k + c] = slots[r, starts[p] + i * k + c]
         full.append(t)
     return full
+
+
+def order_of(world: int, order: str, node_size: int, dest: int):
+    """List of rank groups whose partials are added in list order; inside a
+    group the ranks are added in list order (Section 4.3 readings)."""
+    if order == "rank":
+        return [list(range(world))]
+    if order == "staged":
+        return [[u for u in range(world) if u != dest] + [dest]]
+    groups = []
+    for n in range(world // node_size):
+        members = list(range(n * node_size, (n + 1) * node_size))
+        owner = n * node_size + dest % node_size
+        groups.append([u for u in members if u != owner] + [owner])
+    return groups
+
+
+def reduce_scatter_ordered(world, shapes, grads, alpha, accumulate, old, order="rank", node_size=0):
+    """Like reduce_scatter, in a given order; grads are uint16 (bf16) or float32 arrays."""
+    a = np.float32(alpha)
+    is_f32 = np.asarray(grads[0][0]).dtype == np.float32
+
+    def val(p, u, idx):
+        return np.float32(grads[p][u][idx]) if is_f32 else bf16_value(int(grads[p][u][idx]))
+
+    rows = [-(-d // world) for d, _ in shapes]
+    starts, s = [], 0
+    for (d, k), R in zip(shapes, rows):
+        starts.append(s)
+        s += R * k
+    out = old.copy()
+    for p, ((d, k), R) in enumerate(zip(shapes, rows)):
+        for r in range(world):
+            groups = order_of(world, order, node_size, r)
+            for i in range(R):
+                row = r * R + i
+                for c in range(k):
+                    total = None
+                    for grp in groups:
+                        part = None
+                        for u in grp:
+                            x = val(p, u, row * k + c) if row < d else np.float32(0.0)
+                            part = x if part is None else np.float32(part + x)
+                        total = part if total is None else np.float32(total + part)
+                    y = np.float32(a * total)
+                    pos = starts[p] + i * k + c
+                    out[r, pos] = np.float32(old[r, pos] + y) if accumulate else y
+    return out

@@ -275,3 +275,151 @@ done:
     free(o);
     return rc;
 }
+
+/* ------------------------------------------------------------------------
+ * Summation orders other than rank order, and fp32 gradients.
+ *
+ * Section 4.3: Level 1 adds the L - 1 staged contributions in local-rank
+ * order and then the owner's own contribution, in fp32; Level 2 adds the
+ * node partials.  Orders (readings of that section for virtual ranks):
+ *   ORACLE_ORDER_RANK      ((G0 + G1) + G2) + ...            (rank order)
+ *   ORACLE_ORDER_STAGED    one node: every rank except the destination r in
+ *                          ascending order, then r's own contribution
+ *   ORACLE_ORDER_NODES     W = M L ranks in M nodes of L: node n's partial is
+ *                          its ranks except n L + (r mod L) ascending, then
+ *                          that rank; the M node partials are then added in
+ *                          node order
+ * dtype 0: bf16 gradients (widened exactly); dtype 1: fp32 gradients
+ * (b_grad = 4, used as they are).
+ * ---------------------------------------------------------------------- */
+#define ORACLE_ORDER_RANK 0
+#define ORACLE_ORDER_STAGED 1
+#define ORACLE_ORDER_NODES 2
+
+static float widen(const void *src, int32_t dtype, int64_t j)
+{
+    if (dtype == 0)
+        return bf16_to_f32(((const uint16_t *)src)[j]);
+    return ((const float *)src)[j];
+}
+
+/* The order in which the W contributions to destination rank r are added
+ * (seq), and how many consecutive entries form one partial (group; the
+ * partials are then added in sequence order). */
+static int make_sequence(int32_t world, int32_t order, int32_t node_size, int32_t r, int32_t *seq, int32_t *group)
+{
+    if (order == ORACLE_ORDER_RANK) {
+        for (int32_t u = 0; u < world; ++u)
+            seq[u] = u;
+        *group = world;
+        return ORACLE_OK;
+    }
+    if (order == ORACLE_ORDER_STAGED) {
+        int32_t q = 0;
+        for (int32_t u = 0; u < world; ++u)
+            if (u != r)
+                seq[q++] = u;
+        seq[q] = r;
+        *group = world;
+        return ORACLE_OK;
+    }
+    if (order == ORACLE_ORDER_NODES) {
+        if (node_size < 1 || world % node_size != 0)
+            return ORACLE_EINVAL;
+        int32_t q = 0;
+        for (int32_t n = 0; n < world / node_size; ++n) {
+            int32_t owner = n * node_size + r % node_size;
+            for (int32_t l = 0; l < node_size; ++l)
+                if (n * node_size + l != owner)
+                    seq[q++] = n * node_size + l;
+            seq[q++] = owner;
+        }
+        *group = node_size;
+        return ORACLE_OK;
+    }
+    return ORACLE_EINVAL;
+}
+
+/* Eq. (3) + Eq. (5) for one window of destination rank `dest`, in `order`. */
+int oracle_rs_window_ex(int32_t world, int32_t dtype, int32_t order, int32_t node_size, int32_t dest,
+                        int64_t n_valid, int64_t n_pad, const void *const *src, float alpha, int32_t accumulate,
+                        const float *old, float *out)
+{
+    int64_t n = n_valid + n_pad;
+    if (world < 1 || n_valid < 0 || n_pad < 0 || (dtype != 0 && dtype != 1) || dest < 0 || dest >= world)
+        return ORACLE_EINVAL;
+    if (n == 0)
+        return ORACLE_OK;
+    int32_t *seq = (int32_t *)malloc(sizeof(int32_t) * (size_t)world);
+    float *pack = (float *)malloc((size_t)world * (size_t)n * sizeof(float));
+    int32_t group = world;
+    int rc = (seq && pack) ? make_sequence(world, order, node_size, dest, seq, &group) : ORACLE_ENOMEM;
+    if (rc != ORACLE_OK)
+        goto done;
+    /* pass 1: slice, zero-pad, widen */
+    for (int32_t u = 0; u < world; ++u) {
+        float *dst = pack + (size_t)u * (size_t)n;
+        for (int64_t j = 0; j < n_valid; ++j)
+            dst[j] = widen(src[u], dtype, j);
+        for (int64_t j = n_valid; j < n; ++j)
+            dst[j] = +0.0f;
+    }
+    /* pass 2: partials of `group` consecutive contributions of the sequence,
+     * then the partials in sequence order */
+    for (int64_t j = 0; j < n; ++j) {
+        float total = 0.0f;
+        for (int32_t g0 = 0; g0 < world; g0 += group) {
+            float part = pack[(size_t)seq[g0] * (size_t)n + (size_t)j];
+            for (int32_t q = g0 + 1; q < g0 + group; ++q)
+                part = part + pack[(size_t)seq[q] * (size_t)n + (size_t)j];
+            total = (g0 == 0) ? part : total + part;
+        }
+        float y = alpha * total;
+        out[j] = accumulate ? (old[j] + y) : y;
+    }
+done:
+    free(seq);
+    free(pack);
+    return rc;
+}
+
+/* Full reduce-scatter in `order` with `dtype` gradients (grads[p * world + u]). */
+int oracle_rs_ex(int32_t world, int32_t dtype, int32_t order, int32_t node_size, int32_t nparams,
+                 const int64_t *dim0, const int64_t *row_numel, const void *const *grads, float alpha,
+                 int32_t accumulate, float *out, int64_t stride)
+{
+    const size_t esz = dtype == 0 ? 2u : 4u;
+    int64_t *R = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nparams > 0 ? nparams : 1));
+    int64_t *o = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nparams > 0 ? nparams : 1));
+    const void **src = (const void **)malloc(sizeof(void *) * (size_t)world);
+    int64_t S = 0;
+    int rc = ORACLE_OK;
+    if (!R || !o || !src) {
+        rc = ORACLE_ENOMEM;
+        goto done;
+    }
+    rc = oracle_geometry(world, nparams, dim0, row_numel, R, o, &S);
+    if (rc != ORACLE_OK)
+        goto done;
+    if (stride < S) {
+        rc = ORACLE_EINVAL;
+        goto done;
+    }
+    for (int32_t p = 0; p < nparams && rc == ORACLE_OK; ++p) {
+        int64_t K = row_numel[p];
+        for (int32_t r = 0; r < world && rc == ORACLE_OK; ++r) {
+            int64_t v = oracle_valid_rows(dim0[p], R[p], r);
+            for (int32_t u = 0; u < world; ++u)
+                src[u] = (const char *)grads[(size_t)p * (size_t)world + (size_t)u] +
+                         (size_t)r * (size_t)R[p] * (size_t)K * esz;
+            float *dst = out + (size_t)r * (size_t)stride + (size_t)o[p];
+            rc = oracle_rs_window_ex(world, (int32_t)(esz == 4), order, node_size, r, v * K, (R[p] - v) * K, src,
+                                     alpha, accumulate, dst, dst);
+        }
+    }
+done:
+    free(R);
+    free(o);
+    free((void *)src);
+    return rc;
+}

@@ -368,6 +368,115 @@ def pin_ag_cast_identity(orc, seed=23):
             assert_same_u16(full[p], want, f"AG_cast(shard(x)) W={W} p={p}")
 
 
+def pin_orders_closed_form(orc):
+    """Hand-worked values of the Section 4.3 orders (1.0 and 2^-24 terms):
+    * W=4, one node, destination 0 holding 1.0: the three staged 2^-24 add
+      exactly to 3*2^-24, then 1 + 3*2^-24 is 1.5 ulp: ties to even, 1 + 2^-22;
+      destinations 1..3 start from 1.0 and every +2^-24 ties back to 1.0.
+    * W=4 in nodes of 2, rank 0 holding 1.0: node 0 gives 1.0 (whichever rank
+      is last), node 1 gives 2^-23, the sum 1 + 2^-23 is exact.
+    * W=8 in nodes of 4: destination 0 (node 0's own rank is 0, added last):
+      node 0 = 1 + 3*2^-24 -> 1 + 2^-22, node 1 = 4*2^-24 = 2^-22, total
+      1 + 2^-21; destination 1 (rank 0 comes first): node 0 = 1.0, total 1 + 2^-22.
+    * W=8, one node, destination 3 holding 1.0: 7*2^-24 + 1 is 3.5 ulp: 1 + 2^-21."""
+    big, small = f32_to_bf16_bits([1.0])[0], f32_to_bf16_bits([U])[0]
+
+    def run(W, holder, order, L=0):
+        g = [[np.array([big if u == holder else small] * W, np.uint16) for u in range(W)]]
+        out = np.zeros((W, 1), np.float32)
+        orc.rs_ex(W, [(W, 1)], g, 1.0, False, out, order, L)
+        return out.reshape(-1)
+
+    e = np.float32
+    assert_same_f32(run(4, 0, "staged"), np.array([1 + 2 ** -22, 1, 1, 1], e), "staged W=4")
+    assert_same_f32(run(4, 0, "nodes", 2), np.full(4, 1 + 2 ** -23, e), "nodes W=4 L=2")
+    got = run(8, 0, "nodes", 4)
+    assert_same_f32(got[:2], np.array([1 + 2 ** -21, 1 + 2 ** -22], e), "nodes W=8 L=4")
+    assert_same_f32(run(8, 3, "staged")[3:4], np.array([1 + 2 ** -21], e), "staged W=8 dest 3")
+    assert_same_f32(run(8, 0, "nodes", 8), run(8, 0, "staged"), "nodes with L = W is the one-node order")
+    assert_same_f32(run(8, 0, "nodes", 1), run(8, 0, "rank"), "nodes of one rank is rank order")
+
+
+def pin_orders_brute_force(orc, seed=29):
+    from oracle import brute
+    rnd = random.Random(seed)
+    rng = np.random.default_rng(seed)
+    for c in range(24):
+        W = rnd.choice([1, 2, 3, 4, 6, 8])
+        order = rnd.choice(["rank", "staged", "nodes"])
+        L = rnd.choice([d for d in range(1, W + 1) if W % d == 0]) if order == "nodes" else 0
+        dims = [(rnd.choice([1, 2, W, W + 1, 2 * W + 1]), rnd.choice([1, 3, 4])) for _ in range(rnd.randint(1, 3))]
+        f32 = rnd.random() < 0.4
+        grads = [[(rng.standard_normal(d * k).astype(np.float32) if f32 else _rand_bits(rng, d * k))
+                  for _ in range(W)] for d, k in dims]
+        alpha, acc = rnd.choice([1.0, 0.25, -3.0]), rnd.random() < 0.5
+        _, _, S = orc.geometry(W, dims)
+        old = rng.standard_normal((W, S)).astype(np.float32)
+        out = old.copy()
+        orc.rs_ex(W, dims, grads, alpha, acc, out, order, L)
+        want = brute.reduce_scatter_ordered(W, dims, grads, alpha, acc, old, order, L)
+        assert_same_f32(out, want, f"ordered brute case {c}: W={W} {order} L={L} f32={f32}")
+
+
+def pin_orders_exact_and_bounded(orc, seed=37):
+    """Every order: integer inputs give the exact sum; normal inputs stay
+    within gamma_{W+1} (|alpha| sum |G| + |old|) of the fp64 sum and within
+    1e-6 of the rank-order result in the max-norm (the reordered-variant
+    tolerance); the rank order reproduces the original oracle bit for bit."""
+    rng = np.random.default_rng(seed)
+    for W, L in ((8, 4), (16, 4), (32, 8), (6, 3)):
+        dims = [(4 * W + 3, 9), (W, 1)]
+        ints = [[rng.integers(-128, 129, size=d * k) for _ in range(W)] for d, k in dims]
+        gi = [[f32_to_bf16_bits(x.astype(np.float32)) for x in per] for per in ints]
+        R, o, S = orc.geometry(W, dims)
+        for order in ("staged", "nodes"):
+            out = np.zeros((W, S), np.float32)
+            orc.rs_ex(W, dims, gi, 0.5, False, out, order, L)
+            for p, (d, k) in enumerate(dims):
+                exact = sum(ints[p][u] for u in range(W)).astype(np.float64) * 0.5
+                flat = np.concatenate([out[r, o[p]:o[p] + R[p] * k] for r in range(W)])[:d * k]
+                assert_same_f32(flat, exact.astype(np.float32), f"integer {order} W={W}")
+        g = [[_rand_bits(rng, d * k) for _ in range(W)] for d, k in dims]
+        ref = np.zeros((W, S), np.float32)
+        orc.rs(W, dims, g, 1.0, False, ref)
+        rank_ex = np.zeros((W, S), np.float32)
+        orc.rs_ex(W, dims, g, 1.0, False, rank_ex, "rank", 0)
+        assert_same_f32(rank_ex, ref, "rank order of the ordered oracle == original oracle")
+        gamma = (W + 1) * U / (1 - (W + 1) * U)
+        for order in ("staged", "nodes"):
+            out = np.zeros((W, S), np.float32)
+            orc.rs_ex(W, dims, g, 1.0, False, out, order, L)
+            for p, (d, k) in enumerate(dims):
+                vals = np.stack([bf16_bits_to_f32(g[p][u]).astype(np.float64) for u in range(W)])
+                got = np.concatenate([out[r, o[p]:o[p] + R[p] * k] for r in range(W)])[:d * k]
+                assert (np.abs(got - vals.sum(0)) <= gamma * np.abs(vals).sum(0) + 1e-45).all(), order
+                rk = np.concatenate([ref[r, o[p]:o[p] + R[p] * k] for r in range(W)])[:d * k]
+                assert np.abs(got - rk).max() <= 1e-6 * np.abs(rk).max(), f"{order} vs rank order"
+
+
+def pin_f32_grads_chunk_cat(orc, seed=41):
+    """fp32 gradients (b_grad = 4): torch._chunk_cat's pack of fp32 tensors
+    then a rank-ordered fp32 sum, against the oracle."""
+    rng = np.random.default_rng(seed)
+    for W, dims in ((4, [(333, 17), (7, 5), (64, 1)]), (3, [(5, 2), (1, 1)])):
+        grads = [[rng.standard_normal(d * k).astype(np.float32) for _ in range(W)] for d, k in dims]
+        _, _, S = orc.geometry(W, dims)
+        packs = []
+        for u in range(W):
+            ts = [torch.from_numpy(grads[p][u].reshape(d, k)) for p, (d, k) in enumerate(dims)]
+            t = torch.empty(W, S, dtype=torch.float32)
+            torch._chunk_cat(ts, dim=0, num_chunks=W, out=t)
+            packs.append(t)
+        acc = packs[0].clone()
+        for u in range(1, W):
+            acc = acc + packs[u]
+        want = (acc * torch.tensor(0.5, dtype=torch.float32)).numpy()
+        out = np.zeros((W, S), np.float32)
+        orc.rs_ex(W, dims, grads, 0.5, False, out, "rank", 0)
+        assert_same_f32(out, want, f"fp32 grads W={W}")
+
+
 ALL_PINS = [pin_golden, pin_slot_sizes, pin_torch_chunk, pin_chunk_cat, pin_brute_force, pin_integer_exact,
             pin_order_probe, pin_fp64_bound, pin_special_values, pin_ag_identity, pin_window_matches_full,
-            pin_cast_vs_torch, pin_ag_cast_identity]
+            pin_cast_vs_torch, pin_ag_cast_identity, pin_orders_closed_form, pin_orders_brute_force,
+            pin_orders_exact_and_bounded, pin_f32_grads_chunk_cat]

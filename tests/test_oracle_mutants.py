@@ -43,6 +43,15 @@ MUTANTS = {
     "cast_drops_nan": [("        return (uint16_t)((w >> 16) | 0x0040u);", "        return (uint16_t)0x7F80u;")],
     "ag_cast_drops_offset": [("const float *src_row = slots + (size_t)r * (size_t)stride + (size_t)o[p] +",
                               "const float *src_row = slots + (size_t)r * (size_t)stride +")],
+    "ex_negative_zero_padding": [("            dst[j] = +0.0f;", "            dst[j] = -0.0f;")],
+    "ex_unscaled_accumulate": [("out[j] = accumulate ? (old[j] + y) : y;", "out[j] = accumulate ? (old[j] + total) : y;")],
+    "ex_last_partial_dropped": [("for (int32_t g0 = 0; g0 < world; g0 += group) {",
+                                 "for (int32_t g0 = 0; g0 + group < world || g0 == 0; g0 += group) {")],
+    "staged_own_first": [("        seq[q] = r;\n", "        seq[q] = seq[0];\n        seq[0] = r;\n")],
+    "nodes_owner_fixed": [("int32_t owner = n * node_size + r % node_size;", "int32_t owner = n * node_size;")],
+    "nodes_as_one_chain": [("        *group = node_size;", "        *group = world;")],
+    "f32_grads_truncated": [("    return ((const float *)src)[j];",
+                             "    return bf16_to_f32((uint16_t)(((const uint32_t *)src)[j] >> 16));")],
     "ag_cast_transposed_rank": [("uint16_t *dst_row = full[p] + (size_t)((r * R[p] + i) * K);",
                                  "uint16_t *dst_row = full[p] + (size_t)((i * (int64_t)world + r) * K);")],
 }
