@@ -20,7 +20,8 @@ from ._binding import (  # noqa: F401  (re-exported C-ABI names)
     EXPORTED, LIB_PATH, TIDE_AG_CE_1D, TIDE_AG_CE_2D, TIDE_AG_SM, TIDE_DEBUG_HOST_ONLY, TIDE_DEBUG_SHORT_WAIT,
     TIDE_DEBUG_SKIP_FILL, TIDE_DTYPE_BF16,
     TIDE_ERR_ALIGNMENT, TIDE_ERR_CUDA, TIDE_ERR_INVALID_ARG, TIDE_ERR_OOM, TIDE_ERR_TIMEOUT, TIDE_ERR_UNSUPPORTED,
-    TIDE_KERNEL_AUTO, TIDE_KERNEL_BULK, TIDE_KERNEL_DIRECT, TIDE_OK, TIDE_ORDER_RANK_ASC, TIDE_SCHED_DYNAMIC,
+    TIDE_KERNEL_AUTO, TIDE_KERNEL_BULK, TIDE_KERNEL_DIRECT, TIDE_OK, TIDE_ORDER_NODES, TIDE_ORDER_RANK_ASC,
+    TIDE_ORDER_STAGED_OWN, TIDE_DTYPE_F32, TIDE_SCHED_DYNAMIC,
     TIDE_SCHED_STATIC, PlanFlags, TideError, load_library, make_flags, tide_ag_place, tide_ag_place_f32,
     tide_last_device_status,
     tide_last_error, tide_launch_count, tide_plan_build, tide_plan_destroy, tide_plan_fold_config,
@@ -39,9 +40,10 @@ def _stream_handle(stream) -> int:
     return stream.cuda_stream
 
 
-def _param_descs(grads, offsets=None, require_cuda=True):
+def _param_descs(grads, offsets=None, require_cuda=True, dtype=None):
     """grads[u][p] tensors -> descriptor tuples (pointers [W], dim0, row_numel, offset)."""
     import torch
+    dtype = dtype or torch.bfloat16
     W = len(grads)
     if W < 1:
         raise ValueError("need at least one rank")
@@ -54,8 +56,8 @@ def _param_descs(grads, offsets=None, require_cuda=True):
         ptrs = []
         for u in range(W):
             t = grads[u][p]
-            if t.dtype != torch.bfloat16:
-                raise TypeError(f"gradient [{u}][{p}] is {t.dtype}, expected bfloat16")
+            if t.dtype != dtype:
+                raise TypeError(f"gradient [{u}][{p}] is {t.dtype}, expected {dtype}")
             if t.shape != t0.shape:
                 raise ValueError(f"gradient [{u}][{p}] shape {tuple(t.shape)} != rank 0's {tuple(t0.shape)}")
             if not t.is_contiguous():
@@ -78,9 +80,11 @@ class Plan:
 
     def __init__(self, grads: Sequence[Sequence], flags: Optional[PlanFlags] = None, stream=None,
                  offsets: Optional[Sequence[int]] = None, host_only: bool = False):
+        import torch
         self.world = len(grads)
         self.shapes = [tuple(t.shape) for t in grads[0]]
-        descs = _param_descs(grads, offsets, require_cuda=not host_only)
+        self.grad_dtype = torch.float32 if (flags is not None and flags.grad_dtype == TIDE_DTYPE_F32) else torch.bfloat16
+        descs = _param_descs(grads, offsets, require_cuda=not host_only, dtype=self.grad_dtype)
         if host_only:
             flags = flags or make_flags()
             flags.debug |= TIDE_DEBUG_HOST_ONLY
@@ -89,7 +93,7 @@ class Plan:
         self.slot_numel = tide_plan_slot_numel(self.handle)
 
     def rebind(self, grads, stream=None):
-        tide_plan_rebind(self.handle, _param_descs(grads), _stream_handle(stream))
+        tide_plan_rebind(self.handle, _param_descs(grads, dtype=self.grad_dtype), _stream_handle(stream))
 
     def rs_fold(self, out, alpha: float = 1.0, accumulate: bool = False, stream=None):
         """out: fp32 CUDA tensor [W, stride] with unit inner stride (stride >= slot_numel)."""

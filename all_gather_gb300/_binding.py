@@ -23,11 +23,11 @@ TIDE_ERR_OOM = 4
 TIDE_ERR_CUDA = 5
 TIDE_ERR_TIMEOUT = 6
 # enums
-TIDE_ORDER_RANK_ASC = 0
+TIDE_ORDER_RANK_ASC, TIDE_ORDER_STAGED_OWN, TIDE_ORDER_NODES = 0, 1, 2
 TIDE_SCHED_STATIC, TIDE_SCHED_DYNAMIC = 0, 1
 TIDE_KERNEL_AUTO, TIDE_KERNEL_DIRECT, TIDE_KERNEL_BULK = 0, 1, 2
 TIDE_AG_SM, TIDE_AG_CE_2D, TIDE_AG_CE_1D = 0, 1, 2
-TIDE_DTYPE_BF16 = 0
+TIDE_DTYPE_BF16, TIDE_DTYPE_F32 = 0, 1
 TIDE_DEBUG_HOST_ONLY = 0x1
 TIDE_DEBUG_SHORT_WAIT = 0x2
 TIDE_DEBUG_SKIP_FILL = 0x4
@@ -54,7 +54,7 @@ class PlanFlags(ctypes.Structure):
     _fields_ = [("cta_budget", ctypes.c_int32), ("chunk_bytes", ctypes.c_int32), ("order", ctypes.c_int32),
                 ("sched", ctypes.c_int32), ("kernel", ctypes.c_int32), ("grad_dtype", ctypes.c_int32),
                 ("debug", ctypes.c_uint32), ("fill_bytes", ctypes.c_int32), ("fill_ranks", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 3)]
+                ("node_size", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
 
 
 class Segment(ctypes.Structure):
@@ -137,10 +137,11 @@ def _descs(params: Sequence[Tuple[Sequence[int], int, int, int]]):
 
 def make_flags(cta_budget=0, chunk_bytes=0, order=TIDE_ORDER_RANK_ASC, sched=TIDE_SCHED_STATIC,
                kernel=TIDE_KERNEL_AUTO, grad_dtype=TIDE_DTYPE_BF16, debug=0, fill_bytes=0,
-               fill_ranks=0) -> PlanFlags:
+               fill_ranks=0, node_size=0) -> PlanFlags:
     f = PlanFlags()
     f.cta_budget, f.chunk_bytes, f.order, f.sched = cta_budget, chunk_bytes, order, sched
     f.kernel, f.grad_dtype, f.debug, f.fill_bytes, f.fill_ranks = kernel, grad_dtype, debug, fill_bytes, fill_ranks
+    f.node_size = node_size
     return f
 
 

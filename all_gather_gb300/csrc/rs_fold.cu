@@ -387,33 +387,87 @@ constexpr int32_t kStatusConsumerTimeout = 1;
 constexpr int32_t kStatusProducerTimeout = 2;
 constexpr int32_t kStatusDrainTimeout = 3;
 
-// One element from global memory (pieces the producer does not stage).
-template <int WT, bool ACC>
-__device__ __forceinline__ void fold_scalar_global(const uint64_t *bp, int W, int64_t src_off, float *dst, float alpha)
+// Summation orders (Section 4.3).  The W contributions to destination rank
+// r are added in a sequence of positions q = 0..W-1; positions form groups
+// of `group` consecutive entries whose partials are added in sequence order.
+//   rank order:      q -> q, one group
+//   one-node order:  every rank but r ascending, then r, one group
+//   two-level order: node n = q / L: its ranks except n L + (r mod L)
+//                    ascending, then that rank; groups of L (node partials)
+__device__ __forceinline__ int seq_rank(int order, int q, int r, int W, int L)
 {
-    float acc = ld_bf16(reinterpret_cast<const uint16_t *>(bp[0]) + src_off);
-    for (int u = 1; u < (WT > 0 ? WT : W); ++u)
-        acc = __fadd_rn(acc, ld_bf16(reinterpret_cast<const uint16_t *>(bp[u]) + src_off));
-    float y = __fmul_rn(alpha, acc);
+    if (order == TIDE_ORDER_STAGED_OWN)
+        return q == W - 1 ? r : (q < r ? q : q + 1);
+    if (order == TIDE_ORDER_NODES) {
+        const int n = q / L, l = q - n * L, own = r % L;
+        return n * L + (l == L - 1 ? own : (l < own ? l : l + 1));
+    }
+    return q;
+}
+
+template <typename E>
+__device__ __forceinline__ float ld_elem(const E *p);
+template <>
+__device__ __forceinline__ float ld_elem<uint16_t>(const uint16_t *p)
+{
+    return ld_bf16(p);
+}
+template <>
+__device__ __forceinline__ float ld_elem<float>(const float *p)
+{
+    return __ldg(p);
+}
+
+// One element from global memory (pieces or tails the producer does not
+// stage), in the plan's order.
+template <bool ACC, typename E>
+__device__ void fold_scalar_global(const uint64_t *bp, const FoldParams &fp, int r, int64_t src_off, float *dst)
+{
+    const int W = fp.world;
+    const int group = fp.order == TIDE_ORDER_NODES ? fp.node_size : W;
+    float total = 0.0f, part = 0.0f;
+    for (int q = 0; q < W; ++q) {
+        const int u = seq_rank(fp.order, q, r, W, fp.node_size);
+        const float x = ld_elem<E>(reinterpret_cast<const E *>(bp[u]) + src_off);
+        const int l = q % group;
+        part = l == 0 ? x : __fadd_rn(part, x);
+        if (l == group - 1)
+            total = q < group ? part : __fadd_rn(total, part);
+    }
+    float y = __fmul_rn(fp.alpha, total);
     if (ACC)
         y = __fadd_rn(*dst, y);
     __stcs(dst, y);
 }
 
-template <int WT, bool ACC>
-__global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParams fp)
+// Eight consecutive elements of one rank from a shared-memory stage.
+__device__ __forceinline__ void lds8(const uint16_t *p, float (&f)[8]) { unpack8(lds_v4(p), f); }
+__device__ __forceinline__ void lds8(const float *p, float (&f)[8])
+{
+    const float4 a = *reinterpret_cast<const float4 *>(p);
+    const float4 b = *reinterpret_cast<const float4 *>(p + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+// ACC: accumulate into the existing shard.  E: gradient element (uint16_t =
+// bf16, float = fp32).  GROUPED: the two-level order (node partials); other
+// orders are one chain whose sequence the producer applies when it stages.
+template <bool ACC, typename E, bool GROUPED>
+__global__ void __launch_bounds__(kBulkThreads, 2) fold_bulk_kernel(const FoldParams fp)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    const int W = WT > 0 ? WT : fp.world;
+    const int W = fp.world;
     const int RG = fp.fill_ranks;          // ranks per stage fill
     const int NG = (W + RG - 1) / RG;      // fills per chunk of FILL elements
     const int STAGES = fp.stages;
     const int64_t FILL = fp.fill_elems;
+    const int L = GROUPED ? fp.node_size : W;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + STAGES;
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(empty + STAGES);
-    const uint16_t **src_cache = reinterpret_cast<const uint16_t **>(empty + STAGES + 1);  // producer's W pointers
-    uint16_t *ring = reinterpret_cast<uint16_t *>(smem + bulk_ring_offset(STAGES, W));
+    const E **src_cache = reinterpret_cast<const E **>(empty + STAGES + 1);  // producer's W pointers, in order
+    E *ring = reinterpret_cast<E *>(smem + bulk_ring_offset(STAGES, W));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float alpha = fp.alpha;
 
@@ -432,7 +486,7 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
             return;
         // ------------------------------------------------------------ producer
         // For every chunk of FILL elements of a work item, NG stage fills of
-        // RG ranks each, in rank order.
+        // RG ranks each, in the plan's summation sequence.
         uint32_t stage = 0, phase = 0;
         int64_t fills = 0, skipped = -1;
         bool stop = false;
@@ -444,11 +498,11 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
             const int64_t count = int64_t(item.count_kind & ~kItemPad);
             const uint64_t *bp = fp.ptrs + int64_t(seg.param) * W;
             const int64_t base = seg.src_elem + item.begin;
-            for (int u = 0; u < W; ++u)
-                src_cache[u] = reinterpret_cast<const uint16_t *>(bp[u]) + base;
+            for (int q = 0; q < W; ++q)
+                src_cache[q] = reinterpret_cast<const E *>(bp[seq_rank(fp.order, q, seg.rank, W, fp.node_size)]) + base;
             for (int64_t c = 0; c < count && !stop; c += FILL) {
                 const int64_t len = count - c < FILL ? count - c : FILL;
-                const uint32_t bytes = uint32_t(len & ~int64_t(7)) * 2u;
+                const uint32_t bytes = uint32_t(len & ~int64_t(7)) * uint32_t(sizeof(E));
                 for (int g = 0; g < NG; ++g) {
                     const int u0 = g * RG;
                     const int nr = W - u0 < RG ? W - u0 : RG;
@@ -464,7 +518,7 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
                     } else {
                         mbar_arrive_expect_tx(&full[stage], uint32_t(nr) * bytes);
                         if (bytes) {
-                            uint16_t *dst = ring + size_t(stage) * RG * FILL;
+                            E *dst = ring + size_t(stage) * RG * FILL;
 #pragma unroll 4
                             for (int j = 0; j < nr; ++j)
                                 bulk_copy_g2s(dst + size_t(j) * FILL, src_cache[u0 + j] + c, bytes, &full[stage]);
@@ -493,7 +547,7 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
     // ---------------------------------------------------------------- consumers
     // Each consumer thread owns up to kBulkMaxVec 8-element vectors of a
     // chunk and keeps their fp32 sums in registers across the chunk's NG
-    // fills, so the ranks are added in order 0, 1, ..., W-1.
+    // fills, so the contributions are added in the plan's sequence.
     const int ctid = threadIdx.x - 32;
     constexpr int NCT = 32 * kBulkConsumerWarps;
     uint32_t stage = 0, phase = 0;
@@ -512,7 +566,7 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
         }
         if (seg.src_phase != 0) {
             for (int64_t e = ctid; e < count; e += NCT)
-                fold_scalar_global<WT, ACC>(bp, W, seg.src_elem + item.begin + e, dst + e, alpha);
+                fold_scalar_global<ACC, E>(bp, fp, seg.rank, seg.src_elem + item.begin + e, dst + e);
             continue;
         }
         const bool dst_vec = (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
@@ -520,6 +574,7 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
             const int64_t len = count - c < FILL ? count - c : FILL;
             const int64_t nv = len >> 3;
             float acc[kBulkMaxVec][8];
+            float part[GROUPED ? kBulkMaxVec : 1][8];
             float old[kBulkMaxVec][8];
             if (ACC) {
                 // Issue the loads of the existing shard values before waiting
@@ -540,23 +595,40 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
                     *abort_flag = 1;
                     return;
                 }
-                const uint16_t *sb = ring + size_t(stage) * RG * FILL;
+                const E *sb = ring + size_t(stage) * RG * FILL;
 #pragma unroll
                 for (int k = 0; k < kBulkMaxVec; ++k) {
                     const int64_t v = ctid + int64_t(k) * NCT;
                     if (v < nv) {
-                        int j0 = 0;
-                        if (g == 0) {
-                            unpack8(lds_v4(sb + v * 8), acc[k]);
-                            j0 = 1;
-                        }
+                        if (!GROUPED) {
+                            int j0 = 0;
+                            if (g == 0) {
+                                lds8(sb + v * 8, acc[k]);
+                                j0 = 1;
+                            }
 #pragma unroll 4
-                        for (int j = j0; j < nr; ++j) {
-                            float f[8];
-                            unpack8(lds_v4(sb + size_t(j) * FILL + v * 8), f);
+                            for (int j = j0; j < nr; ++j) {
+                                float f[8];
+                                lds8(sb + size_t(j) * FILL + v * 8, f);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                acc[k][e] = __fadd_rn(acc[k][e], f[e]);
+                                for (int e = 0; e < 8; ++e)
+                                    acc[k][e] = __fadd_rn(acc[k][e], f[e]);
+                            }
+                        } else {
+                            const int kk = GROUPED ? k : 0;
+                            for (int j = 0; j < nr; ++j) {
+                                float f[8];
+                                lds8(sb + size_t(j) * FILL + v * 8, f);
+                                const int q = u0 + j, l = q % L;
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    part[kk][e] = l == 0 ? f[e] : __fadd_rn(part[kk][e], f[e]);
+                                if (l == L - 1) {
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e)
+                                        acc[k][e] = q < L ? part[kk][e] : __fadd_rn(acc[k][e], part[kk][e]);
+                                }
+                            }
                         }
                     }
                 }
@@ -575,34 +647,29 @@ __global__ void __launch_bounds__(kBulkThreads) fold_bulk_kernel(const FoldParam
                     store8_onto<ACC>(dst + c + v * 8, acc[k], old[k], alpha, dst_vec);
             }
             for (int64_t e = nv * 8 + ctid; e < len; e += NCT)
-                fold_scalar_global<WT, ACC>(bp, W, seg.src_elem + item.begin + c + e, dst + c + e, alpha);
+                fold_scalar_global<ACC, E>(bp, fp, seg.rank, seg.src_elem + item.begin + c + e, dst + c + e);
         }
     }
 }
 
 template <bool ACC>
-FoldKernel pick_bulk(int world)
+FoldKernel pick_bulk(int dtype, int order)
 {
-    switch (world) {
-    case 1: return fold_bulk_kernel<1, ACC>;
-    case 2: return fold_bulk_kernel<2, ACC>;
-    case 4: return fold_bulk_kernel<4, ACC>;
-    case 8: return fold_bulk_kernel<8, ACC>;
-    case 16: return fold_bulk_kernel<16, ACC>;
-    case 32: return fold_bulk_kernel<32, ACC>;
-    default: return fold_bulk_kernel<0, ACC>;
-    }
+    const bool grouped = order == TIDE_ORDER_NODES;
+    if (dtype == TIDE_DTYPE_F32)
+        return grouped ? fold_bulk_kernel<ACC, float, true> : fold_bulk_kernel<ACC, float, false>;
+    return grouped ? fold_bulk_kernel<ACC, uint16_t, true> : fold_bulk_kernel<ACC, uint16_t, false>;
 }
 
 }  // namespace
 
-BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_sm)
+BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_sm, int elem_bytes)
 {
     // Default: 4 KB of each of up to 8 ranks per stage fill (32 KB stages),
     // three stages per CTA, two CTAs per SM.  Wider groups take several fills
     // per chunk; the consumers keep the partial sums in registers meanwhile.
     BulkShape b{};
-    int64_t fill = fill_elems > 0 ? fill_elems : 2048;
+    int64_t fill = fill_elems > 0 ? fill_elems : 4096 / elem_bytes;
     if (fill > kBulkMaxFill)
         fill = kBulkMaxFill;
     fill &= ~int64_t(7);
@@ -611,9 +678,9 @@ BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_s
     int rg = fill_ranks > 0 ? fill_ranks : 8;
     if (rg > world)
         rg = world;
-    while (fill > 8 && fill * rg * 2 * 2 > 200 * 1024)  // two stages must fit in shared memory
+    while (fill > 8 && fill * rg * elem_bytes * 2 > 200 * 1024)  // two stages must fit in shared memory
         fill = (fill / 2) & ~int64_t(7);
-    const int64_t stage_bytes = fill * rg * 2;
+    const int64_t stage_bytes = fill * rg * elem_bytes;
     // A CTA that has an SM to itself (small CTA budgets) takes twice the ring.
     int64_t stages = (whole_sm ? 2 * kBulkSmemTarget : kBulkSmemTarget) / stage_bytes;
     if (stages > 16)
@@ -627,18 +694,18 @@ BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_s
     return b;
 }
 
-size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems, int fill_ranks, bool whole_sm)
+size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems, int fill_ranks, bool whole_sm, int elem_bytes)
 {
     if (kernel == TIDE_KERNEL_BULK)
-        return bulk_shape(world, fill_elems, fill_ranks, whole_sm).smem_bytes;
+        return bulk_shape(world, fill_elems, fill_ranks, whole_sm, elem_bytes).smem_bytes;
     return size_t(world) * sizeof(uint64_t);
 }
 
-cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *blocks_per_sm)
+cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *blocks_per_sm, int dtype, int order)
 {
     if (kernel == TIDE_KERNEL_BULK) {
-        // Allow the device maximum once per kernel: the generic-world instance
-        // serves several stage sizes.
+        // Allow the device maximum once per kernel instance: it serves every
+        // world size and stage shape.
         int dev = 0, optin = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess)
@@ -648,12 +715,13 @@ cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *b
         if (smem > size_t(optin))
             return cudaErrorInvalidValue;
         for (int acc = 0; acc < 2; ++acc) {
-            FoldKernel k = acc ? pick_bulk<true>(world) : pick_bulk<false>(world);
+            FoldKernel k = acc ? pick_bulk<true>(dtype, order) : pick_bulk<false>(dtype, order);
             e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
             if (e != cudaSuccess)
                 return e;
         }
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, pick_bulk<false>(world), block, smem);
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, pick_bulk<false>(dtype, order), block,
+                                                             smem);
     }
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, pick_direct<false>(world), block, smem);
 }
@@ -663,7 +731,7 @@ cudaError_t launch_fold(const FoldParams &fp, int kernel, int accumulate, int gr
 {
     FoldKernel k;
     if (kernel == TIDE_KERNEL_BULK)
-        k = accumulate ? pick_bulk<true>(fp.world) : pick_bulk<false>(fp.world);
+        k = accumulate ? pick_bulk<true>(fp.dtype, fp.order) : pick_bulk<false>(fp.dtype, fp.order);
     else
         k = accumulate ? pick_direct<true>(fp.world) : pick_direct<false>(fp.world);
     k<<<grid, block, smem, stream>>>(fp);

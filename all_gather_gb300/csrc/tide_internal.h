@@ -68,6 +68,9 @@ struct FoldParams {
     int32_t fill_elems;       // elements per rank per stage fill (multiple of 8)
     int32_t fill_ranks;       // ranks per stage fill
     int32_t stages;           // ring depth
+    int32_t order;            // TIDE_ORDER_*
+    int32_t node_size;        // ranks per node of TIDE_ORDER_NODES
+    int32_t dtype;            // TIDE_DTYPE_* of the gradients
 };
 
 // Stage geometry of the bulk kernel for a world size.
@@ -78,7 +81,7 @@ struct BulkShape {
     size_t smem_bytes;
 };
 // fill_elems / fill_ranks 0 = default; whole_sm: the grid has at most one CTA per SM
-BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_sm);
+BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_sm, int elem_bytes);
 
 struct AgParams {
     const Seg *segs;
@@ -95,8 +98,10 @@ struct AgParams {
 // Launchers (rs_fold.cu / ag_place.cu).  Return cudaGetLastError() of the launch.
 cudaError_t launch_fold(const FoldParams &fp, int kernel, int accumulate, int grid, int block, size_t smem,
                         cudaStream_t stream);
-cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *blocks_per_sm);
-size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems, int fill_ranks, bool whole_sm);
+cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *blocks_per_sm,
+                           int dtype = TIDE_DTYPE_BF16, int order = TIDE_ORDER_RANK_ASC);
+size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems, int fill_ranks, bool whole_sm,
+                       int elem_bytes = 2);
 cudaError_t launch_ag(const AgParams &ap, int grid, cudaStream_t stream);
 cudaError_t launch_ag_f32(const AgParams &ap, int grid, cudaStream_t stream);
 
@@ -124,6 +129,7 @@ struct tide_plan {
     int32_t grid = 0, block = 0, sms = 0;
     size_t fold_smem = 0;
     int kernel = TIDE_KERNEL_DIRECT;
+    int elem_bytes = 2;                  // gradient element size (bf16 2, fp32 4)
     bool whole_sm = false;               // bulk kernel: at most one CTA per SM (deeper ring)
     bool host_only = false;
     int device = -1;

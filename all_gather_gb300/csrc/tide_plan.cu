@@ -54,11 +54,13 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Source phase of a piece: (address / 2) mod 8 of rank u's first element when
 // every rank agrees, else -1 (the fold then uses scalar loads for it).
-int32_t piece_phase(const uint64_t *ptrs_p, int32_t W, int64_t src_elem)
+int32_t piece_phase(const uint64_t *ptrs_p, int32_t W, int64_t src_elem, int elem_bytes)
 {
+    const int shift = elem_bytes == 4 ? 2 : 1;
+    const uint64_t mask = uint64_t(16 / elem_bytes - 1);
     int32_t ph = -1;
     for (int32_t u = 0; u < W; ++u) {
-        int32_t x = int32_t(((ptrs_p[u] >> 1) + uint64_t(src_elem)) & 7u);
+        int32_t x = int32_t(((ptrs_p[u] >> shift) + uint64_t(src_elem)) & mask);
         if (u == 0)
             ph = x;
         else if (x != ph)
@@ -69,7 +71,7 @@ int32_t piece_phase(const uint64_t *ptrs_p, int32_t W, int64_t src_elem)
 
 tide_status_t check_flags(const tide_plan_flags_t &f)
 {
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < 2; ++i)
         if (f.reserved[i] != 0)
             return fail(TIDE_ERR_INVALID_ARG, "flags.reserved[%d] must be zero", i);
     if (f.fill_bytes != 0 && (f.fill_bytes < 16 || f.fill_bytes % 16 != 0 || f.fill_bytes > 4096))
@@ -82,14 +84,20 @@ tide_status_t check_flags(const tide_plan_flags_t &f)
     if (f.chunk_bytes != 0 && (f.chunk_bytes < 256 || f.chunk_bytes % 256 != 0 || f.chunk_bytes > (1 << 26)))
         return fail(TIDE_ERR_INVALID_ARG, "flags.chunk_bytes %d: need 0 or a multiple of 256 in [256, 2^26]",
                     f.chunk_bytes);
-    if (f.order != TIDE_ORDER_RANK_ASC)
+    if (f.order != TIDE_ORDER_RANK_ASC && f.order != TIDE_ORDER_STAGED_OWN && f.order != TIDE_ORDER_NODES)
         return fail(TIDE_ERR_UNSUPPORTED, "flags.order %d is not implemented", f.order);
+    if (f.order == TIDE_ORDER_NODES ? f.node_size < 1 : f.node_size != 0)
+        return fail(TIDE_ERR_INVALID_ARG, "flags.node_size %d (positive with TIDE_ORDER_NODES only)", f.node_size);
     if (f.sched != TIDE_SCHED_STATIC && f.sched != TIDE_SCHED_DYNAMIC)
         return fail(TIDE_ERR_INVALID_ARG, "flags.sched %d", f.sched);
     if (f.kernel != TIDE_KERNEL_AUTO && f.kernel != TIDE_KERNEL_DIRECT && f.kernel != TIDE_KERNEL_BULK)
         return fail(TIDE_ERR_INVALID_ARG, "flags.kernel %d", f.kernel);
-    if (f.grad_dtype != TIDE_DTYPE_BF16)
+    if (f.grad_dtype != TIDE_DTYPE_BF16 && f.grad_dtype != TIDE_DTYPE_F32)
         return fail(TIDE_ERR_UNSUPPORTED, "flags.grad_dtype %d is not implemented", f.grad_dtype);
+    if ((f.order != TIDE_ORDER_RANK_ASC || f.grad_dtype != TIDE_DTYPE_BF16) &&
+        (f.kernel == TIDE_KERNEL_DIRECT || f.sched == TIDE_SCHED_DYNAMIC))
+        return fail(TIDE_ERR_UNSUPPORTED,
+                    "orders other than rank order and fp32 gradients run on the statically scheduled bulk kernel");
     if (f.debug & ~(TIDE_DEBUG_HOST_ONLY | TIDE_DEBUG_SHORT_WAIT | TIDE_DEBUG_SKIP_FILL))
         return fail(TIDE_ERR_INVALID_ARG, "unknown debug bits 0x%x", f.debug);
     if (f.kernel == TIDE_KERNEL_BULK && f.sched == TIDE_SCHED_DYNAMIC)
@@ -113,19 +121,20 @@ tide_status_t load_pointers(tide_plan_t *plan, const tide_param_desc_t *params)
             uintptr_t a = reinterpret_cast<uintptr_t>(params[p].rank_base[u]);
             if (numel > 0 && a == 0)
                 return fail(TIDE_ERR_INVALID_ARG, "params[%d].rank_base[%d] is NULL", p, u);
-            if (a & 1u)
-                return fail(TIDE_ERR_ALIGNMENT, "params[%d].rank_base[%d] is not 2-byte aligned", p, u);
+            if (a & uintptr_t(plan->elem_bytes - 1))
+                return fail(TIDE_ERR_ALIGNMENT, "params[%d].rank_base[%d] is not %d-byte aligned", p, u,
+                            plan->elem_bytes);
             plan->ptrs[size_t(p) * W + u] = a;
             if (numel > 0) {
                 lo = std::min(lo, a);
-                hi = std::max(hi, a + uintptr_t(numel) * 2u);
+                hi = std::max(hi, a + uintptr_t(numel) * uintptr_t(plan->elem_bytes));
             }
         }
     }
     plan->src_lo = lo;
     plan->src_hi = hi;
     for (auto &s : plan->segs)
-        s.src_phase = piece_phase(&plan->ptrs[size_t(s.param) * W], W, s.src_elem);
+        s.src_phase = piece_phase(&plan->ptrs[size_t(s.param) * W], W, s.src_elem, plan->elem_bytes);
     return TIDE_OK;
 }
 
@@ -137,7 +146,7 @@ bool overlaps_gradients(const tide_plan_t *plan, uintptr_t lo, uintptr_t hi)
     if (lo >= hi || !ranges_overlap(lo, hi, plan->src_lo, plan->src_hi))
         return false;
     for (int32_t p = 0; p < plan->nparams; ++p) {
-        const uintptr_t bytes = uintptr_t(plan->dim0[p] * plan->row_numel[p]) * 2u;
+        const uintptr_t bytes = uintptr_t(plan->dim0[p] * plan->row_numel[p]) * uintptr_t(plan->elem_bytes);
         for (int32_t u = 0; u < plan->world; ++u) {
             uintptr_t a = plan->ptrs[size_t(p) * plan->world + u];
             if (bytes && ranges_overlap(lo, hi, a, a + bytes))
@@ -254,6 +263,9 @@ tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_para
     plan->host_only = (f.debug & TIDE_DEBUG_HOST_ONLY) != 0;
     plan->chunk_elems = (f.chunk_bytes ? f.chunk_bytes : tide::kDefaultChunkBytes) / 2;
     plan->kernel = f.kernel == TIDE_KERNEL_AUTO ? TIDE_KERNEL_BULK : f.kernel;
+    plan->elem_bytes = f.grad_dtype == TIDE_DTYPE_F32 ? 4 : 2;
+    if (f.order == TIDE_ORDER_NODES && world % f.node_size != 0)
+        return bail(fail(TIDE_ERR_INVALID_ARG, "node_size %d does not divide world %d", f.node_size, world));
     if (f.kernel == TIDE_KERNEL_AUTO && f.sched == TIDE_SCHED_DYNAMIC)
         plan->kernel = TIDE_KERNEL_DIRECT;  // only the direct kernel claims items dynamically
 
@@ -345,7 +357,8 @@ tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_para
         return bail(fail(TIDE_ERR_UNSUPPORTED, "too many work items; raise chunk_bytes"));
 
     plan->block = plan->kernel == TIDE_KERNEL_BULK ? tide::kBulkThreads : tide::kFoldThreads;
-    plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, f.fill_bytes / 2, f.fill_ranks, false);
+    plan->fold_smem =
+        tide::fold_smem_bytes(plan->kernel, world, f.fill_bytes / plan->elem_bytes, f.fill_ranks, false, plan->elem_bytes);
     if (plan->host_only) {
         plan->grid = f.cta_budget ? f.cta_budget : 0;
         *plan_out = plan;
@@ -363,9 +376,10 @@ tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_para
     plan->sms = sms;
     plan->whole_sm = plan->kernel == TIDE_KERNEL_BULK && f.cta_budget > 0 && f.cta_budget <= sms;
     if (plan->whole_sm)
-        plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, f.fill_bytes / 2, f.fill_ranks, true);
+        plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, f.fill_bytes / plan->elem_bytes, f.fill_ranks,
+                                                true, plan->elem_bytes);
     int per_sm = 0;
-    e = tide::fold_occupancy(plan->kernel, world, plan->block, plan->fold_smem, &per_sm);
+    e = tide::fold_occupancy(plan->kernel, world, plan->block, plan->fold_smem, &per_sm, f.grad_dtype, f.order);
     if (e != cudaSuccess)
         return bail(cuda_fail(e, "fold occupancy"));
     if (per_sm < 1)
@@ -486,8 +500,11 @@ tide_status_t tide_rs_fold(tide_plan_t *plan, float *out_base, int64_t out_slot_
     fp.status = plan->d_status;
     fp.debug = plan->flags.debug;
     fp.wait_budget_ns = (plan->flags.debug & TIDE_DEBUG_SHORT_WAIT) ? tide::kShortWaitBudgetNs : tide::kWaitBudgetNs;
-    const tide::BulkShape bs =
-        tide::bulk_shape(plan->world, plan->flags.fill_bytes / 2, plan->flags.fill_ranks, plan->whole_sm);
+    const tide::BulkShape bs = tide::bulk_shape(plan->world, plan->flags.fill_bytes / plan->elem_bytes,
+                                                plan->flags.fill_ranks, plan->whole_sm, plan->elem_bytes);
+    fp.order = plan->flags.order;
+    fp.node_size = plan->flags.node_size;
+    fp.dtype = plan->flags.grad_dtype;
     fp.fill_elems = bs.fill_elems;
     fp.fill_ranks = bs.fill_ranks;
     fp.stages = bs.stages;

@@ -435,7 +435,7 @@ def run_ours(args):
 
     # the other placement engines and the mixed-precision placement, timed alone after the step
     if rank == 0 and not args.no_variants:
-        result["variants"] = time_variants(plan, w, S, slots, full, dev, steps=min(K, 20))
+        result["variants"] = time_variants(plan, w, S, slots, full, dev, gs.views, steps=min(K, 20))
 
     # two-pass stock-FSDP2-style baseline (chunk_cat pack to fp32, then reduce), timed alone
     if not args.no_baseline and rank == 0:
@@ -470,10 +470,11 @@ def run_ours(args):
     return 0
 
 
-def time_variants(plan, w, S, slots, full, dev, steps: int = 20) -> dict:
-    """Mean event time of each placement variant over `steps` launches."""
+def time_variants(plan, w, S, slots, full, dev, gs_views, steps: int = 20) -> dict:
+    """Mean event time of each placement and fold variant over `steps` launches."""
     import torch
 
+    import all_gather_gb300 as tide
     import workloads
     N = w.total_numel()
     slots32 = torch.stack([workloads.normal_fp32(S, workloads.slot_seed(w, r), 0.02, dev) for r in range(w.world)])
@@ -483,6 +484,23 @@ def time_variants(plan, w, S, slots, full, dev, steps: int = 20) -> dict:
         "ag_place ce2d (copy engines, one 2D copy per parameter)": (lambda: plan.ag_place(slots, full, "ce2d"), 4 * N),
         "ag_place ce1d (copy engines, one copy per piece)": (lambda: plan.ag_place(slots, full, "ce1d"), 4 * N),
     }
+    # the fold in the other Section 4.3 orders, and with fp32 gradients
+    out_v = torch.zeros(w.world, S, device=dev)
+    rs_b = w.world * N * 2 + N * 4 + (N * 4 if w.accumulate else 0)
+    L = max(1, w.world // 2)
+    plans = {
+        "rs_fold order=staged_own (one-node Level 1 order)": tide.Plan(
+            gs_views, tide.make_flags(order=tide.TIDE_ORDER_STAGED_OWN)),
+        f"rs_fold order=nodes node_size={L} (two-level order)": tide.Plan(
+            gs_views, tide.make_flags(order=tide.TIDE_ORDER_NODES, node_size=L)),
+    }
+    for name, pl in plans.items():
+        calls[name] = ((lambda pl=pl: pl.rs_fold(out_v, alpha=w.alpha, accumulate=w.accumulate)), rs_b)
+    grads32 = [[v.float() for v in vs] for vs in gs_views]
+    plan32 = tide.Plan(grads32, tide.make_flags(grad_dtype=tide.TIDE_DTYPE_F32))
+    calls["rs_fold fp32 gradients (b_grad = 4)"] = (
+        lambda: plan32.rs_fold(out_v, alpha=w.alpha, accumulate=w.accumulate),
+        w.world * N * 4 + N * 4 + (N * 4 if w.accumulate else 0))
     res = {}
     for name, (fn, nbytes) in calls.items():
         for _ in range(3):
@@ -496,7 +514,10 @@ def time_variants(plan, w, S, slots, full, dev, steps: int = 20) -> dict:
         torch.cuda.synchronize()
         ms = s.elapsed_time(e) / steps
         res[name] = {"ms": round(ms, 4), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "alg_bytes": nbytes}
-    del slots32
+    for pl in list(plans.values()) + [plan32]:
+        pl.close()
+    del slots32, grads32, out_v
+    torch.cuda.empty_cache()
     return res
 
 

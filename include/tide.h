@@ -72,10 +72,11 @@ typedef struct tide_plan tide_plan_t;
 
 /* One parameter of the group (Section 2.1 notation). */
 typedef struct {
-    /* Host array of W device pointers: rank_base[u] is G_p^(u), the bf16
-     * gradient of this parameter on virtual rank u, row-major and contiguous
-     * (dim0 * row_numel elements).  2-byte aligned; 16-byte alignment enables
-     * the vector path.  The array itself is copied during the call. */
+    /* Host array of W device pointers: rank_base[u] is G_p^(u), the gradient
+     * of this parameter on virtual rank u (bf16, or fp32 with
+     * TIDE_DTYPE_F32), row-major and contiguous (dim0 * row_numel elements).
+     * Aligned to the element size; 16-byte alignment enables the vector and
+     * bulk-copy paths.  The array itself is copied during the call. */
     const void *const *rank_base;
     int64_t dim0;          /* D_p >= 0: extent of dimension 0 (0 = empty tensor, pointers may be NULL) */
     int64_t row_numel;     /* K_p >= 0: product of the trailing dimensions (1 for a vector) */
@@ -84,9 +85,18 @@ typedef struct {
                               make two shards overlap. */
 } tide_param_desc_t;
 
-/* Summation order of the reduce-scatter fold. */
+/* Summation order of the reduce-scatter fold (Section 4.3).  Every order is
+ * deterministic (bitwise reproducible for a plan); orders other than rank
+ * order differ from it by rounding only (within 1e-6 of it in the max-norm
+ * on the benchmark workloads). */
 enum {
-    TIDE_ORDER_RANK_ASC = 0  /* ((G0 + G1) + G2) + ... : the bit-exact contract */
+    TIDE_ORDER_RANK_ASC = 0,   /* ((G0 + G1) + G2) + ... : the bit-exact contract */
+    TIDE_ORDER_STAGED_OWN = 1, /* one node (Level 1): every rank except the destination r in
+                                  ascending order, then r's own contribution */
+    TIDE_ORDER_NODES = 2       /* two levels: W = M nodes of node_size ranks; each node's partial
+                                  adds its ranks except n*node_size + (r mod node_size) in
+                                  ascending order, then that rank; the node partials are then
+                                  added in node order */
 };
 
 /* Work distribution of the fold's persistent grid (bitwise identical results). */
@@ -111,9 +121,10 @@ enum {
     TIDE_AG_CE_1D = 2    /* copy engines: one 1D copy per (parameter, rank) piece */
 };
 
-/* Gradient element type. */
+/* Gradient element type (b_grad of Section 2.1). */
 enum {
-    TIDE_DTYPE_BF16 = 0
+    TIDE_DTYPE_BF16 = 0,  /* widened exactly to fp32 */
+    TIDE_DTYPE_F32 = 1    /* fp32 gradients, summed as they are */
 };
 
 /* Debug bits. */
@@ -136,7 +147,8 @@ typedef struct {
                              (multiple of 16, at most 4096); 0 = 4096 */
     int32_t fill_ranks;   /* bulk kernel: ranks per stage fill (0 = min(W, 8)); wider groups take
                              several fills per chunk, summed in registers in rank order */
-    int32_t reserved[3];  /* must be zero */
+    int32_t node_size;    /* TIDE_ORDER_NODES: ranks per node, dividing the world; else 0 */
+    int32_t reserved[2];  /* must be zero */
 } tide_plan_flags_t;
 
 /* Read-only view of one (parameter, rank) shard piece of a plan. */
@@ -157,9 +169,11 @@ typedef struct {
  * asynchronous copies on `stream`.  `params` is a host array; `flags` may be
  * NULL for defaults.  On success *plan_out owns the tables.
  * Errors: INVALID_ARG (world, counts, dims, null pointers, overlapping
- * explicit offsets, nonzero reserved fields), ALIGNMENT (a gradient pointer
- * not 2-byte aligned), UNSUPPORTED (an order, dtype or kernel this build
- * lacks), OOM, CUDA.
+ * explicit offsets, nonzero reserved fields, node_size not dividing world),
+ * ALIGNMENT (a gradient pointer not aligned to its element size),
+ * UNSUPPORTED (a combination this build lacks: orders other than rank order
+ * and fp32 gradients run on the bulk kernel with static scheduling only),
+ * OOM, CUDA.
  */
 TIDE_API tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_param_desc_t *params,
                               const tide_plan_flags_t *flags, void *stream, tide_plan_t **plan_out);

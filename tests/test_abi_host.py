@@ -137,6 +137,9 @@ def test_empty_group(tide):
     ("neg_offset", "TIDE_ERR_INVALID_ARG"), ("sched", "TIDE_ERR_INVALID_ARG"),
     ("fill", "TIDE_ERR_INVALID_ARG"), ("bulk_dynamic", "TIDE_ERR_UNSUPPORTED"),
     ("skip_fill_direct", "TIDE_ERR_INVALID_ARG"), ("debug_bits", "TIDE_ERR_INVALID_ARG"),
+    ("node_size_not_dividing", "TIDE_ERR_INVALID_ARG"), ("node_size_without_nodes", "TIDE_ERR_INVALID_ARG"),
+    ("nodes_without_size", "TIDE_ERR_INVALID_ARG"), ("staged_direct", "TIDE_ERR_UNSUPPORTED"),
+    ("f32_dynamic", "TIDE_ERR_UNSUPPORTED"), ("f32_misaligned", "TIDE_ERR_ALIGNMENT"),
 ])
 def test_build_validation(tide, case, status):
     W, dims = 4, [(8, 8), (5, 1)]
@@ -160,7 +163,7 @@ def test_build_validation(tide, case, status):
     elif case == "order":
         kw["order"] = 7
     elif case == "dtype":
-        kw["grad_dtype"] = 1
+        kw["grad_dtype"] = 7
     elif case == "overflow":
         dims = [(1 << 40, 1 << 30), (5, 1)]
     elif case == "neg_offset":
@@ -173,6 +176,19 @@ def test_build_validation(tide, case, status):
         kw.update(kernel=tide.TIDE_KERNEL_BULK, sched=tide.TIDE_SCHED_DYNAMIC)
     elif case == "skip_fill_direct":
         kw.update(kernel=tide.TIDE_KERNEL_DIRECT)
+    elif case == "node_size_not_dividing":
+        kw.update(order=tide.TIDE_ORDER_NODES, node_size=3)
+    elif case == "node_size_without_nodes":
+        kw.update(node_size=2)
+    elif case == "nodes_without_size":
+        kw.update(order=tide.TIDE_ORDER_NODES)
+    elif case == "staged_direct":
+        kw.update(order=tide.TIDE_ORDER_STAGED_OWN, kernel=tide.TIDE_KERNEL_DIRECT)
+    elif case == "f32_dynamic":
+        kw.update(grad_dtype=tide.TIDE_DTYPE_F32, sched=tide.TIDE_SCHED_DYNAMIC)
+    elif case == "f32_misaligned":
+        kw.update(grad_dtype=tide.TIDE_DTYPE_F32)
+        ptrs[1][1] += 2
     flags_debug = tide.TIDE_DEBUG_HOST_ONLY
     if case == "skip_fill_direct":
         flags_debug |= tide.TIDE_DEBUG_SKIP_FILL
@@ -180,7 +196,7 @@ def test_build_validation(tide, case, status):
         flags_debug |= 0x100
     flags = tide.make_flags(debug=flags_debug, **kw)
     if case == "reserved":
-        flags.reserved[2] = 1
+        flags.reserved[1] = 1
     params = [(ptrs[p], d, k, -1 if offsets is None else offsets[p]) for p, (d, k) in enumerate(dims)]
     with pytest.raises(tide.TideError) as e:
         tide.tide_plan_build(world, params, flags, 0)

@@ -13,7 +13,7 @@ import torch
 import all_gather_gb300 as tide
 import oracle
 import workloads
-from bits import assert_same_bf16, assert_same_f32, assert_same_u16, f32_to_bf16_bits
+from bits import assert_same_bf16, assert_same_f32, assert_same_u16, bf16_bits_to_f32, f32_to_bf16_bits
 from gpu_helpers import (ag_expected, bits16, oracle_rs_full, sampled_rs_check, sentinel_slots)
 
 pytestmark = pytest.mark.gpu
@@ -198,6 +198,107 @@ def test_determinism_across_launch_shapes():
             ref = got
         else:
             assert_same_f32(got, ref, f"launch shape {kw}")
+
+
+ORDER_CASES = [("staged", tide.TIDE_ORDER_STAGED_OWN, 0), ("nodes2", tide.TIDE_ORDER_NODES, 2),
+               ("nodes_w", tide.TIDE_ORDER_NODES, -1), ("nodes1", tide.TIDE_ORDER_NODES, 1)]
+
+
+def _ordered_fold(grads_uv, alpha, acc, out, order, node_size, f32=False, **kw):
+    flags = tide.make_flags(kernel=tide.TIDE_KERNEL_BULK, order=order, node_size=node_size,
+                            grad_dtype=tide.TIDE_DTYPE_F32 if f32 else tide.TIDE_DTYPE_BF16, **kw)
+    with tide.Plan(grads_uv, flags) as plan:
+        plan.rs_fold(out, alpha=alpha, accumulate=acc)
+        torch.cuda.synchronize()
+        assert plan.device_status() == tide.TIDE_OK
+    return out
+
+
+def _host_grads(grads_uv, f32):
+    W, P = len(grads_uv), len(grads_uv[0])
+    if f32:
+        return [[grads_uv[u][p].reshape(-1).cpu().numpy() for u in range(W)] for p in range(P)]
+    return [[bits16(grads_uv[u][p]) for u in range(W)] for p in range(P)]
+
+
+@pytest.mark.parametrize("case", ORDER_CASES, ids=[c[0] for c in ORDER_CASES])
+@pytest.mark.parametrize("f32", [False, True], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("world", [4, 6, 8, 32])
+def test_orders_and_fp32_grads(case, f32, world):
+    """Every Section 4.3 order, bf16 and fp32 gradients: bit-exact against the
+    oracle in the same order, and within 1e-6 (max-norm, per parameter and
+    rank) of the rank-order oracle."""
+    name, order, L = case
+    L = world if L == -1 else L
+    if order == tide.TIDE_ORDER_NODES and world % L:
+        pytest.skip("node size must divide the world")
+    rnd = random.Random(world * 7 + L)
+    shapes = [(rnd.randint(1, 3 * world + 7), rnd.choice([1, 3, 8, 17, 64])) for _ in range(4)]
+    shapes += [(world * 37 + 5, 100), (4099,)]
+    w = workloads.custom(world, shapes, index=200 + world)
+    gs = workloads.make_grads(w, device="cuda")
+    views = [[v.float() for v in gs.views[u]] for u in range(world)] if f32 else gs.views
+    if f32:  # fp32 gradients carry bits below bf16 precision
+        views = [[v + torch.randn_like(v) * 1e-6 for v in vs] for vs in views]
+    dims = w.dim0_rownumel()
+    R, o, S = oracle.geometry(world, dims)
+    oname = {tide.TIDE_ORDER_STAGED_OWN: "staged", tide.TIDE_ORDER_NODES: "nodes"}[order]
+    host = _host_grads(views, f32)
+    for acc, kw in ((False, {}), (True, {"fill_bytes": 64, "fill_ranks": 3}), (False, {"chunk_bytes": 256})):
+        init = torch.randn(world, S, device="cuda") if acc else None
+        buf, out = _guarded_out(world, S, 2, init)
+        before = out.clone()
+        _ordered_fold(views, 0.5, acc, out, order, L if order == tide.TIDE_ORDER_NODES else 0, f32, **kw)
+        want = before.cpu().numpy().copy()
+        oracle.rs_ex(world, dims, host, 0.5, acc, want, oname, L if oname == "nodes" else 0)
+        got = out.cpu().numpy()
+        assert_same_f32(got[:, :S], want[:, :S], f"{name} f32={f32} W={world} acc={acc} {kw}")
+        _check_canaries(buf, out, S)
+        rank = before.cpu().numpy().copy()
+        oracle.rs_ex(world, dims, host, 0.5, acc, rank, "rank", 0)
+        old_h = before.cpu().numpy()
+        gamma = (world + 1) * 2.0 ** -24 / (1 - (world + 1) * 2.0 ** -24)
+        for p, (d, k) in enumerate(dims):
+            a = np.concatenate([got[r, o[p]:o[p] + R[p] * k] for r in range(world)])[:d * k]
+            b = np.concatenate([rank[r, o[p]:o[p] + R[p] * k] for r in range(world)])[:d * k]
+            if d * k >= 1024:  # reordered-variant tolerance, max-norm over the parameter tensor
+                assert np.abs(a - b).max() <= 1e-6 * np.abs(b).max(), f"{name} tolerance p={p}"
+            # any order: textbook bound around the exact sum, for every element
+            vals = np.stack([np.asarray(host[p][u], dtype=np.float32).astype(np.float64) if f32 else
+                             bf16_bits_to_f32(host[p][u]).astype(np.float64) for u in range(world)])
+            base = np.concatenate([old_h[r, o[p]:o[p] + R[p] * k] for r in range(world)])[:d * k].astype(np.float64)
+            exact = 0.5 * vals.sum(0) + (base if acc else 0.0)
+            mag = 0.5 * np.abs(vals).sum(0) + (np.abs(base) if acc else 0.0)
+            assert (np.abs(a.astype(np.float64) - exact) <= gamma * mag + 1e-45).all(), f"{name} bound p={p}"
+
+
+@pytest.mark.parametrize("f32", [False, True], ids=["bf16", "fp32"])
+def test_orders_misaligned_pieces(f32):
+    """Pieces the bulk producer cannot stage (rank phases differ) take the
+    scalar path, in the same order."""
+    world, shapes = 4, [(67, 33), (9, 8), (5,)]
+    esz = 4 if f32 else 2
+    dt = torch.float32 if f32 else torch.bfloat16
+    views = []
+    for u in range(world):
+        buf = torch.empty(4096, dtype=dt, device="cuda")
+        vs, cur = [], u + 1
+        for s_ in shapes:
+            n = int(np.prod(s_))
+            vs.append(buf[cur:cur + n].view(s_))
+            vs[-1].copy_(torch.randn(s_, device="cuda").to(dt))
+            cur += n + 3
+        views.append(vs)
+    dims = [(s_[0], int(np.prod(s_[1:])) if len(s_) > 1 else 1) for s_ in shapes]
+    _, _, S = oracle.geometry(world, dims)
+    host = _host_grads(views, f32)
+    for order, L, oname in ((tide.TIDE_ORDER_STAGED_OWN, 0, "staged"), (tide.TIDE_ORDER_NODES, 2, "nodes"),
+                            (tide.TIDE_ORDER_RANK_ASC, 0, "rank")):
+        out = torch.zeros(world, S, device="cuda")
+        _ordered_fold(views, 1.0, False, out, order, L, f32)
+        want = np.zeros((world, S), np.float32)
+        oracle.rs_ex(world, dims, host, 1.0, False, want, oname, L)
+        assert_same_f32(out.cpu().numpy(), want, f"misaligned {oname} f32={f32}")
 
 
 def test_bulk_wait_timeout_reports_status():
