@@ -35,7 +35,13 @@ TIDE_DEBUG_SKIP_FILL = 0x4
 EXPORTED = ("tide_plan_build", "tide_plan_rebind", "tide_rs_fold", "tide_ag_place", "tide_plan_destroy",
             "tide_plan_slot_numel", "tide_plan_num_segments", "tide_plan_segment", "tide_plan_fold_config",
             "tide_last_device_status", "tide_launch_count", "tide_status_string", "tide_last_error",
-            "tide_rs_fold_noalloc", "tide_ag_place_f32")
+            "tide_rs_fold_noalloc", "tide_ag_place_f32", "tide_latin_square_gpu", "tide_rs_wave_plan",
+            "tide_rs_wave_zero_mask", "tide_bruck_schedule")
+
+
+class WavePlan(ctypes.Structure):
+    _fields_ = [("waves", ctypes.c_int32), ("generations", ctypes.c_int32), ("network_rounds", ctypes.c_int32),
+                ("zero_blocks", ctypes.c_int32)]
 
 
 class TideError(RuntimeError):
@@ -107,6 +113,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tide_rs_fold_noalloc.restype = st
     lib.tide_ag_place_f32.argtypes = [vp, vp, i64, ctypes.POINTER(vp), vp]
     lib.tide_ag_place_f32.restype = st
+    lib.tide_latin_square_gpu.argtypes = [i32, i32, i32, i32, i32]
+    lib.tide_latin_square_gpu.restype = i32
+    lib.tide_rs_wave_plan.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(WavePlan)]
+    lib.tide_rs_wave_plan.restype = st
+    lib.tide_rs_wave_zero_mask.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_uint64)]
+    lib.tide_rs_wave_zero_mask.restype = st
+    lib.tide_bruck_schedule.argtypes = [i32, ctypes.POINTER(i32), ctypes.POINTER(i32), i32]
+    lib.tide_bruck_schedule.restype = i32
     _lib = lib
     return lib
 
@@ -234,3 +248,30 @@ def tide_rs_fold_noalloc(world: int, params, out_base: int, out_slot_stride: int
     _check(load_library().tide_rs_fold_noalloc(world, len(params), arr, ctypes.c_void_p(out_base or None),
                                                out_slot_stride, ctypes.c_float(alpha), int(accumulate),
                                                ctypes.c_void_p(stream or None)), "tide_rs_fold_noalloc")
+
+
+def tide_latin_square_gpu(s: int, m: int, n: int, M: int, L: int) -> int:
+    return int(load_library().tide_latin_square_gpu(s, m, n, M, L))
+
+
+def tide_rs_wave_plan(M: int, L: int, w_wave: int, k: int, me: int):
+    """(status, dict) -- status TIDE_OK (accepted) or TIDE_ERR_UNSUPPORTED (collision); other errors raise."""
+    plan = WavePlan()
+    st = load_library().tide_rs_wave_plan(M, L, w_wave, k, me, ctypes.byref(plan))
+    if st not in (TIDE_OK, TIDE_ERR_UNSUPPORTED):
+        _check(st, "tide_rs_wave_plan")
+    return st, {k_: getattr(plan, k_) for k_, _ in WavePlan._fields_}
+
+
+def tide_rs_wave_zero_mask(M: int, L: int, w_wave: int, me: int, wave: int):
+    arr = (ctypes.c_uint64 * L)()
+    _check(load_library().tide_rs_wave_zero_mask(M, L, w_wave, me, wave, arr), "tide_rs_wave_zero_mask")
+    return list(arr)
+
+
+def tide_bruck_schedule(M: int, max_rounds: int = 64):
+    cnt, stp = (ctypes.c_int32 * max_rounds)(), (ctypes.c_int32 * max_rounds)()
+    R = load_library().tide_bruck_schedule(M, cnt, stp, max_rounds)
+    if R < 0:
+        raise ValueError(f"tide_bruck_schedule rejected M={M}")
+    return [(d, cnt[d], stp[d]) for d in range(R)]

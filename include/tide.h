@@ -291,6 +291,47 @@ TIDE_API tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params, c
                                             float *out_base, int64_t out_slot_stride, float alpha,
                                             int32_t accumulate, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Multi-node schedule planners (host only).  A single GPU runs none of these
+ * schedules; a multi-node runtime plans with them.
+ * ---------------------------------------------------------------------- */
+
+/* Section 4.2, Equations (6)-(8): for destination node m and contributor
+ * node n of M nodes with L GPUs each, the send-order contributor index is
+ * c = (m - n) mod M (n != m) or M (own node), and its partial for sub-slice s
+ * lands in inbox block s of destination GPU (s - c mod M) mod L.  Returns that
+ * GPU, or -1 for arguments out of range. */
+TIDE_API int32_t tide_latin_square_gpu(int32_t s, int32_t m, int32_t n, int32_t M, int32_t L);
+
+typedef struct {
+    int32_t waves;          /* ceil(M / w_wave) */
+    int32_t generations;    /* inbox buffer generations: 1 for one wave or me = 1, else 2 */
+    int32_t network_rounds; /* sum over waves of ceil(remote contributors of the wave / k) */
+    int32_t zero_blocks;    /* stale inbox blocks zeroed before landings, whole schedule */
+} tide_wave_plan_t;
+
+/* Appendix D base-plan check for (M, L, w_wave, k, me): contributors 1..M in
+ * increasing order, w_wave per wave, k concurrent rail transfers per round,
+ * me = 1 for the memory-efficient single-generation inbox.  TIDE_OK when every
+ * wave is collision-free (Proposition 4.1 guarantees it when w_wave divides
+ * L); TIDE_ERR_UNSUPPORTED when two contributors of a wave would land on the
+ * same GPU (the plan must be rejected); INVALID_ARG for M < 1, L outside
+ * [1, 64], w_wave < 1, k < 1 or a bad me. */
+TIDE_API tide_status_t tide_rs_wave_plan(int32_t M, int32_t L, int32_t w_wave, int32_t k, int32_t me,
+                                         tide_wave_plan_t *out);
+
+/* Stale blocks to zero before landing `wave`: blocks the previous wave on the
+ * same buffer generation wrote that this wave does not.  zero_mask[j] bit s
+ * set = zero block s of GPU j (host array of L entries). */
+TIDE_API tide_status_t tide_rs_wave_zero_mask(int32_t M, int32_t L, int32_t w_wave, int32_t me, int32_t wave,
+                                              uint64_t *zero_mask);
+
+/* Section 3.1: recursive doubling over M nodes.  Writes, for each round d,
+ * count[d] = min(2^d, M - 2^d) shards forwarded to (n - 2^d) mod M and
+ * step[d] = 2^d; returns the number of rounds ceil(log2 M), or -1 if M < 1 or
+ * max_rounds is too small. */
+TIDE_API int32_t tide_bruck_schedule(int32_t M, int32_t *count, int32_t *step, int32_t max_rounds);
+
 /* Human-readable name of a status code. */
 TIDE_API const char *tide_status_string(tide_status_t status);
 

@@ -114,3 +114,9 @@ def bruck_simulate(M: int) -> List[List[int]]:
     for d, c, step in bruck_rounds(M):
         held = [held[n] + held[(n + step) % M][:c] for n in range(M)]
     return held
+
+
+def network_rounds(M: int, w_wave: int, k: int) -> int:
+    """Rounds of the schedule: each wave sends its remote contributors (every
+    c but the own node M), k concurrent rail transfers per round."""
+    return sum(-(-sum(1 for c in w if c != M) // k) for w in waves(M, w_wave))
