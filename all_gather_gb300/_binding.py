@@ -36,7 +36,7 @@ EXPORTED = ("tide_plan_build", "tide_plan_rebind", "tide_rs_fold", "tide_ag_plac
             "tide_plan_slot_numel", "tide_plan_num_segments", "tide_plan_segment", "tide_plan_fold_config",
             "tide_last_device_status", "tide_launch_count", "tide_status_string", "tide_last_error",
             "tide_rs_fold_noalloc", "tide_ag_place_f32", "tide_latin_square_gpu", "tide_rs_wave_plan",
-            "tide_rs_wave_zero_mask", "tide_bruck_schedule")
+            "tide_rs_wave_zero_mask", "tide_bruck_schedule", "tide_sm_probe", "tide_sm_probe_max_clusters")
 
 
 class WavePlan(ctypes.Structure):
@@ -121,6 +121,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tide_rs_wave_zero_mask.restype = st
     lib.tide_bruck_schedule.argtypes = [i32, ctypes.POINTER(i32), ctypes.POINTER(i32), i32]
     lib.tide_bruck_schedule.restype = i32
+    lib.tide_sm_probe.argtypes = [i32, i32, i32, ctypes.c_uint64, vp, vp, vp, vp, vp]
+    lib.tide_sm_probe.restype = st
+    lib.tide_sm_probe_max_clusters.argtypes = [i32, i32]
+    lib.tide_sm_probe_max_clusters.restype = i32
     _lib = lib
     return lib
 
@@ -275,3 +279,15 @@ def tide_bruck_schedule(M: int, max_rounds: int = 64):
     if R < 0:
         raise ValueError(f"tide_bruck_schedule rejected M={M}")
     return [(d, cnt[d], stp[d]) for d in range(R)]
+
+
+def tide_sm_probe(ctas: int, cluster: int, smem_bytes: int, hold_ns: int, smid: int, t_in: int, t_out: int,
+                  t_ready: int = 0, stream: int = 0) -> None:
+    _check(load_library().tide_sm_probe(ctas, cluster, smem_bytes, hold_ns, ctypes.c_void_p(smid),
+                                        ctypes.c_void_p(t_in), ctypes.c_void_p(t_out),
+                                        ctypes.c_void_p(t_ready or None), ctypes.c_void_p(stream or None)),
+           "tide_sm_probe")
+
+
+def tide_sm_probe_max_clusters(cluster: int, smem_bytes: int) -> int:
+    return int(load_library().tide_sm_probe_max_clusters(cluster, smem_bytes))

@@ -126,6 +126,117 @@ def measure(workload: str = "llama3.1_8b_block", budgets=(0, 64, 16), n_rs: int 
     return res
 
 
+PROBE_SMEM = 213 * 1024   # the one-wave GEMM's per-CTA footprint on the page: one CTA fills an SM
+PROBE_CLUSTERS = 32       # 256x8192x8192 GEMM: 128 CTAs in 32 four-CTA clusters
+
+
+BLOCKED_NS = 5000  # a probe CTA entering later than this after its stream reached it was blocked
+
+
+def _probe_once(tide, ctas, cluster, hold_ns, bufs, stream):
+    smid, tin, tout, ready = bufs
+    tide.tide_sm_probe(ctas, cluster, PROBE_SMEM, hold_ns, smid.data_ptr(), tin.data_ptr(), tout.data_ptr(),
+                       ready.data_ptr(), stream.cuda_stream)
+
+
+def _displaced(tin, tout, n):
+    """Probe CTAs that entered after the first probe CTA left (second wave)."""
+    a, b = tin[:n].cpu(), tout[:n].cpu()
+    return int((a > b.min()).sum())
+
+
+def _blocked(tin, ready, n):
+    """Probe CTAs that entered more than BLOCKED_NS after the probe was reached."""
+    return int(((tin[:n].cpu() - ready[0].cpu()) > BLOCKED_NS).sum())
+
+
+def sm_probe(workload: str = "llama3.1_8b_block", budgets=(0, 152, 64, 16), windows: int = 30, device: int = 0,
+             grads=None, hold_us: float = 30.0) -> dict:
+    """Table 5 / Figure 3 measurement on this GPU: (1) the cluster slots of the
+    one-wave GEMM's shape; (2) per reduce-scatter arm, over `windows` probe
+    launches at random points of the reduce-scatter, the displaced probe CTAs
+    (mode) and the share of windows with any; (3) with one SM-filling probe
+    CTA per SM, the mean number of SMs the reduce-scatter held."""
+    import random
+
+    import torch
+
+    import all_gather_gb300 as tide
+    import workloads
+    from all_gather_gb300 import baselines
+
+    torch.cuda.set_device(device)
+    dev = torch.device("cuda", device)
+    n_sm = torch.cuda.get_device_properties(device).multi_processor_count
+    slots = tide.tide_sm_probe_max_clusters(4, PROBE_SMEM)
+    res = {"sms": n_sm, "cluster_slots_4cta_213KB": slots, "probe": f"{PROBE_CLUSTERS} x 4-CTA clusters, "
+           f"{PROBE_SMEM // 1024} KB smem per CTA, hold {hold_us} us; resident probe: {n_sm} single CTAs", "arms": {}}
+    if slots < 1:
+        res["skipped"] = "the device cannot hold one probe cluster"
+        return res
+    w = workloads.get(workload)
+    gs = grads if grads is not None else workloads.make_grads(w, device=dev)
+    nmax = max(PROBE_CLUSTERS * 4, n_sm)
+    bufs = (torch.zeros(nmax, dtype=torch.int32, device=dev), torch.zeros(nmax, dtype=torch.int64, device=dev),
+            torch.zeros(nmax, dtype=torch.int64, device=dev), torch.zeros(1, dtype=torch.int64, device=dev))
+    s_rs, s_pr = torch.cuda.Stream(), torch.cuda.Stream()
+    hold = int(hold_us * 1000)
+    # the probe alone: no displacement expected when it fits in one wave (the
+    # first launch also loads the kernel, so it is a warm-up)
+    _probe_once(tide, PROBE_CLUSTERS * 4, 4, hold, bufs, s_pr)
+    torch.cuda.synchronize()
+    _probe_once(tide, PROBE_CLUSTERS * 4, 4, hold, bufs, s_pr)
+    torch.cuda.synchronize()
+    res["alone_displaced"] = _displaced(bufs[1], bufs[2], PROBE_CLUSTERS * 4)
+    res["alone_blocked"] = _blocked(bufs[1], bufs[3], PROBE_CLUSTERS * 4)
+    plans = {(f"fused_cta{b}" if b else "fused_full_wave"): tide.Plan(gs.views, tide.make_flags(cta_budget=b))
+             for b in budgets}
+    S = next(iter(plans.values())).slot_numel
+    out = torch.zeros(w.world, S, device=dev)
+    pack = torch.empty(w.world, w.world * S, device=dev)
+    arms = {name: (lambda p=p: p.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)) for name, p in plans.items()}
+    arms["two_pass_baseline"] = lambda: baselines.two_pass_rs(gs.views, pack, out, w.alpha, w.accumulate)
+    rnd = random.Random(5)
+    clock_hz = 1.9e9  # nominal SM clock: only sets the random start delay of a probe window
+    for name, fn in arms.items():
+        # reduce-scatter duration alone, to place the probes inside it
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fn()
+        torch.cuda.synchronize()
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        rs_ms = e0.elapsed_time(e1)
+        disp, blocked, resident = [], [], []
+        for kind, ctas, cluster in (("gemm", PROBE_CLUSTERS * 4, 4), ("resident", n_sm, 1)):
+            for _ in range(windows):
+                torch.cuda.synchronize()
+                with torch.cuda.stream(s_rs):
+                    fn()
+                delay = int(rnd.random() * 0.8 * rs_ms * 1e-3 * clock_hz)
+                with torch.cuda.stream(s_pr):
+                    if delay > 0:
+                        torch.cuda._sleep(delay)
+                    _probe_once(tide, ctas, cluster, hold, bufs, s_pr)
+                torch.cuda.synchronize()
+                if kind == "gemm":
+                    disp.append(_displaced(bufs[1], bufs[2], ctas))
+                    blocked.append(_blocked(bufs[1], bufs[3], ctas))
+                else:
+                    resident.append(_blocked(bufs[1], bufs[3], ctas))
+        mode = max(set(disp), key=disp.count)
+        res["arms"][name] = {"rs_ms": round(rs_ms, 4), "displaced_mode": mode,
+                             "windows_hit_pct": round(100.0 * sum(b > 0 for b in blocked) / len(blocked), 1),
+                             "blocked_gemm_ctas_mean": round(sum(blocked) / len(blocked), 1),
+                             "resident_sms_mean": round(sum(resident) / len(resident), 2)}
+    for p in plans.values():
+        p.close()
+    del pack, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def summarize(res: dict) -> dict:
     """victim -> {arm: slowdown} plus the RS times per arm."""
     return {"slowdown": {v: {a: r["slowdown"] for a, r in e["arms"].items()} for v, e in res["victims"].items()},
@@ -142,8 +253,11 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama3.1_8b_block")
     ap.add_argument("--budgets", default="0,64,16")
     ap.add_argument("--n-rs", type=int, default=20)
+    ap.add_argument("--probe", action="store_true", help="run the SM-id probe (Table 5) instead")
+    ap.add_argument("--windows", type=int, default=30)
     a = ap.parse_args(argv)
-    res = measure(a.workload, tuple(int(x) for x in a.budgets.split(",")), a.n_rs)
+    budgets = tuple(int(x) for x in a.budgets.split(","))
+    res = sm_probe(a.workload, budgets, a.windows) if a.probe else measure(a.workload, budgets, a.n_rs)
     print(json.dumps(res), flush=True)
     return 0
 

@@ -41,7 +41,7 @@ SAMPLE_PARAMS = ("q_proj", "k_proj", "v_proj", "o_proj")  # CPU sample: the atte
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -449,6 +449,8 @@ def run_ours(args):
         from all_gather_gb300 import interference
         result["interference"] = interference.summarize(
             interference.measure(w.name, budgets=(0, 64, 16), n_rs=20, device=local, grads=gs))
+        result["interference"]["sm_probe"] = interference.sm_probe(w.name, budgets=(0, 152, 64, 16), windows=20,
+                                                                   device=local, grads=gs)
 
     # end to end through the public API: pinned host inputs -> device -> fold + place -> host
     if not args.no_e2e:

@@ -332,6 +332,28 @@ TIDE_API tide_status_t tide_rs_wave_zero_mask(int32_t M, int32_t L, int32_t w_wa
  * max_rounds is too small. */
 TIDE_API int32_t tide_bruck_schedule(int32_t M, int32_t *count, int32_t *step, int32_t max_rounds);
 
+/* ------------------------------------------------------------------------
+ * Diagnostics
+ * ---------------------------------------------------------------------- */
+
+/* SM-id probe (the measurement of Table 5 / Figure 3): launches `ctas` CTAs
+ * of 128 threads in clusters of `cluster` (1..8), each with `smem_bytes` of
+ * dynamic shared memory (enough to fill an SM keeps one CTA per SM).  Each
+ * CTA writes smid[i] (the SM it ran on) and t_in[i] / t_out[i] (%globaltimer
+ * nanoseconds at entry and exit) and holds its SM for hold_ns (at most 10 ms;
+ * the wait is bounded by time).  Outputs are device arrays of `ctas` entries.
+ * If t_ready (device, one entry) is not NULL, a one-thread kernel launched
+ * just before the probe on the same stream writes the time the stream
+ * reached the probe, so that entry delays (blocked CTAs) can be measured.
+ * Enqueued on `stream`. */
+TIDE_API tide_status_t tide_sm_probe(int32_t ctas, int32_t cluster, int32_t smem_bytes, uint64_t hold_ns,
+                                     uint32_t *smid, uint64_t *t_in, uint64_t *t_out, uint64_t *t_ready,
+                                     void *stream);
+
+/* Clusters of the probe's shape the current device can hold at once
+ * (its "cluster slots"), or -1. */
+TIDE_API int32_t tide_sm_probe_max_clusters(int32_t cluster, int32_t smem_bytes);
+
 /* Human-readable name of a status code. */
 TIDE_API const char *tide_status_string(tide_status_t status);
 
