@@ -55,7 +55,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-baseline", action="store_true", help="skip the two-pass GPU baseline")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-interference", action="store_true", help="skip the concurrent-GEMM harness")
     ap.add_argument("--no-variants", action="store_true", help="skip timing the other placement variants")
     return ap.parse_args()
@@ -524,45 +524,85 @@ def time_variants(plan, w, S, slots, full, dev, gs_views, steps: int = 20) -> di
 
 
 def e2e(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world):
+    """End to end through the public API with host buffers: every step uploads
+    its gradients and slots from pinned host memory, runs tide_rs_fold and
+    tide_ag_place, and reads the fp32 shards and full parameters back.  Steps
+    are pipelined over two device buffer sets on three streams (upload,
+    compute, read-back), so that step i's read-back overlaps step i+1's
+    upload: the host link carries both directions at once."""
     import torch
     import torch.distributed as dist
-    stream = torch.cuda.current_stream()
+
+    import all_gather_gb300 as tide
+    import workloads
+    K = max(2, args.e2e_steps)
+    # pinned host inputs (one set: every step uploads the same bytes) and outputs (two sets)
     h_arenas = [a.cpu().pin_memory() for a in gs.arenas]
     h_slots = slots.cpu().pin_memory()
     h_out0 = out.cpu().pin_memory()
-    h_out = torch.empty_like(h_out0).pin_memory()
-    h_full = [torch.empty(f.shape, dtype=f.dtype).pin_memory() for f in full]
+    h_outs = [torch.empty_like(h_out0).pin_memory() for _ in range(2)]
+    h_fulls = [[torch.empty(f.shape, dtype=f.dtype).pin_memory() for f in full] for _ in range(2)]
+    # two device buffer sets; the second set has its own arenas and plan
+    sets = [(gs.arenas, gs.views, plan, out, slots, full)]
+    gs2 = workloads.make_grads(w, device=dev)
+    plan2 = tide.Plan(gs2.views)
+    sets.append((gs2.arenas, gs2.views, plan2, torch.empty_like(out), torch.empty_like(slots),
+                 [torch.empty_like(f) for f in full]))
     h2d = sum(a.numel() * a.element_size() for a in h_arenas) + h_slots.numel() * 2
     h2d += h_out0.numel() * 4 if w.accumulate else 0
-    d2h = h_out.numel() * 4 + sum(f.numel() * 2 for f in h_full)
-    K = max(1, args.e2e_steps)
+    d2h = h_out0.numel() * 4 + sum(f.numel() * 2 for f in full)
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
 
-    def one():
-        for a, h in zip(gs.arenas, h_arenas):
-            a.copy_(h, non_blocking=True)
-        slots.copy_(h_slots, non_blocking=True)
-        if w.accumulate:
-            out.copy_(h_out0, non_blocking=True)
-        plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
-        plan.ag_place(slots, full, mode=args.ag_mode)
-        h_out.copy_(out, non_blocking=True)
-        for f, h in zip(full, h_full):
-            h.copy_(f, non_blocking=True)
+    def step(i, first):
+        b = i % 2
+        arenas, _, pl, o, sl, fu = sets[b]
+        with torch.cuda.stream(s_in):
+            if not first[b]:
+                s_in.wait_event(ev["comp"][b])  # device inputs of set b are free again
+            for a, h in zip(arenas, h_arenas):
+                a.copy_(h, non_blocking=True)
+            sl.copy_(h_slots, non_blocking=True)
+            ev["in"][b].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(ev["in"][b])
+            if not first[b]:
+                s_comp.wait_event(ev["out"][b])  # outputs of set b were read back
+            if w.accumulate:
+                o.copy_(h_out0, non_blocking=True)
+            pl.rs_fold(o, alpha=w.alpha, accumulate=w.accumulate, stream=s_comp)
+            pl.ag_place(sl, fu, mode=args.ag_mode, stream=s_comp)
+            ev["comp"][b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["comp"][b])
+            h_outs[b].copy_(o, non_blocking=True)
+            for f, h in zip(fu, h_fulls[b]):
+                h.copy_(f, non_blocking=True)
+            ev["out"][b].record(s_out)
+        first[b] = False
 
-    one()
+    first = [True, True]
+    for i in range(2):  # warm-up, one step on each buffer set
+        step(i, first)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    for _ in range(K):
-        one()
-    e.record(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    for i in range(K):
+        step(i, first)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_comp)
+    end.record(s_out)
     torch.cuda.synchronize()
-    ms = max_over_ranks(s.elapsed_time(e) / K, world, dev)
+    ms = max_over_ranks(start.elapsed_time(end) / K, world, dev)
+    ok = torch.equal(h_outs[(K - 1) % 2], sets[(K - 1) % 2][3].cpu())  # read-back == on-device result
+    plan2.close()
+    del gs2, sets
     return {"value": round(whole_job_gbs(step_bytes, world, ms), 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "steps": K,
-            "note": "pinned host grads+slots -> device, tide_rs_fold + tide_ag_place, shards+full params -> host"}
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "steps": K, "readback_matches_device": ok,
+            "note": "per step: pinned host grads+slots -> device, tide_rs_fold + tide_ag_place, fp32 shards + full "
+                    "params -> pinned host; two device buffer sets, upload / compute / read-back streams"}
 
 
 def main():
