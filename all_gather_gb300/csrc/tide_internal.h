@@ -143,4 +143,5 @@ struct tide_plan {
     uint32_t *d_counters = nullptr;
     int32_t *d_status = nullptr;
     cudaEvent_t last_use = nullptr;
+    bool captured = false;               // a launch of this plan was captured into a CUDA graph
 };

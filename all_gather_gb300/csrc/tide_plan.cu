@@ -156,6 +156,22 @@ bool overlaps_gradients(const tide_plan_t *plan, uintptr_t lo, uintptr_t hi)
     return false;
 }
 
+// Record the plan's last-use event on `stream`, except while the stream is
+// being captured into a CUDA graph: a captured record would not mark a real
+// point of execution, so destroy() synchronises the device instead (below).
+cudaError_t mark_use(tide_plan_t *plan, cudaStream_t stream)
+{
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess)
+        return e;
+    if (cap != cudaStreamCaptureStatusNone) {
+        plan->captured = true;
+        return cudaSuccess;
+    }
+    return cudaEventRecord(plan->last_use, stream);
+}
+
 tide_status_t upload_tables(tide_plan_t *plan, cudaStream_t stream, bool pointers_only)
 {
     cudaError_t e;
@@ -177,7 +193,7 @@ tide_status_t upload_tables(tide_plan_t *plan, cudaStream_t stream, bool pointer
                         cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "upload segment table");
-    e = cudaEventRecord(plan->last_use, stream);
+    e = mark_use(plan, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "record plan event");
     return TIDE_OK;
@@ -190,6 +206,8 @@ void free_device(tide_plan_t *plan)
         cudaEventDestroy(plan->last_use);
         plan->last_use = nullptr;
     }
+    if (plan->captured)  // graphs may still replay launches that read the tables
+        cudaDeviceSynchronize();
     if (plan->d_block) {
         cudaFree(plan->d_block);
         plan->d_block = nullptr;
@@ -514,7 +532,7 @@ tide_status_t tide_rs_fold(tide_plan_t *plan, float *out_base, int64_t out_slot_
     if (e != cudaSuccess)
         return cuda_fail(e, "fold launch");
     tide::g_launches.fetch_add(1);
-    e = cudaEventRecord(plan->last_use, stream);
+    e = mark_use(plan, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "record plan event");
     return TIDE_OK;
@@ -653,7 +671,7 @@ tide_status_t tide_ag_place(tide_plan_t *plan, const void *slots_base, int64_t s
             }
         }
     }
-    e = cudaEventRecord(plan->last_use, stream);
+    e = mark_use(plan, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "record plan event");
     return TIDE_OK;
@@ -670,7 +688,7 @@ tide_status_t tide_ag_place_f32(tide_plan_t *plan, const float *slots_base, int6
     st = launch_placement(plan, nullptr, slots_base, slot_stride, full, stream);
     if (st != TIDE_OK)
         return st;
-    cudaError_t e = cudaEventRecord(plan->last_use, stream);
+    cudaError_t e = mark_use(plan, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "record plan event");
     return TIDE_OK;

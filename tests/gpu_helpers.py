@@ -39,7 +39,8 @@ def row_windows(R: int, v: int, rnd: random.Random, span: int = 3) -> List[Tuple
 
 
 def sampled_rs_check(world: int, dims, grads_uv, out_before: torch.Tensor, out_after: torch.Tensor, alpha: float,
-                     accumulate: bool, seed: int = 0, ranks_per_param: int = 3, what: str = "") -> int:
+                     accumulate: bool, seed: int = 0, ranks_per_param: int = 3, what: str = "",
+                     order: str = "rank", node_size: int = 0) -> int:
     """Compare sampled windows of a full-size fold with the oracle, window by
     window (oracle.rs_window).  Returns the number of elements compared."""
     rnd = random.Random(seed)
@@ -53,9 +54,15 @@ def sampled_rs_check(world: int, dims, grads_uv, out_before: torch.Tensor, out_a
                 lo, hi = i0 * k, i1 * k
                 nv = max(0, min(hi, v * k) - lo)
                 base = r * R[p] * k + lo
-                srcs = [bits16(grads_uv[u][p].reshape(-1)[base:base + nv]) for u in range(world)]
+                pieces = [grads_uv[u][p].reshape(-1)[base:base + nv] for u in range(world)]
                 old = out_before[r, o[p] + lo:o[p] + hi].cpu().numpy() if accumulate else None
-                want = oracle.rs_window(srcs, nv, (hi - lo) - nv, alpha, accumulate, old)
+                if pieces[0].dtype == torch.float32 or order != "rank":
+                    srcs = [x.cpu().numpy() if x.dtype == torch.float32 else bits16(x) for x in pieces]
+                    want = oracle.load().rs_window_ex(srcs, nv, (hi - lo) - nv, alpha, accumulate, r, order,
+                                                      node_size, old)
+                else:
+                    srcs = [bits16(x) for x in pieces]
+                    want = oracle.rs_window(srcs, nv, (hi - lo) - nv, alpha, accumulate, old)
                 got = out_after[r, o[p] + lo:o[p] + hi].cpu().numpy()
                 assert_same_f32(got, want, f"{what} p={p} r={r} rows [{i0},{i1})")
                 checked += hi - lo

@@ -485,6 +485,48 @@ def test_ag_shard_roundtrip_identity():
             assert_same_u16(bits16(f), bits16(x), f"AG(shard(x)) {mode} p={p}")
 
 
+def test_graph_captured_step():
+    """The step (fold, placement, mixed-precision placement) captured once in a
+    CUDA graph and replayed on new inputs copied into the same buffers."""
+    w = workloads.get(1)
+    dims = w.dim0_rownumel()
+    g1 = workloads.make_grads(w, device="cuda")
+    g2 = workloads.make_grads(workloads.custom(w.world, w.shapes, index=93), device="cuda")
+    _, _, S = oracle.geometry(w.world, dims)
+    out = torch.zeros(w.world, S, device="cuda")
+    slots = workloads.make_slots(w, S, device="cuda")
+    slots32 = torch.randn(w.world, S, device="cuda")
+    full = [torch.empty(s_, dtype=torch.bfloat16, device="cuda") for s_ in w.shapes]
+    full32 = [torch.empty_like(f) for f in full]
+    with tide.Plan(g1.views) as plan:
+        plan.rs_fold(out, alpha=0.25)  # warm-up outside the capture
+        plan.ag_place(slots, full)
+        plan.ag_place_f32(slots32, full32)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            plan.rs_fold(out, alpha=0.25)
+            plan.ag_place(slots, full)
+            plan.ag_place_f32(slots32, full32)
+        for src in (g2, g1, g2):
+            for a, b in zip(g1.arenas, src.arenas):
+                if a.data_ptr() != b.data_ptr():
+                    a.copy_(b)
+            slots.copy_(slots.flip(0))
+            slots32.mul_(-1.5)
+            out.zero_()
+            graph.replay()
+            torch.cuda.synchronize()
+            want = oracle_rs_full(w.world, dims, src.views, 0.25, False, torch.zeros(w.world, S))
+            assert_same_f32(out.cpu().numpy(), want, "replayed fold")
+            wf = ag_expected(w.world, dims, slots)
+            wf32 = oracle.ag_cast(w.world, dims, slots32.cpu().numpy())
+            for p in range(len(dims)):
+                assert_same_u16(bits16(full[p]), wf[p], "replayed placement")
+                assert_same_bf16(bits16(full32[p]), wf32[p], "replayed mixed-precision placement")
+        del graph
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads in the benchmark's launch configuration
 @pytest.mark.parametrize("index", [2, 3, 4, 5])
@@ -522,4 +564,36 @@ def test_full_size_sampled(index):
         for p, f in enumerate(full):
             assert_same_bf16(bits16(f), want[p], f"{w.name} ag_f32 p={p}")
     del gs
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("index", [2, 5])
+def test_full_size_orders_and_fp32(index):
+    """Full-size groups: the Section 4.3 orders and fp32 gradients, sampled
+    windows recomputed by the oracle in the same order."""
+    w = workloads.get(index)
+    dims = w.dim0_rownumel()
+    gs = workloads.make_grads(w, device="cuda")
+    _, _, S = oracle.geometry(w.world, dims)
+    L = w.world // 2
+    for order, oname, ns in ((tide.TIDE_ORDER_STAGED_OWN, "staged", 0), (tide.TIDE_ORDER_NODES, "nodes", L)):
+        out = torch.empty(w.world, S, device="cuda")
+        with tide.Plan(gs.views, tide.make_flags(order=order, node_size=ns)) as plan:
+            plan.rs_fold(out, alpha=w.alpha)
+            torch.cuda.synchronize()
+        n = sampled_rs_check(w.world, dims, gs.views, None, out, w.alpha, False, seed=index,
+                             what=f"{w.name} {oname}", order=oname, node_size=ns)
+        assert n > 0
+    # fp32 gradients (the bf16 values plus a small fp32 perturbation), accumulate mode
+    views32 = [[v.float() + 1e-6 * torch.randn(v.shape, device="cuda") for v in vs] for vs in gs.views]
+    del gs
+    out = workloads.make_out_init(w, S, device="cuda")
+    before = out.clone()
+    with tide.Plan(views32, tide.make_flags(grad_dtype=tide.TIDE_DTYPE_F32)) as plan:
+        plan.rs_fold(out, alpha=1.0 / w.world, accumulate=True)
+        torch.cuda.synchronize()
+    n = sampled_rs_check(w.world, dims, views32, before, out, 1.0 / w.world, True, seed=index + 1,
+                         what=f"{w.name} fp32 grads")
+    assert n > 0
+    del views32, out, before
     torch.cuda.empty_cache()
