@@ -86,7 +86,7 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float x)
 __global__ void __launch_bounds__(kAgThreads) ag_cast_kernel(const __grid_constant__ AgParams ap)
 {
     constexpr int NT = kAgThreads;
-    constexpr int U = 2;
+    constexpr int U = 4;  // 8-element vectors in flight per thread
     const int tid = threadIdx.x;
     for (int64_t i = ap.item_begin + blockIdx.x; i < ap.item_end; i += gridDim.x) {
         const Item item = ap.items[i];

@@ -615,19 +615,40 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fold_bulk_kernel(const FoldPa
                                     acc[k][e] = __fadd_rn(acc[k][e], f[e]);
                             }
                         } else {
+                            // The fill's ranks, as runs of consecutive ranks of one node.
                             const int kk = GROUPED ? k : 0;
-                            for (int j = 0; j < nr; ++j) {
+                            for (int j = 0; j < nr;) {
+                                const int q = u0 + j, l = q % L;
+                                const int run = nr - j < L - l ? nr - j : L - l;
                                 float f[8];
                                 lds8(sb + size_t(j) * FILL + v * 8, f);
-                                const int q = u0 + j, l = q % L;
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    part[kk][e] = l == 0 ? f[e] : __fadd_rn(part[kk][e], f[e]);
-                                if (l == L - 1) {
+                                if (l == 0) {
 #pragma unroll
                                     for (int e = 0; e < 8; ++e)
-                                        acc[k][e] = q < L ? part[kk][e] : __fadd_rn(acc[k][e], part[kk][e]);
+                                        part[kk][e] = f[e];
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e)
+                                        part[kk][e] = __fadd_rn(part[kk][e], f[e]);
                                 }
+                                for (int t = 1; t < run; ++t) {
+                                    lds8(sb + size_t(j + t) * FILL + v * 8, f);
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e)
+                                        part[kk][e] = __fadd_rn(part[kk][e], f[e]);
+                                }
+                                if (l + run == L) {  // node complete: add its partial
+                                    if (q == l) {
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e)
+                                            acc[k][e] = part[kk][e];
+                                    } else {
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e)
+                                            acc[k][e] = __fadd_rn(acc[k][e], part[kk][e]);
+                                    }
+                                }
+                                j += run;
                             }
                         }
                     }
