@@ -324,6 +324,28 @@ def test_bulk_wait_timeout_reports_status():
     assert_same_f32(out.cpu().numpy(), want, "after timeout")
 
 
+@pytest.mark.parametrize("world", [33, 257, 1024])
+def test_maximum_and_odd_worlds(world):
+    """The widest groups: up to 1024 virtual ranks (the library's maximum),
+    every kernel, rank order and the one-node order, against the oracle."""
+    shapes = [(world * 3 + 1, 24), (world // 2 + 1, 8), (7,)]
+    w = workloads.custom(world, shapes, index=300 + world)
+    gs = workloads.make_grads(w, device="cuda")
+    dims = w.dim0_rownumel()
+    _, _, S = oracle.geometry(world, dims)
+    host = _host_grads(gs.views, False)
+    for kw, oname in (({"kernel": tide.TIDE_KERNEL_DIRECT}, "rank"), ({"kernel": tide.TIDE_KERNEL_BULK}, "rank"),
+                      ({"kernel": tide.TIDE_KERNEL_BULK, "order": tide.TIDE_ORDER_STAGED_OWN}, "staged")):
+        out = torch.zeros(world, S, device="cuda")
+        with tide.Plan(gs.views, tide.make_flags(**kw)) as plan:
+            plan.rs_fold(out, alpha=1.0 / world)
+            torch.cuda.synchronize()
+            assert plan.device_status() == tide.TIDE_OK
+        want = np.zeros((world, S), np.float32)
+        oracle.rs_ex(world, dims, host, 1.0 / world, False, want, oname, 0)
+        assert_same_f32(out.cpu().numpy(), want, f"W={world} {kw}")
+
+
 def test_repeated_calls_and_rebind():
     w = workloads.get(1)
     dims = w.dim0_rownumel()
