@@ -214,15 +214,23 @@ extern "C" tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params,
     fp.sched = TIDE_SCHED_STATIC;
     fp.counters = nullptr;
     fp.status = reinterpret_cast<int32_t *>(scratch + o_status);
-    const size_t smem = tide::fold_smem_bytes(TIDE_KERNEL_DIRECT, world, 0, 0, false);
+    fp.wait_budget_ns = tide::kWaitBudgetNs;
+    fp.order = TIDE_ORDER_RANK_ASC;
+    fp.node_size = 0;
+    fp.dtype = TIDE_DTYPE_BF16;
+    // The default bulk-copy fold, as tide_plan_build would configure it.
+    const tide::BulkShape bs = tide::bulk_shape(world, 0, 0, false, 2);
+    fp.fill_elems = bs.fill_elems;
+    fp.fill_ranks = bs.fill_ranks;
+    fp.stages = bs.stages;
     int per_sm = 0, sms = 0;
-    e = tide::fold_occupancy(TIDE_KERNEL_DIRECT, world, tide::kFoldThreads, smem, &per_sm);
+    e = tide::fold_occupancy(TIDE_KERNEL_BULK, world, tide::kBulkThreads, bs.smem_bytes, &per_sm);
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
         return noalloc_fail(TIDE_ERR_CUDA, "launch geometry: %s", cudaGetErrorString(e));
     const int grid = int(std::min<int64_t>(int64_t(std::max(per_sm, 1)) * sms, n_items));
-    e = tide::launch_fold(fp, TIDE_KERNEL_DIRECT, accumulate, grid, tide::kFoldThreads, smem, stream);
+    e = tide::launch_fold(fp, TIDE_KERNEL_BULK, accumulate, grid, tide::kBulkThreads, bs.smem_bytes, stream);
     if (e != cudaSuccess)
         return noalloc_fail(TIDE_ERR_CUDA, "fold launch: %s", cudaGetErrorString(e));
     tide::g_launches.fetch_add(1);
