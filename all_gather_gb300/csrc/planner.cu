@@ -35,7 +35,11 @@ int32_t tide_latin_square_gpu(int32_t s, int32_t m, int32_t n, int32_t M, int32_
     return landing(s, c, M, L);
 }
 
-tide_status_t tide_rs_wave_plan(int32_t M, int32_t L, int32_t w_wave, int32_t k, int32_t me, tide_wave_plan_t *out)
+static tide_status_t rs_wave_zero_mask_impl(int32_t M, int32_t L, int32_t w_wave, int32_t me, int32_t wave,
+                                            uint64_t *zero_mask);
+
+static tide_status_t rs_wave_plan_impl(int32_t M, int32_t L, int32_t w_wave, int32_t k, int32_t me,
+                                       tide_wave_plan_t *out)
 {
     tide::record_error("");
     if (!args_ok(M, L, w_wave) || k < 1 || (me != 0 && me != 1) || !out) {
@@ -71,15 +75,15 @@ tide_status_t tide_rs_wave_plan(int32_t M, int32_t L, int32_t w_wave, int32_t k,
     // Stale inbox blocks over the schedule (zeroed before each landing).
     for (int32_t w = 0; w < W; ++w) {
         std::vector<uint64_t> mask(static_cast<size_t>(L));
-        tide_rs_wave_zero_mask(M, L, w_wave, me, w, mask.data());
+        rs_wave_zero_mask_impl(M, L, w_wave, me, w, mask.data());
         for (uint64_t m : mask)
             out->zero_blocks += __builtin_popcountll(m);
     }
     return TIDE_OK;
 }
 
-tide_status_t tide_rs_wave_zero_mask(int32_t M, int32_t L, int32_t w_wave, int32_t me, int32_t wave,
-                                     uint64_t *zero_mask)
+static tide_status_t rs_wave_zero_mask_impl(int32_t M, int32_t L, int32_t w_wave, int32_t me, int32_t wave,
+                                            uint64_t *zero_mask)
 {
     if (!args_ok(M, L, w_wave) || (me != 0 && me != 1) || !zero_mask) {
         tide::record_error("need M >= 1, 1 <= L <= 64, w_wave >= 1, me in {0, 1}, zero_mask != NULL");
@@ -108,6 +112,27 @@ tide_status_t tide_rs_wave_zero_mask(int32_t M, int32_t L, int32_t w_wave, int32
     for (int32_t j = 0; j < L; ++j)
         zero_mask[j] = before[size_t(j)] & ~now[size_t(j)];
     return TIDE_OK;
+}
+
+tide_status_t tide_rs_wave_plan(int32_t M, int32_t L, int32_t w_wave, int32_t k, int32_t me, tide_wave_plan_t *out)
+{
+    try {
+        return rs_wave_plan_impl(M, L, w_wave, k, me, out);
+    } catch (...) {
+        tide::record_error("host memory allocation failed");
+        return TIDE_ERR_OOM;
+    }
+}
+
+tide_status_t tide_rs_wave_zero_mask(int32_t M, int32_t L, int32_t w_wave, int32_t me, int32_t wave,
+                                     uint64_t *zero_mask)
+{
+    try {
+        return rs_wave_zero_mask_impl(M, L, w_wave, me, wave, zero_mask);
+    } catch (...) {
+        tide::record_error("host memory allocation failed");
+        return TIDE_ERR_OOM;
+    }
 }
 
 int32_t tide_bruck_schedule(int32_t M, int32_t *count, int32_t *step, int32_t max_rounds)

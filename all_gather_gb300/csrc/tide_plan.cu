@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <new>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -19,18 +20,32 @@ std::atomic<uint64_t> g_launches{0};
 
 namespace {
 
-thread_local std::string t_last_error;
+// Detail of the last failing call on this thread: a fixed buffer, so that
+// reporting a failure never allocates (or throws).
+thread_local char t_last_error[512];
 
 tide_status_t fail(tide_status_t st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 tide_status_t fail(tide_status_t st, const char *fmt, ...)
 {
-    char buf[512];
     va_list ap;
     va_start(ap, fmt);
-    vsnprintf(buf, sizeof buf, fmt, ap);
+    vsnprintf(t_last_error, sizeof t_last_error, fmt, ap);
     va_end(ap);
-    t_last_error = buf;
     return st;
+}
+
+// Run a C-ABI body so that no C++ exception crosses the ABI: host
+// allocation failures become TIDE_ERR_OOM.
+template <typename F>
+tide_status_t guarded(F &&body)
+{
+    try {
+        return body();
+    } catch (const std::bad_alloc &) {
+        return fail(TIDE_ERR_OOM, "host memory allocation failed");
+    } catch (...) {
+        return fail(TIDE_ERR_INVALID_ARG, "unexpected internal error");
+    }
 }
 
 tide_status_t cuda_fail(cudaError_t e, const char *what)
@@ -243,14 +258,14 @@ const char *tide_status_string(tide_status_t s)
     return "TIDE_ERR_UNKNOWN";
 }
 
-const char *tide_last_error(void) { return t_last_error.c_str(); }
+const char *tide_last_error(void) { return t_last_error; }
 
 uint64_t tide_launch_count(void) { return tide::g_launches.load(); }
 
-tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_param_desc_t *params,
+static tide_status_t plan_build_impl(int32_t world, int32_t num_params, const tide_param_desc_t *params,
                               const tide_plan_flags_t *flags, void *stream_, tide_plan_t **plan_out)
 {
-    t_last_error.clear();
+    t_last_error[0] = '\0';
     if (!plan_out)
         return fail(TIDE_ERR_INVALID_ARG, "plan_out is NULL");
     *plan_out = nullptr;
@@ -442,9 +457,9 @@ tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_para
     return TIDE_OK;
 }
 
-tide_status_t tide_plan_rebind(tide_plan_t *plan, const tide_param_desc_t *params, void *stream)
+static tide_status_t plan_rebind_impl(tide_plan_t *plan, const tide_param_desc_t *params, void *stream)
 {
-    t_last_error.clear();
+    t_last_error[0] = '\0';
     if (!plan)
         return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
     if (plan->nparams > 0 && !params)
@@ -477,7 +492,7 @@ tide_status_t tide_plan_rebind(tide_plan_t *plan, const tide_param_desc_t *param
 tide_status_t tide_rs_fold(tide_plan_t *plan, float *out_base, int64_t out_slot_stride, float alpha,
                            int32_t accumulate, void *stream_)
 {
-    t_last_error.clear();
+    t_last_error[0] = '\0';
     if (!plan)
         return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
     if (plan->host_only)
@@ -622,10 +637,10 @@ tide_status_t launch_placement(tide_plan_t *plan, const uint16_t *slots, const f
 
 extern "C" {
 
-tide_status_t tide_ag_place(tide_plan_t *plan, const void *slots_base, int64_t slot_stride, void *const *full,
+static tide_status_t ag_place_impl(tide_plan_t *plan, const void *slots_base, int64_t slot_stride, void *const *full,
                             int32_t mode, void *stream_)
 {
-    t_last_error.clear();
+    t_last_error[0] = '\0';
     if (mode != TIDE_AG_SM && mode != TIDE_AG_CE_2D && mode != TIDE_AG_CE_1D)
         return fail(TIDE_ERR_INVALID_ARG, "unknown placement mode %d", mode);
     tide_status_t st = check_placement(plan, slots_base, slot_stride, 2, full);
@@ -677,10 +692,10 @@ tide_status_t tide_ag_place(tide_plan_t *plan, const void *slots_base, int64_t s
     return TIDE_OK;
 }
 
-tide_status_t tide_ag_place_f32(tide_plan_t *plan, const float *slots_base, int64_t slot_stride, void *const *full,
+static tide_status_t ag_place_f32_impl(tide_plan_t *plan, const float *slots_base, int64_t slot_stride, void *const *full,
                                 void *stream_)
 {
-    t_last_error.clear();
+    t_last_error[0] = '\0';
     tide_status_t st = check_placement(plan, slots_base, slot_stride, 4, full);
     if (st != TIDE_OK || plan->ag_items.empty())
         return st;
@@ -696,7 +711,7 @@ tide_status_t tide_ag_place_f32(tide_plan_t *plan, const float *slots_base, int6
 
 tide_status_t tide_plan_destroy(tide_plan_t *plan)
 {
-    t_last_error.clear();
+    t_last_error[0] = '\0';
     if (!plan)
         return TIDE_OK;
     free_device(plan);
@@ -743,7 +758,7 @@ tide_status_t tide_plan_fold_config(const tide_plan_t *plan, int32_t *grid, int3
 
 tide_status_t tide_last_device_status(tide_plan_t *plan, void *stream_)
 {
-    t_last_error.clear();
+    t_last_error[0] = '\0';
     if (!plan)
         return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
     if (plan->host_only)
@@ -767,5 +782,33 @@ tide_status_t tide_last_device_status(tide_plan_t *plan, void *stream_)
 }  // extern "C"
 
 namespace tide {
-void record_error(const char *msg) { t_last_error = msg; }
+void record_error(const char *msg) { snprintf(t_last_error, sizeof t_last_error, "%s", msg); }
 }  // namespace tide
+
+// C-ABI entry points whose bodies allocate host memory: no exception escapes.
+extern "C" {
+
+tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_param_desc_t *params,
+                              const tide_plan_flags_t *flags, void *stream, tide_plan_t **plan_out)
+{
+    return guarded([&] { return plan_build_impl(world, num_params, params, flags, stream, plan_out); });
+}
+
+tide_status_t tide_plan_rebind(tide_plan_t *plan, const tide_param_desc_t *params, void *stream)
+{
+    return guarded([&] { return plan_rebind_impl(plan, params, stream); });
+}
+
+tide_status_t tide_ag_place(tide_plan_t *plan, const void *slots_base, int64_t slot_stride, void *const *full,
+                            int32_t mode, void *stream)
+{
+    return guarded([&] { return ag_place_impl(plan, slots_base, slot_stride, full, mode, stream); });
+}
+
+tide_status_t tide_ag_place_f32(tide_plan_t *plan, const float *slots_base, int64_t slot_stride, void *const *full,
+                                void *stream)
+{
+    return guarded([&] { return ag_place_f32_impl(plan, slots_base, slot_stride, full, stream); });
+}
+
+}  // extern "C"
