@@ -53,7 +53,9 @@ def time_two_pass(w, grads_uv, S: int, out: torch.Tensor, slots: torch.Tensor, f
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     for i in range(steps):
         ev[i][0].record(stream)
+        torch.cuda.nvtx.range_push("two_pass_rs")  # lets a profiler select exactly these kernels
         two_pass_rs(grads_uv, pack, out_b, w.alpha, w.accumulate)
+        torch.cuda.nvtx.range_pop()
         ev[i][1].record(stream)
         copy_out_ag(slots[:, :S], padded, sizes)
         ev[i][2].record(stream)
