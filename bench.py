@@ -223,6 +223,39 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
+def _profile_kv(name: str):
+    """key: value lines of a committed profile summary, or None if missing or
+    if the fold kernel's source changed since the summary was taken."""
+    import hashlib
+    src = os.path.join(ROOT, "all_gather_gb300", "csrc", "rs_fold.cu")
+    try:
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+        kv = {}
+        with open(os.path.join(ROOT, "profiles", name)) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+    except OSError:
+        return None
+    return kv if kv.get("rs_fold_cu_sha256_16") == digest else None
+
+
+def profile_sm_time(workload: str):
+    kv = _profile_kv(f"sm_time_{workload}.txt")
+    if not kv:
+        return None
+    try:
+        f, b = float(kv["fused_sm_ms_per_rs"]), float(kv["two_pass_sm_ms_per_rs"])
+        return {"fused_sm_ms_per_rs": f, "two_pass_sm_ms_per_rs": b, "ratio": round(b / f, 2),
+                "fused_dram_gb_per_rs": float(kv["fused_dram_gb_per_rs"]),
+                "two_pass_dram_gb_per_rs": float(kv["two_pass_dram_gb_per_rs"]),
+                "source": f"profiles/sm_time_{workload}.txt (ncu sm__cycles_active.sum)"}
+    except (KeyError, ValueError):
+        return None
+
+
 def profile_traffic(workload: str):
     """Per-launch DRAM bytes of the fold kernel from the committed ncu summary,
     or None if there is none or the kernel source changed since it was taken."""
@@ -431,6 +464,7 @@ def run_ours(args):
                      "frac_of_8tbs_nominal": round(achieved / 8000.0, 4)},
         "gpu_launches": int(launches),
         "clocks": clk,
+        "sm_time": profile_sm_time(w.name),
     }
 
     # the other placement engines and the mixed-precision placement, timed alone after the step
