@@ -7,13 +7,18 @@
 //     y    = alpha * acc
 //     out[r * stride + o_p + j] = accumulate ? out_old + y : y
 // and for padding positions (rows past D_p) the same with zero contributions.
+// (Section 4.3's other orders permute or group the additions; see seq_rank.)
 //
 // The work is HBM-bound (W bf16 reads + one fp32 write, +1 fp32 read when
-// accumulating, per output element; ~0.4 flop/byte), so the kernels are built
-// around bytes in flight: one persistent grid that walks the plan's work list,
-// each CTA streaming the W rank rows of one chunk with 16-byte vector loads
-// straight from the gradients' own storage (no pack buffer), adding in fp32
-// registers and writing the shard with 16-byte streaming stores.
+// accumulating, per output element; ~0.4 flop/byte), so both kernels are
+// built around bytes in flight.  One persistent grid walks the plan's work
+// list of (piece, chunk) items, reading every rank's rows in place from the
+// gradients' own storage (no pack buffer):
+//   fold_bulk_kernel (default): one producer lane per CTA stages the rank rows
+//     in a shared-memory ring with bulk asynchronous copies (the TMA engine),
+//     four consumer warps add them in fp32 registers and store the shard;
+//   fold_direct_kernel: every thread loads 16-byte vectors of the rank rows
+//     straight into registers (static or dynamic item scheduling).
 #include <cuda_runtime.h>
 
 #include "tide_internal.h"

@@ -9,9 +9,20 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/tide.h"
 
 namespace tide {
+
+// NVTX range for the lifetime of a scope (header-only NVTX v3: a no-op unless
+// a profiler is attached), so that profilers can select the library's calls.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 constexpr int kMaxWorld = 1024;
 constexpr int kFoldThreads = 256;            // threads per fold CTA (direct kernel)

@@ -492,6 +492,7 @@ static tide_status_t plan_rebind_impl(tide_plan_t *plan, const tide_param_desc_t
 tide_status_t tide_rs_fold(tide_plan_t *plan, float *out_base, int64_t out_slot_stride, float alpha,
                            int32_t accumulate, void *stream_)
 {
+    tide::NvtxRange range("tide_rs_fold");
     t_last_error[0] = '\0';
     if (!plan)
         return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
@@ -791,6 +792,7 @@ extern "C" {
 tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_param_desc_t *params,
                               const tide_plan_flags_t *flags, void *stream, tide_plan_t **plan_out)
 {
+    tide::NvtxRange range("tide_plan_build");
     return guarded([&] { return plan_build_impl(world, num_params, params, flags, stream, plan_out); });
 }
 
@@ -802,12 +804,14 @@ tide_status_t tide_plan_rebind(tide_plan_t *plan, const tide_param_desc_t *param
 tide_status_t tide_ag_place(tide_plan_t *plan, const void *slots_base, int64_t slot_stride, void *const *full,
                             int32_t mode, void *stream)
 {
+    tide::NvtxRange range("tide_ag_place");
     return guarded([&] { return ag_place_impl(plan, slots_base, slot_stride, full, mode, stream); });
 }
 
 tide_status_t tide_ag_place_f32(tide_plan_t *plan, const float *slots_base, int64_t slot_stride, void *const *full,
                                 void *stream)
 {
+    tide::NvtxRange range("tide_ag_place_f32");
     return guarded([&] { return ag_place_f32_impl(plan, slots_base, slot_stride, full, stream); });
 }
 

@@ -223,14 +223,22 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
+def kernel_digest() -> str:
+    """sha256 (16 hex digits) of the fold kernels' code: rs_fold.cu without
+    its // comments and blank lines, so that comment edits keep profiles valid."""
+    import hashlib
+    import re
+    with open(os.path.join(ROOT, "all_gather_gb300", "csrc", "rs_fold.cu")) as f:
+        lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in f]
+    code = "\n".join(ln for ln in lines if ln.strip())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
+
+
 def _profile_kv(name: str):
     """key: value lines of a committed profile summary, or None if missing or
-    if the fold kernel's source changed since the summary was taken."""
-    import hashlib
-    src = os.path.join(ROOT, "all_gather_gb300", "csrc", "rs_fold.cu")
+    if the fold kernels' code changed since the summary was taken."""
     try:
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+        digest = kernel_digest()
         kv = {}
         with open(os.path.join(ROOT, "profiles", name)) as f:
             for line in f:
@@ -258,23 +266,11 @@ def profile_sm_time(workload: str):
 
 def profile_traffic(workload: str):
     """Per-launch DRAM bytes of the fold kernel from the committed ncu summary,
-    or None if there is none or the kernel source changed since it was taken."""
-    import hashlib
-    path = os.path.join(ROOT, "profiles", f"rs_fold_{workload}_traffic.txt")
-    src = os.path.join(ROOT, "all_gather_gb300", "csrc", "rs_fold.cu")
+    or None if there is none or the kernel code changed since it was taken."""
+    kv = _profile_kv(f"rs_fold_{workload}_traffic.txt")
     try:
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()[:16]
-        kv = {}
-        with open(path) as f:
-            for line in f:
-                if ":" in line and not line.startswith("#"):
-                    k, v = line.split(":", 1)
-                    kv[k.strip()] = v.strip()
-        if kv.get("rs_fold_cu_sha256_16") != digest:
-            return None
-        return float(kv["traffic_bytes_per_launch"])
-    except (OSError, KeyError, ValueError):
+        return float(kv["traffic_bytes_per_launch"]) if kv else None
+    except (KeyError, ValueError):
         return None
 
 
@@ -441,6 +437,10 @@ def run_ours(args):
     value = whole_job_gbs(step_bytes, world, ms_per_step)
     rs_mean = sum(rs_ms) / K
     ag_mean = sum(ag_ms) / K
+
+    def pct(xs, q):
+        ys = sorted(xs)
+        return round(ys[min(len(ys) - 1, int(q * len(ys)))], 4)
     peak, peak_kind = measured_peak_gbs()
     achieved = rs_b / (rs_mean * 1e-3) / 1e9
     clk = clocks.summary(t_wall0, t_wall1)
@@ -454,9 +454,13 @@ def run_ours(args):
                    "fold_grid": cfg["grid"], "fold_block": cfg["block"], "fold_items": cfg["items"],
                    "chunk_elems": cfg["chunk_elems"], "l2": "inputs larger than L2 (no flush)",
                    "step": "tide_rs_fold + tide_ag_place", "parallelism": f"weak: {world} independent replicas"},
-        "parts": {"rs_fold": {"ms": round(rs_mean, 4), "gbs": round(achieved, 1), "alg_bytes": rs_b},
+        "parts": {"rs_fold": {"ms": round(rs_mean, 4), "gbs": round(achieved, 1), "alg_bytes": rs_b,
+                              "p10_ms": pct(rs_ms, 0.1), "p50_ms": pct(rs_ms, 0.5), "p90_ms": pct(rs_ms, 0.9)},
                   "ag_place": {"ms": round(ag_mean, 4), "gbs": round(ag_b / (ag_mean * 1e-3) / 1e9, 1),
-                               "alg_bytes": ag_b}},
+                               "alg_bytes": ag_b, "p10_ms": pct(ag_ms, 0.1), "p50_ms": pct(ag_ms, 0.5),
+                               "p90_ms": pct(ag_ms, 0.9)}},
+        "device": {"name": torch.cuda.get_device_name(dev),
+                   "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profile_traffic(w.name),
                      "kernel": "tide_rs_fold", "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
