@@ -58,6 +58,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose or os.environ.get("TIDE_PTXAS_VERBOSE") else []
+    extra += os.environ.get("TIDE_NVCC_DEFINES", "").split()  # e.g. -DTIDE_BULK_RING_KB=64 for tuning builds
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")

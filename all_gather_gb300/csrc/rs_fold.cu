@@ -364,12 +364,33 @@ __device__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t budge
     }
 }
 
-__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+#ifndef TIDE_BULK_L2_EVICT_FIRST
+#define TIDE_BULK_L2_EVICT_FIRST 0  // 1: bulk gradient loads carry an L2 evict-first policy (slower here)
+#endif
+
+// L2 policy for read-once gradient data (only used with TIDE_BULK_L2_EVICT_FIRST).
+__device__ __forceinline__ uint64_t evict_first_policy()
 {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy)
+{
+#if TIDE_BULK_L2_EVICT_FIRST
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy));
+#else
+    (void)policy;
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar)));
+#endif
 }
 
 __device__ __forceinline__ uint4 lds_v4(const uint16_t *p)
@@ -495,6 +516,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fold_bulk_kernel(const FoldPa
         uint32_t stage = 0, phase = 0;
         int64_t fills = 0, skipped = -1;
         bool stop = false;
+        const uint64_t policy = TIDE_BULK_L2_EVICT_FIRST ? evict_first_policy() : 0;
         for (int64_t it = blockIdx.x; it < fp.n_items && !stop; it += gridDim.x) {
             const Item item = fp.items[it];
             const Seg seg = fp.segs[item.seg];
@@ -526,7 +548,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fold_bulk_kernel(const FoldPa
                             E *dst = ring + size_t(stage) * RG * FILL;
 #pragma unroll 4
                             for (int j = 0; j < nr; ++j)
-                                bulk_copy_g2s(dst + size_t(j) * FILL, src_cache[u0 + j] + c, bytes, &full[stage]);
+                                bulk_copy_g2s(dst + size_t(j) * FILL, src_cache[u0 + j] + c, bytes, &full[stage], policy);
                         }
                     }
                     ++fills;

@@ -28,7 +28,10 @@ constexpr int kMaxWorld = 1024;
 constexpr int kFoldThreads = 256;            // threads per fold CTA (direct kernel)
 constexpr int kBulkConsumerWarps = 4;        // bulk kernel: warp 0 produces, warps 1..4 consume
 constexpr int kBulkThreads = 32 * (1 + kBulkConsumerWarps);
-constexpr int kBulkSmemTarget = 96 * 1024;   // stage ring bytes per bulk CTA (two CTAs per SM)
+#ifndef TIDE_BULK_RING_KB
+#define TIDE_BULK_RING_KB 96
+#endif
+constexpr int kBulkSmemTarget = TIDE_BULK_RING_KB * 1024;  // stage ring bytes per bulk CTA (96 KB: two CTAs per SM)
 constexpr uint64_t kWaitBudgetNs = 4000000000ull;   // bounded mbarrier waits: 4 s
 constexpr uint64_t kShortWaitBudgetNs = 50000000ull; // with TIDE_DEBUG_SHORT_WAIT: 50 ms
 constexpr int kAgThreads = 256;              // threads per placement CTA
