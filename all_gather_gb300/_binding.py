@@ -60,7 +60,7 @@ class PlanFlags(ctypes.Structure):
     _fields_ = [("cta_budget", ctypes.c_int32), ("chunk_bytes", ctypes.c_int32), ("order", ctypes.c_int32),
                 ("sched", ctypes.c_int32), ("kernel", ctypes.c_int32), ("grad_dtype", ctypes.c_int32),
                 ("debug", ctypes.c_uint32), ("fill_bytes", ctypes.c_int32), ("fill_ranks", ctypes.c_int32),
-                ("node_size", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
+                ("node_size", ctypes.c_int32), ("ce_streams", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
 
 
 class Segment(ctypes.Structure):
@@ -155,11 +155,11 @@ def _descs(params: Sequence[Tuple[Sequence[int], int, int, int]]):
 
 def make_flags(cta_budget=0, chunk_bytes=0, order=TIDE_ORDER_RANK_ASC, sched=TIDE_SCHED_STATIC,
                kernel=TIDE_KERNEL_AUTO, grad_dtype=TIDE_DTYPE_BF16, debug=0, fill_bytes=0,
-               fill_ranks=0, node_size=0) -> PlanFlags:
+               fill_ranks=0, node_size=0, ce_streams=0) -> PlanFlags:
     f = PlanFlags()
     f.cta_budget, f.chunk_bytes, f.order, f.sched = cta_budget, chunk_bytes, order, sched
     f.kernel, f.grad_dtype, f.debug, f.fill_bytes, f.fill_ranks = kernel, grad_dtype, debug, fill_bytes, fill_ranks
-    f.node_size = node_size
+    f.node_size, f.ce_streams = node_size, ce_streams
     return f
 
 

@@ -157,5 +157,10 @@ struct tide_plan {
     uint32_t *d_counters = nullptr;
     int32_t *d_status = nullptr;
     cudaEvent_t last_use = nullptr;
+    // copy-engine placement: internal streams, fork / join events
+    int32_t n_ce = 0;
+    cudaStream_t ce_stream[8] = {};
+    cudaEvent_t ce_fork = nullptr;
+    cudaEvent_t ce_join[8] = {};
     bool captured = false;               // a launch of this plan was captured into a CUDA graph
 };

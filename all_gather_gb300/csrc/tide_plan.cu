@@ -86,9 +86,10 @@ int32_t piece_phase(const uint64_t *ptrs_p, int32_t W, int64_t src_elem, int ele
 
 tide_status_t check_flags(const tide_plan_flags_t &f)
 {
-    for (int i = 0; i < 2; ++i)
-        if (f.reserved[i] != 0)
-            return fail(TIDE_ERR_INVALID_ARG, "flags.reserved[%d] must be zero", i);
+    if (f.reserved[0] != 0)
+        return fail(TIDE_ERR_INVALID_ARG, "flags.reserved[0] must be zero");
+    if (f.ce_streams < 0 || f.ce_streams > 8)
+        return fail(TIDE_ERR_INVALID_ARG, "flags.ce_streams %d outside [0, 8]", f.ce_streams);
     if (f.fill_bytes != 0 && (f.fill_bytes < 16 || f.fill_bytes % 16 != 0 || f.fill_bytes > 4096))
         return fail(TIDE_ERR_INVALID_ARG, "flags.fill_bytes %d: need 0 or a multiple of 16 in [16, 4096]",
                     f.fill_bytes);
@@ -223,6 +224,16 @@ void free_device(tide_plan_t *plan)
     }
     if (plan->captured)  // graphs may still replay launches that read the tables
         cudaDeviceSynchronize();
+    for (int i = 0; i < plan->n_ce; ++i) {
+        cudaStreamSynchronize(plan->ce_stream[i]);
+        cudaStreamDestroy(plan->ce_stream[i]);
+        cudaEventDestroy(plan->ce_join[i]);
+    }
+    plan->n_ce = 0;
+    if (plan->ce_fork) {
+        cudaEventDestroy(plan->ce_fork);
+        plan->ce_fork = nullptr;
+    }
     if (plan->d_block) {
         cudaFree(plan->d_block);
         plan->d_block = nullptr;
@@ -446,6 +457,20 @@ static tide_status_t plan_build_impl(int32_t world, int32_t num_params, const ti
     e = cudaEventCreateWithFlags(&plan->last_use, cudaEventDisableTiming);
     if (e != cudaSuccess)
         return bail(cuda_fail(e, "create plan event"));
+    e = cudaEventCreateWithFlags(&plan->ce_fork, cudaEventDisableTiming);
+    if (e != cudaSuccess)
+        return bail(cuda_fail(e, "create copy-engine event"));
+    for (int i = 0, n = f.ce_streams ? f.ce_streams : 8; i < n; ++i) {
+        e = cudaStreamCreateWithFlags(&plan->ce_stream[i], cudaStreamNonBlocking);
+        if (e == cudaSuccess) {
+            e = cudaEventCreateWithFlags(&plan->ce_join[i], cudaEventDisableTiming);
+            if (e != cudaSuccess)
+                cudaStreamDestroy(plan->ce_stream[i]);
+        }
+        if (e != cudaSuccess)
+            return bail(cuda_fail(e, "create copy-engine stream"));
+        plan->n_ce = i + 1;
+    }
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     e = cudaMemsetAsync(base + o_cnt, 0, o_st + sizeof(int32_t) - o_cnt, stream);
     if (e != cudaSuccess)
@@ -604,6 +629,103 @@ tide_status_t check_placement(tide_plan_t *plan, const void *slots_base, int64_t
     return check_device(plan);
 }
 
+// Copy-engine placement.  Rank r's piece of p: slot r at o_p -> full_p rows
+// [r R, r R + v).  As 2D copies, one per parameter over the ranks holding R
+// real rows (source pitch = slot stride, destination pitch = R K) plus one
+// tail copy, or as one 1D copy per piece.  Pieces of kCeRowCopyBytes or more
+// are copied one by one even in 2D mode: they need few descriptors, and the
+// copy engines move large 1D copies faster than 2D ones.  The copies are spread over the
+// plan's internal streams so that several copy engines work at once: large
+// 2D copies are split by rows, then each copy goes to the least loaded
+// stream.  The internal streams fork from and join back into `stream`.
+constexpr size_t kCeRowCopyBytes = size_t(1) << 20;
+
+struct CeCopy {
+    char *dst;
+    size_t dpitch;
+    const char *src;
+    size_t spitch, width, height;
+};
+
+tide_status_t copy_engine_placement(tide_plan_t *plan, const uint16_t *slots, int64_t slot_stride, void *const *full,
+                                    bool two_d, cudaStream_t stream)
+{
+    std::vector<CeCopy> jobs;
+    size_t total = 0;
+    for (int32_t p = 0; p < plan->nparams; ++p) {
+        const int64_t D = plan->dim0[p], K = plan->row_numel[p], R = plan->rows[p];
+        if (D * K == 0)
+            continue;
+        char *dst = static_cast<char *>(full[p]);
+        const char *src = reinterpret_cast<const char *>(slots + plan->offset[p]);
+        const size_t piece = size_t(R * K) * 2u, spitch = size_t(slot_stride) * 2u;
+        const int64_t nfull = D / R;  // ranks holding R real rows
+        if (two_d && nfull > 0 && piece < kCeRowCopyBytes) {
+            jobs.push_back({dst, piece, src, spitch, piece, size_t(nfull)});
+        } else {
+            for (int64_t r = 0; r < nfull; ++r)
+                jobs.push_back({dst + size_t(r) * piece, piece, src + size_t(r) * spitch, spitch, piece, 1});
+        }
+        const int64_t tail_rows = D - nfull * R;
+        if (tail_rows > 0)
+            jobs.push_back({dst + size_t(nfull) * piece, piece, src + size_t(nfull) * spitch, spitch,
+                            size_t(tail_rows * K) * 2u, 1});
+        total += size_t(D * K) * 2u;
+    }
+    const int n = plan->n_ce;
+    if (n > 1) {  // split large 2D copies by rows into pieces of about total / (2 n)
+        const size_t target = std::max<size_t>(total / size_t(2 * n), 1);
+        std::vector<CeCopy> split;
+        for (const CeCopy &j : jobs) {
+            const size_t bytes = j.width * j.height;
+            size_t k = std::min(j.height, (bytes + target - 1) / target);
+            if (k <= 1) {
+                split.push_back(j);
+                continue;
+            }
+            const size_t rows = (j.height + k - 1) / k;
+            for (size_t r0 = 0; r0 < j.height; r0 += rows)
+                split.push_back({j.dst + r0 * j.dpitch, j.dpitch, j.src + r0 * j.spitch, j.spitch, j.width,
+                                 std::min(rows, j.height - r0)});
+        }
+        jobs.swap(split);
+        std::stable_sort(jobs.begin(), jobs.end(),
+                         [](const CeCopy &a, const CeCopy &b) { return a.width * a.height > b.width * b.height; });
+    }
+    cudaError_t e = cudaSuccess;
+    if (n > 1) {
+        e = cudaEventRecord(plan->ce_fork, stream);
+        for (int i = 0; i < n && e == cudaSuccess; ++i)
+            e = cudaStreamWaitEvent(plan->ce_stream[i], plan->ce_fork, 0);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "fork copy-engine streams");
+    }
+    std::vector<size_t> load(size_t(std::max(n, 1)), 0);
+    for (const CeCopy &j : jobs) {
+        size_t best = 0;
+        for (size_t i = 1; i < load.size(); ++i)
+            if (load[i] < load[best])
+                best = i;
+        load[best] += j.width * j.height;
+        cudaStream_t s = n > 1 ? plan->ce_stream[best] : stream;
+        e = j.height > 1 ? cudaMemcpy2DAsync(j.dst, j.dpitch, j.src, j.spitch, j.width, j.height,
+                                             cudaMemcpyDeviceToDevice, s)
+                         : cudaMemcpyAsync(j.dst, j.src, j.width, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "placement copy");
+    }
+    if (n > 1) {
+        for (int i = 0; i < n && e == cudaSuccess; ++i) {
+            e = cudaEventRecord(plan->ce_join[i], plan->ce_stream[i]);
+            if (e == cudaSuccess)
+                e = cudaStreamWaitEvent(stream, plan->ce_join[i], 0);
+        }
+        if (e != cudaSuccess)
+            return cuda_fail(e, "join copy-engine streams");
+    }
+    return TIDE_OK;
+}
+
 // Placement kernel launches, at most kAgParamsPerLaunch destination pointers each.
 tide_status_t launch_placement(tide_plan_t *plan, const uint16_t *slots, const float *slots_f32,
                                int64_t slot_stride, void *const *full, cudaStream_t stream)
@@ -656,36 +778,9 @@ static tide_status_t ag_place_impl(tide_plan_t *plan, const void *slots_base, in
         if (st != TIDE_OK)
             return st;
     } else {
-        // Copy engines.  Rank r's piece of p: slot r at o_p -> full_p rows [r R, r R + v).
-        for (int32_t p = 0; p < plan->nparams; ++p) {
-            const int64_t D = plan->dim0[p], K = plan->row_numel[p], R = plan->rows[p];
-            if (D * K == 0)
-                continue;
-            char *dst = static_cast<char *>(full[p]);
-            const char *src = reinterpret_cast<const char *>(slots + plan->offset[p]);
-            const size_t piece = size_t(R * K) * 2u;
-            const int64_t nfull = D / R;  // ranks holding R real rows
-            if (mode == TIDE_AG_CE_2D && nfull > 0) {
-                e = cudaMemcpy2DAsync(dst, piece, src, size_t(slot_stride) * 2u, piece, size_t(nfull),
-                                      cudaMemcpyDeviceToDevice, stream);
-                if (e != cudaSuccess)
-                    return cuda_fail(e, "2D placement copy");
-            } else {
-                for (int64_t r = 0; r < nfull; ++r) {
-                    e = cudaMemcpyAsync(dst + size_t(r) * piece, src + size_t(r * slot_stride) * 2u, piece,
-                                        cudaMemcpyDeviceToDevice, stream);
-                    if (e != cudaSuccess)
-                        return cuda_fail(e, "1D placement copy");
-                }
-            }
-            const int64_t tail_rows = D - nfull * R;
-            if (tail_rows > 0) {
-                e = cudaMemcpyAsync(dst + size_t(nfull) * piece, src + size_t(nfull * slot_stride) * 2u,
-                                    size_t(tail_rows * K) * 2u, cudaMemcpyDeviceToDevice, stream);
-                if (e != cudaSuccess)
-                    return cuda_fail(e, "tail placement copy");
-            }
-        }
+        st = copy_engine_placement(plan, slots, slot_stride, full, mode == TIDE_AG_CE_2D, stream);
+        if (st != TIDE_OK)
+            return st;
     }
     e = mark_use(plan, stream);
     if (e != cudaSuccess)

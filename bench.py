@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--chunk-bytes", type=int, default=0)
     ap.add_argument("--fill-bytes", type=int, default=0, help="bulk kernel: bytes per rank per stage fill")
     ap.add_argument("--fill-ranks", type=int, default=0, help="bulk kernel: ranks per stage fill")
+    ap.add_argument("--ce-streams", type=int, default=0, help="copy-engine placement: internal streams")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-baseline", action="store_true", help="skip the two-pass GPU baseline")
@@ -383,7 +384,7 @@ def run_ours(args):
 
     gs = workloads.make_grads(w, device=dev)
     flags = tide.make_flags(cta_budget=args.cta_budget, chunk_bytes=args.chunk_bytes, fill_bytes=args.fill_bytes,
-                            fill_ranks=args.fill_ranks,
+                            fill_ranks=args.fill_ranks, ce_streams=args.ce_streams,
                             sched={"static": 0, "dynamic": 1}[args.sched],
                             kernel={"auto": 0, "direct": 1, "bulk": 2}[args.kernel])
     plan = tide.Plan(gs.views, flags)

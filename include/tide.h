@@ -121,7 +121,9 @@ enum {
 enum {
     TIDE_AG_SM = 0,      /* placement kernel: 16-byte vector copies per (parameter, rank) piece */
     TIDE_AG_CE_2D = 1,   /* copy engines: one 2D copy per parameter over its full-shard ranks
-                            (source pitch = slot stride, destination pitch = R_p K_p) + 1 tail copy */
+                            (source pitch = slot stride, destination pitch = R_p K_p) + 1 tail copy;
+                            pieces of 1 MiB or more are copied one by one instead, and large 2D
+                            copies are split by rows to balance the copy-engine streams */
     TIDE_AG_CE_1D = 2    /* copy engines: one 1D copy per (parameter, rank) piece */
 };
 
@@ -152,7 +154,9 @@ typedef struct {
     int32_t fill_ranks;   /* bulk kernel: ranks per stage fill (0 = min(W, 8)); wider groups take
                              several fills per chunk, summed in registers in rank order */
     int32_t node_size;    /* TIDE_ORDER_NODES: ranks per node, dividing the world; else 0 */
-    int32_t reserved[2];  /* must be zero */
+    int32_t ce_streams;   /* copy-engine placement: internal streams the copies are spread over,
+                             so several copy engines work at once (0 = 8, at most 8) */
+    int32_t reserved[1];  /* must be zero */
 } tide_plan_flags_t;
 
 /* Read-only view of one (parameter, rank) shard piece of a plan. */

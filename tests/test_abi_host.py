@@ -140,6 +140,7 @@ def test_empty_group(tide):
     ("node_size_not_dividing", "TIDE_ERR_INVALID_ARG"), ("node_size_without_nodes", "TIDE_ERR_INVALID_ARG"),
     ("nodes_without_size", "TIDE_ERR_INVALID_ARG"), ("staged_direct", "TIDE_ERR_UNSUPPORTED"),
     ("f32_dynamic", "TIDE_ERR_UNSUPPORTED"), ("f32_misaligned", "TIDE_ERR_ALIGNMENT"),
+    ("ce_streams", "TIDE_ERR_INVALID_ARG"),
 ])
 def test_build_validation(tide, case, status):
     W, dims = 4, [(8, 8), (5, 1)]
@@ -186,6 +187,8 @@ def test_build_validation(tide, case, status):
         kw.update(order=tide.TIDE_ORDER_STAGED_OWN, kernel=tide.TIDE_KERNEL_DIRECT)
     elif case == "f32_dynamic":
         kw.update(grad_dtype=tide.TIDE_DTYPE_F32, sched=tide.TIDE_SCHED_DYNAMIC)
+    elif case == "ce_streams":
+        kw.update(ce_streams=9)
     elif case == "f32_misaligned":
         kw.update(grad_dtype=tide.TIDE_DTYPE_F32)
         ptrs[1][1] += 2
@@ -196,7 +199,7 @@ def test_build_validation(tide, case, status):
         flags_debug |= 0x100
     flags = tide.make_flags(debug=flags_debug, **kw)
     if case == "reserved":
-        flags.reserved[1] = 1
+        flags.reserved[0] = 1
     params = [(ptrs[p], d, k, -1 if offsets is None else offsets[p]) for p, (d, k) in enumerate(dims)]
     with pytest.raises(tide.TideError) as e:
         tide.tide_plan_build(world, params, flags, 0)
