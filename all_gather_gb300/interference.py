@@ -6,8 +6,8 @@ the slowdown is the median duration of the victims that ran entirely inside
 the reduce-scatter window over the median duration of the victim alone,
 minus one.  Victims: a bf16 GEMM of 256 x 8192 x 8192 (the page's one-wave
 GEMM), a large 8192^3 bf16 GEMM, and a 256 MiB bf16 elementwise kernel.
-Arms: the fused fold at several CTA budgets and the two-pass stock-FSDP2
-baseline.  Set CUDA_DEVICE_MAX_CONNECTIONS=32 before CUDA starts (the page's
+Arms: the fused fold at several CTA budgets, the two-pass stock-FSDP2
+baseline, and the all-gather placement on SMs and on the copy engines.  Set CUDA_DEVICE_MAX_CONNECTIONS=32 before CUDA starts (the page's
 setting) so the two streams get separate hardware queues.
 
     python -m all_gather_gb300.interference [--workload NAME] [--budgets 0,16,64]
@@ -86,7 +86,7 @@ def _co_run(rs_call: Callable[[], None], n_rs: int, victim, victim_ms: float, rs
 
 
 def measure(workload: str = "llama3.1_8b_block", budgets=(0, 64, 16), n_rs: int = 20, device: int = 0,
-            grads=None) -> dict:
+            grads=None, with_placement: bool = True) -> dict:
     import torch
 
     import all_gather_gb300 as tide
@@ -106,6 +106,13 @@ def measure(workload: str = "llama3.1_8b_block", budgets=(0, 64, 16), n_rs: int 
     pack = torch.empty(w.world, w.world * S, device=dev)
     arms = {name: (lambda p=p: p.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)) for name, p in plans.items()}
     arms["two_pass_baseline"] = lambda: baselines.two_pass_rs(gs.views, pack, out, w.alpha, w.accumulate)
+    if with_placement:
+        # the all-gather side: placement on SMs vs on the copy engines (no SMs)
+        slots = workloads.make_slots(w, S, device=dev)
+        full = [torch.empty(s_, dtype=torch.bfloat16, device=dev) for s_ in w.shapes]
+        pl = next(iter(plans.values()))
+        arms["placement_sm_kernel"] = lambda: pl.ag_place(slots, full, mode="sm")
+        arms["placement_copy_engines"] = lambda: pl.ag_place(slots, full, mode="ce2d")
 
     quiet = torch.cuda.Stream()
     rs_alone = {name: _time_alone(fn, 10, quiet) for name, fn in arms.items()}
