@@ -23,9 +23,10 @@
  *
  * Conventions for every call:
  *   - Ownership: the caller owns every tensor (gradients, fp32 shards, bf16
- *     slots, full parameters).  A plan owns only its device tables (allocated
- *     in tide_plan_build, freed in tide_plan_destroy).  tide_rs_fold and
- *     tide_ag_place allocate nothing.
+ *     slots, full parameters).  A plan owns only its device tables and the
+ *     streams and events of its copy-engine placement (created in
+ *     tide_plan_build, released in tide_plan_destroy).  tide_rs_fold and the
+ *     placements allocate no device memory.
  *   - Pointers named "device" must be CUDA device (or managed) memory of the
  *     current device; pointers named "host" are ordinary host memory read
  *     before the call returns.
@@ -40,10 +41,11 @@
  *     was enqueued.  tide_last_error() gives a human-readable detail for the
  *     last failing call on the calling thread.
  *   - Numerics: bf16 -> fp32 widening is exact; the W contributions are added
- *     in fp32, round-to-nearest-even, in rank order 0, 1, ..., W-1 starting
- *     from rank 0's value; then y = alpha * sum; then out = old + y in
- *     accumulate mode.  No FMA contraction, no flush-to-zero.  Results are
- *     bitwise independent of CTA budget, chunk size and scheduling.
+ *     in fp32, round-to-nearest-even, in the plan's order -- by default rank
+ *     order 0, 1, ..., W-1 starting from rank 0's value; then y = alpha * sum;
+ *     then out = old + y in accumulate mode.  No FMA contraction, no
+ *     flush-to-zero.  Results are bitwise independent of CTA budget, chunk
+ *     size, stage shape and scheduling.
  */
 #ifndef TIDE_H
 #define TIDE_H
