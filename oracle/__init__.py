@@ -206,7 +206,7 @@ class Oracle:
 
 
     # -- other summation orders, fp32 gradients ----------------------------
-    ORDERS = {"rank": 0, "staged": 1, "nodes": 2}
+    ORDERS = {"rank": 0, "staged": 1, "nodes": 2, "tree": 3}
 
     def rs_ex(self, world: int, dims, grads, alpha: float, accumulate: bool, out: np.ndarray,
               order: str = "rank", node_size: int = 0) -> np.ndarray:

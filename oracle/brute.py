@@ -93,7 +93,7 @@ def all_gather(world: int, shapes: Sequence[Tuple[int, int]], slots: np.ndarray)
 def order_of(world: int, order: str, node_size: int, dest: int):
     """List of rank groups whose partials are added in list order; inside a
     group the ranks are added in list order (Section 4.3 readings)."""
-    if order == "rank":
+    if order in ("rank", "tree"):
         return [list(range(world))]
     if order == "staged":
         return [[u for u in range(world) if u != dest] + [dest]]
@@ -103,6 +103,20 @@ def order_of(world: int, order: str, node_size: int, dest: int):
         owner = n * node_size + dest % node_size
         groups.append([u for u in members if u != owner] + [owner])
     return groups
+
+
+def tree_sum(xs):
+    """Pairwise summation of xs (fp32) written recursively: the values before
+    the largest power of two below len(xs) form one balanced subtree, the rest
+    the other.  This is the same tree as adding neighbours level by level and
+    carrying an odd last value up (a different construction of it)."""
+    n = len(xs)
+    if n == 1:
+        return xs[0]
+    h = 1
+    while 2 * h < n:
+        h *= 2
+    return np.float32(tree_sum(xs[:h]) + tree_sum(xs[h:]))
 
 
 def reduce_scatter_ordered(world, shapes, grads, alpha, accumulate, old, order="rank", node_size=0):
@@ -126,7 +140,10 @@ def reduce_scatter_ordered(world, shapes, grads, alpha, accumulate, old, order="
                 row = r * R + i
                 for c in range(k):
                     total = None
-                    for grp in groups:
+                    if order == "tree":
+                        total = tree_sum([val(p, u, row * k + c) if row < d else np.float32(0.0)
+                                          for u in range(world)])
+                    for grp in ([] if order == "tree" else groups):
                         part = None
                         for u in grp:
                             x = val(p, u, row * k + c) if row < d else np.float32(0.0)

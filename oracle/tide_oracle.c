@@ -289,12 +289,20 @@ done:
  *                          its ranks except n L + (r mod L) ascending, then
  *                          that rank; the M node partials are then added in
  *                          node order
+ *   ORACLE_ORDER_TREE      pairwise (balanced-tree) summation of the rank
+ *                          sequence 0..W-1: level by level, neighbours
+ *                          (2i, 2i+1) are added and an odd last value moves
+ *                          up unchanged, until one value is left.  The page
+ *                          names no tree order; this is the textbook pairwise
+ *                          summation, whose rounding error grows with
+ *                          ceil(log2 W) instead of W - 1.
  * dtype 0: bf16 gradients (widened exactly); dtype 1: fp32 gradients
  * (b_grad = 4, used as they are).
  * ---------------------------------------------------------------------- */
 #define ORACLE_ORDER_RANK 0
 #define ORACLE_ORDER_STAGED 1
 #define ORACLE_ORDER_NODES 2
+#define ORACLE_ORDER_TREE 3
 
 static float widen(const void *src, int32_t dtype, int64_t j)
 {
@@ -308,7 +316,7 @@ static float widen(const void *src, int32_t dtype, int64_t j)
  * partials are then added in sequence order). */
 static int make_sequence(int32_t world, int32_t order, int32_t node_size, int32_t r, int32_t *seq, int32_t *group)
 {
-    if (order == ORACLE_ORDER_RANK) {
+    if (order == ORACLE_ORDER_RANK || order == ORACLE_ORDER_TREE) {
         for (int32_t u = 0; u < world; ++u)
             seq[u] = u;
         *group = world;
@@ -352,8 +360,9 @@ int oracle_rs_window_ex(int32_t world, int32_t dtype, int32_t order, int32_t nod
         return ORACLE_OK;
     int32_t *seq = (int32_t *)malloc(sizeof(int32_t) * (size_t)world);
     float *pack = (float *)malloc((size_t)world * (size_t)n * sizeof(float));
+    float *level = (float *)malloc(sizeof(float) * (size_t)world);
     int32_t group = world;
-    int rc = (seq && pack) ? make_sequence(world, order, node_size, dest, seq, &group) : ORACLE_ENOMEM;
+    int rc = (seq && pack && level) ? make_sequence(world, order, node_size, dest, seq, &group) : ORACLE_ENOMEM;
     if (rc != ORACLE_OK)
         goto done;
     /* pass 1: slice, zero-pad, widen */
@@ -365,14 +374,28 @@ int oracle_rs_window_ex(int32_t world, int32_t dtype, int32_t order, int32_t nod
             dst[j] = +0.0f;
     }
     /* pass 2: partials of `group` consecutive contributions of the sequence,
-     * then the partials in sequence order */
+     * then the partials in sequence order; or the pairwise tree */
     for (int64_t j = 0; j < n; ++j) {
         float total = 0.0f;
-        for (int32_t g0 = 0; g0 < world; g0 += group) {
-            float part = pack[(size_t)seq[g0] * (size_t)n + (size_t)j];
-            for (int32_t q = g0 + 1; q < g0 + group; ++q)
-                part = part + pack[(size_t)seq[q] * (size_t)n + (size_t)j];
-            total = (g0 == 0) ? part : total + part;
+        if (order == ORACLE_ORDER_TREE) {
+            int32_t m = world;
+            for (int32_t q = 0; q < world; ++q)
+                level[q] = pack[(size_t)seq[q] * (size_t)n + (size_t)j];
+            while (m > 1) {
+                for (int32_t i = 0; i < m / 2; ++i)
+                    level[i] = level[2 * i] + level[2 * i + 1];
+                if (m % 2 == 1)
+                    level[m / 2] = level[m - 1];
+                m = (m + 1) / 2;
+            }
+            total = level[0];
+        } else {
+            for (int32_t g0 = 0; g0 < world; g0 += group) {
+                float part = pack[(size_t)seq[g0] * (size_t)n + (size_t)j];
+                for (int32_t q = g0 + 1; q < g0 + group; ++q)
+                    part = part + pack[(size_t)seq[q] * (size_t)n + (size_t)j];
+                total = (g0 == 0) ? part : total + part;
+            }
         }
         float y = alpha * total;
         out[j] = accumulate ? (old[j] + y) : y;
@@ -380,6 +403,7 @@ int oracle_rs_window_ex(int32_t world, int32_t dtype, int32_t order, int32_t nod
 done:
     free(seq);
     free(pack);
+    free(level);
     return rc;
 }
 

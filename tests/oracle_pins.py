@@ -397,13 +397,49 @@ def pin_orders_closed_form(orc):
     assert_same_f32(run(8, 0, "nodes", 1), run(8, 0, "rank"), "nodes of one rank is rank order")
 
 
+def pin_tree_closed_form(orc):
+    """Hand-worked values of the pairwise (tree) order, 1.0 and U = 2^-24 terms
+    listed in rank order (near 1.0 one ulp is 2^-23, so U is half an ulp):
+    * W=3 [1,U,U]: (1+U)+U, each a tie back to 1: 1.0 (the odd value is
+      added last, as in rank order); [U,U,1]: 2U+1 = 1 + 2^-23.
+    * W=4 [1,U,U,U]: (1+U) = 1, (U+U) = 2U, 1 + 2U = 1 + 2^-23 exact
+      (rank order gives 1.0).
+    * W=5 [1,U,U,U,U]: 1, 2U, U -> 1 + 2^-23, U -> 1 + 1.5 ulp, tie to even:
+      1 + 2^-22.
+    * W=6 [1,0,U,U,0,0]: 1, 2U, 0 -> 1 + 2^-23, 0 -> 1 + 2^-23 (halving the
+      ranks 3 | 3 would give ((1+0)+U) + ((U+0)+0) = 1.0).
+    * W=7 [1,U,U,U,U,U,U]: 1, 2U, 2U, U -> 1 + 2^-23, 3U -> 1 + 2.5 ulp,
+      tie to even: 1 + 2^-22.
+    * W=8 [1,U x 7]: 1, 2U, 2U, 2U -> 1 + 2^-23, 4U -> 1 + 3 * 2^-23 exact.
+    * W=16 [1,U x 15]: 1, 2U x 7 -> 1 + 2^-23, 4U x 3 -> 1 + 3 * 2^-23, 8U
+      -> 1 + 7 * 2^-23 exact."""
+    one, u = 1.0, U
+
+    def run(vals):
+        W = len(vals)
+        bits = f32_to_bf16_bits(np.array(vals, np.float32))
+        g = [[np.array([bits[q]] * W, np.uint16) for q in range(W)]]
+        out = np.zeros((W, 1), np.float32)
+        orc.rs_ex(W, [(W, 1)], g, 1.0, False, out, "tree", 0)
+        return out.reshape(-1)
+
+    cases = [([one, u, u], 1.0), ([u, u, one], 1 + 2 ** -23), ([one, u, u, u], 1 + 2 ** -23),
+             ([one] + [u] * 4, 1 + 2 ** -22), ([one, 0.0, u, u, 0.0, 0.0], 1 + 2 ** -23),
+             ([one] + [u] * 6, 1 + 2 ** -22), ([one] + [u] * 7, 1 + 3 * 2 ** -23),
+             ([one] + [u] * 15, 1 + 7 * 2 ** -23)]
+    for vals, want in cases:
+        W = len(vals)
+        assert_same_f32(run(vals), np.full(W, want, np.float32), f"tree W={W} {vals[:3]}...")
+    assert_same_f32(run([one, u]), np.full(2, 1.0, np.float32), "tree of two is one add")
+
+
 def pin_orders_brute_force(orc, seed=29):
     from oracle import brute
     rnd = random.Random(seed)
     rng = np.random.default_rng(seed)
-    for c in range(24):
-        W = rnd.choice([1, 2, 3, 4, 6, 8])
-        order = rnd.choice(["rank", "staged", "nodes"])
+    for c in range(32):
+        W = rnd.choice([1, 2, 3, 4, 5, 6, 7, 8, 11, 13])
+        order = rnd.choice(["rank", "staged", "nodes", "tree"])
         L = rnd.choice([d for d in range(1, W + 1) if W % d == 0]) if order == "nodes" else 0
         dims = [(rnd.choice([1, 2, W, W + 1, 2 * W + 1]), rnd.choice([1, 3, 4])) for _ in range(rnd.randint(1, 3))]
         f32 = rnd.random() < 0.4
@@ -420,18 +456,19 @@ def pin_orders_brute_force(orc, seed=29):
 
 def pin_orders_exact_and_bounded(orc, seed=37):
     """Every order: integer inputs give the exact sum; normal inputs stay
-    within gamma_{W+1} (|alpha| sum |G| + |old|) of the fp64 sum and within
-    1e-6 of the rank-order result in the max-norm (the reordered-variant
-    tolerance); the rank order reproduces the original oracle bit for bit."""
+    within gamma_{W+1} (|alpha| sum |G| + |old|) of the fp64 sum (the tree
+    order within gamma_{ceil(log2 W)}, its depth) and within 1e-6 of the
+    rank-order result in the max-norm (the reordered-variant tolerance); the
+    rank order reproduces the original oracle bit for bit."""
     rng = np.random.default_rng(seed)
     for W, L in ((8, 4), (16, 4), (32, 8), (6, 3)):
         dims = [(4 * W + 3, 9), (W, 1)]
         ints = [[rng.integers(-128, 129, size=d * k) for _ in range(W)] for d, k in dims]
         gi = [[f32_to_bf16_bits(x.astype(np.float32)) for x in per] for per in ints]
         R, o, S = orc.geometry(W, dims)
-        for order in ("staged", "nodes"):
+        for order in ("staged", "nodes", "tree"):
             out = np.zeros((W, S), np.float32)
-            orc.rs_ex(W, dims, gi, 0.5, False, out, order, L)
+            orc.rs_ex(W, dims, gi, 0.5, False, out, order, L if order == "nodes" else 0)
             for p, (d, k) in enumerate(dims):
                 exact = sum(ints[p][u] for u in range(W)).astype(np.float64) * 0.5
                 flat = np.concatenate([out[r, o[p]:o[p] + R[p] * k] for r in range(W)])[:d * k]
@@ -443,13 +480,15 @@ def pin_orders_exact_and_bounded(orc, seed=37):
         orc.rs_ex(W, dims, g, 1.0, False, rank_ex, "rank", 0)
         assert_same_f32(rank_ex, ref, "rank order of the ordered oracle == original oracle")
         gamma = (W + 1) * U / (1 - (W + 1) * U)
-        for order in ("staged", "nodes"):
+        depth = (W - 1).bit_length()
+        for order in ("staged", "nodes", "tree"):
             out = np.zeros((W, S), np.float32)
-            orc.rs_ex(W, dims, g, 1.0, False, out, order, L)
+            orc.rs_ex(W, dims, g, 1.0, False, out, order, L if order == "nodes" else 0)
+            bound = gamma if order != "tree" else depth * U / (1 - depth * U)
             for p, (d, k) in enumerate(dims):
                 vals = np.stack([bf16_bits_to_f32(g[p][u]).astype(np.float64) for u in range(W)])
                 got = np.concatenate([out[r, o[p]:o[p] + R[p] * k] for r in range(W)])[:d * k]
-                assert (np.abs(got - vals.sum(0)) <= gamma * np.abs(vals).sum(0) + 1e-45).all(), order
+                assert (np.abs(got - vals.sum(0)) <= bound * np.abs(vals).sum(0) + 1e-45).all(), order
                 rk = np.concatenate([ref[r, o[p]:o[p] + R[p] * k] for r in range(W)])[:d * k]
                 assert np.abs(got - rk).max() <= 1e-6 * np.abs(rk).max(), f"{order} vs rank order"
 
@@ -478,5 +517,6 @@ def pin_f32_grads_chunk_cat(orc, seed=41):
 
 ALL_PINS = [pin_golden, pin_slot_sizes, pin_torch_chunk, pin_chunk_cat, pin_brute_force, pin_integer_exact,
             pin_order_probe, pin_fp64_bound, pin_special_values, pin_ag_identity, pin_window_matches_full,
-            pin_cast_vs_torch, pin_ag_cast_identity, pin_orders_closed_form, pin_orders_brute_force,
+            pin_cast_vs_torch, pin_ag_cast_identity, pin_orders_closed_form, pin_tree_closed_form,
+            pin_orders_brute_force,
             pin_orders_exact_and_bounded, pin_f32_grads_chunk_cat]

@@ -52,6 +52,9 @@ MUTANTS = {
     "nodes_as_one_chain": [("        *group = node_size;", "        *group = world;")],
     "f32_grads_truncated": [("    return ((const float *)src)[j];",
                              "    return bf16_to_f32((uint16_t)(((const uint32_t *)src)[j] >> 16));")],
+    "tree_as_rank_order": [("        if (order == ORACLE_ORDER_TREE) {", "        if (0) {")],
+    "tree_far_pairs": [("level[i] = level[2 * i] + level[2 * i + 1];", "level[i] = level[i] + level[i + m / 2];")],
+    "tree_odd_value_dropped": [("                    level[m / 2] = level[m - 1];", "                    ;")],
     "ag_cast_transposed_rank": [("uint16_t *dst_row = full[p] + (size_t)((r * R[p] + i) * K);",
                                  "uint16_t *dst_row = full[p] + (size_t)((i * (int64_t)world + r) * K);")],
 }
