@@ -7,7 +7,8 @@
 //     y    = alpha * acc
 //     out[r * stride + o_p + j] = accumulate ? out_old + y : y
 // and for padding positions (rows past D_p) the same with zero contributions.
-// (Section 4.3's other orders permute or group the additions; see seq_rank.)
+// (Section 4.3's other orders permute or group the additions, see seq_rank;
+// the tree order adds them pairwise, see tree_push.)
 //
 // The work is HBM-bound (W bf16 reads + one fp32 write, +1 fp32 read when
 // accumulating, per output element; ~0.4 flop/byte), so both kernels are
@@ -450,15 +451,39 @@ template <bool ACC, typename E>
 __device__ void fold_scalar_global(const uint64_t *bp, const FoldParams &fp, int r, int64_t src_off, float *dst)
 {
     const int W = fp.world;
-    const int group = fp.order == TIDE_ORDER_NODES ? fp.node_size : W;
-    float total = 0.0f, part = 0.0f;
-    for (int q = 0; q < W; ++q) {
-        const int u = seq_rank(fp.order, q, r, W, fp.node_size);
-        const float x = ld_elem<E>(reinterpret_cast<const E *>(bp[u]) + src_off);
-        const int l = q % group;
-        part = l == 0 ? x : __fadd_rn(part, x);
-        if (l == group - 1)
-            total = q < group ? part : __fadd_rn(total, part);
+    float total = 0.0f;
+    if (fp.order == TIDE_ORDER_TREE) {
+        // Pairwise order as a binary counter: slot[l] holds the sum of a
+        // complete subtree of 2^l ranks; rank q first absorbs the slots of
+        // the set bits below q's lowest clear bit.  The slots left (the set
+        // bits of W) are then added from the lowest level up.
+        float slot[11];  // W <= 1024
+        for (int q = 0; q < W; ++q) {
+            float c = ld_elem<E>(reinterpret_cast<const E *>(bp[q]) + src_off);
+            int l = 0;
+            while ((q >> l) & 1) {
+                c = __fadd_rn(slot[l], c);
+                ++l;
+            }
+            slot[l] = c;
+        }
+        bool have = false;
+        for (int l = 0; l < 11; ++l)
+            if ((W >> l) & 1) {
+                total = have ? __fadd_rn(slot[l], total) : slot[l];
+                have = true;
+            }
+    } else {
+        const int group = fp.order == TIDE_ORDER_NODES ? fp.node_size : W;
+        float part = 0.0f;
+        for (int q = 0; q < W; ++q) {
+            const int u = seq_rank(fp.order, q, r, W, fp.node_size);
+            const float x = ld_elem<E>(reinterpret_cast<const E *>(bp[u]) + src_off);
+            const int l = q % group;
+            part = l == 0 ? x : __fadd_rn(part, x);
+            if (l == group - 1)
+                total = q < group ? part : __fadd_rn(total, part);
+        }
     }
     float y = __fmul_rn(fp.alpha, total);
     if (ACC)
@@ -476,12 +501,132 @@ __device__ __forceinline__ void lds8(const float *p, float (&f)[8])
     f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
+__device__ __forceinline__ void add8(const float (&a)[8], float (&c)[8])
+{
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        c[e] = __fadd_rn(a[e], c[e]);
+}
+
+__device__ __forceinline__ void copy8(const float (&a)[8], float (&c)[8])
+{
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        c[e] = a[e];
+}
+
+// Tree order, one stage fill of nr <= 8 ranks (a power-of-two count, or the
+// last fill): a binary counter over the fill's ranks with compile-time
+// levels (slot[l]: complete subtree of 2^l ranks), then the slots of nr's
+// set bits folded from the lowest level up into `part`, earlier ranks on
+// the left of every addition.
+template <typename E>
+__device__ __forceinline__ void tree_fill(const E *sb, int64_t FILL, int64_t v, int nr, float (&part)[8])
+{
+    float s0[8], s1[8], s2[8], s3[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (j < nr) {
+            float c[8];
+            lds8(sb + size_t(j) * FILL + v * 8, c);
+            if (j & 1) {
+                add8(s0, c);
+                if (j & 2) {
+                    add8(s1, c);
+                    if (j & 4) {
+                        add8(s2, c);
+                        copy8(c, s3);
+                    } else {
+                        copy8(c, s2);
+                    }
+                } else {
+                    copy8(c, s1);
+                }
+            } else {
+                copy8(c, s0);
+            }
+        }
+    }
+    bool have = false;
+    if (nr & 1) {
+        copy8(s0, part);
+        have = true;
+    }
+    if (nr & 2) {
+        if (have) add8(s1, part); else copy8(s1, part);
+        have = true;
+    }
+    if (nr & 4) {
+        if (have) add8(s2, part); else copy8(s2, part);
+        have = true;
+    }
+    if (nr & 8) {
+        if (have) add8(s3, part); else copy8(s3, part);
+    }
+}
+
+// Tree order, a full fill of N = 2^k ranks: the balanced tree with
+// compile-time shape, e.g. ((x0+x1)+(x2+x3))+((x4+x5)+(x6+x7)) for N = 8.
+template <int N, typename E>
+__device__ __forceinline__ void tree_fill_pow2(const E *sb, int64_t FILL, int64_t v, float (&part)[8])
+{
+    float x[N][8];
+#pragma unroll
+    for (int j = 0; j < N; ++j)
+        lds8(sb + size_t(j) * FILL + v * 8, x[j]);
+    // After the level of width h, the subtree of ranks [j, j + 2h) is held in
+    // x[j + 2h - 1]; its left half (the earlier ranks) in x[j + h - 1].
+#pragma unroll
+    for (int h = 1; h < N; h *= 2)
+#pragma unroll
+        for (int j = 0; j < N; j += 2 * h)
+            add8(x[j + h - 1], x[j + 2 * h - 1]);
+    copy8(x[N - 1], part);
+}
+
+// Tree order across fills: push the partial of complete fill g into the
+// counter x (x[l]: complete subtree of 2^l fills; g < 2^LV - 1).  g is the
+// same for the whole CTA, so the switch is a uniform branch and every slot
+// index is a compile-time constant.
+template <int LV>
+__device__ __forceinline__ void tree_push(float (&x)[LV][8], int g, float (&part)[8])
+{
+    const int t = __ffs(~g) - 1;  // trailing ones of g: the slots this fill absorbs
+#pragma unroll
+    for (int l = 0; l < LV; ++l) {
+        if (l == t) {
+#pragma unroll
+            for (int m = 0; m < l; ++m)
+                add8(x[m], part);
+            copy8(part, x[l]);
+        }
+    }
+}
+
+// Consumer modes of the bulk kernel: one chain in the sequence the producer
+// stages (rank and one-node orders), node partials (two-level order), or the
+// pairwise tree: all ranks in one fill (no counter), up to 2^3 - 1 full fills
+// per chunk, or up to 2^kTreeLevels - 1 (each counter level costs 8
+// registers per vector, so the smaller counters keep two vectors per thread).
+enum { kModeChain = 0, kModeNodes = 1, kModeTreeOne = 2, kModeTree = 3, kModeTreeDeep = 4 };
+constexpr int kTreeLevelsShallow = 3;
+
+template <int MODE>
+struct TreeShape {
+    static constexpr bool tree = MODE >= kModeTreeOne;
+    static constexpr int levels = MODE == kModeTreeDeep ? kTreeLevels : MODE == kModeTree ? kTreeLevelsShallow : 0;
+    static constexpr int vec = MODE == kModeTreeDeep ? 1 : kBulkMaxVec;  // vectors per consumer thread
+};
+
 // ACC: accumulate into the existing shard.  E: gradient element (uint16_t =
-// bf16, float = fp32).  GROUPED: the two-level order (node partials); other
-// orders are one chain whose sequence the producer applies when it stages.
-template <bool ACC, typename E, bool GROUPED>
+// bf16, float = fp32).  MODE: how the consumers combine the staged ranks.
+template <bool ACC, typename E, int MODE>
 __global__ void __launch_bounds__(kBulkThreads, 2) fold_bulk_kernel(const FoldParams fp)
 {
+    constexpr bool GROUPED = MODE == kModeNodes;
+    constexpr bool TREE = TreeShape<MODE>::tree;
+    constexpr int LV = TreeShape<MODE>::levels;
+    constexpr int NV = TREE ? TreeShape<MODE>::vec : kBulkMaxVec;
     extern __shared__ __align__(128) unsigned char smem[];
     const int W = fp.world;
     const int RG = fp.fill_ranks;          // ranks per stage fill
@@ -572,7 +717,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fold_bulk_kernel(const FoldPa
     }
 
     // ---------------------------------------------------------------- consumers
-    // Each consumer thread owns up to kBulkMaxVec 8-element vectors of a
+    // Each consumer thread owns up to NV 8-element vectors of a
     // chunk and keeps their fp32 sums in registers across the chunk's NG
     // fills, so the contributions are added in the plan's sequence.
     const int ctid = threadIdx.x - 32;
@@ -600,14 +745,15 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fold_bulk_kernel(const FoldPa
         for (int64_t c = 0; c < count; c += FILL) {
             const int64_t len = count - c < FILL ? count - c : FILL;
             const int64_t nv = len >> 3;
-            float acc[kBulkMaxVec][8];
-            float part[GROUPED ? kBulkMaxVec : 1][8];
-            float old[kBulkMaxVec][8];
+            float acc[NV][8];
+            float part[GROUPED ? NV : 1][8];
+            float tx[TREE ? NV : 1][LV > 0 ? LV : 1][8];
+            float old[NV][8];
             if (ACC) {
                 // Issue the loads of the existing shard values before waiting
                 // for the chunk's fills, so their latency overlaps the copies.
 #pragma unroll
-                for (int k = 0; k < kBulkMaxVec; ++k) {
+                for (int k = 0; k < NV; ++k) {
                     const int64_t v = ctid + int64_t(k) * NCT;
                     if (v < nv)
                         load8(dst + c + v * 8, old[k], dst_vec);
@@ -624,10 +770,26 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fold_bulk_kernel(const FoldPa
                 }
                 const E *sb = ring + size_t(stage) * RG * FILL;
 #pragma unroll
-                for (int k = 0; k < kBulkMaxVec; ++k) {
+                for (int k = 0; k < NV; ++k) {
                     const int64_t v = ctid + int64_t(k) * NCT;
                     if (v < nv) {
-                        if (!GROUPED) {
+                        if constexpr (TREE) {
+                            float p[8];
+                            if (nr == 8)
+                                tree_fill_pow2<8>(sb, FILL, v, p);
+                            else if (nr == 4)
+                                tree_fill_pow2<4>(sb, FILL, v, p);
+                            else if (nr == 2)
+                                tree_fill_pow2<2>(sb, FILL, v, p);
+                            else
+                                tree_fill(sb, FILL, v, nr, p);
+                            if constexpr (LV == 0)
+                                copy8(p, acc[k]);  // the one fill holds every rank
+                            else if (nr == RG)
+                                tree_push<LV>(tx[k], g, p);
+                            else
+                                copy8(p, acc[k]);  // the last fill, short: its partial waits in acc
+                        } else if (!GROUPED) {
                             int j0 = 0;
                             if (g == 0) {
                                 lds8(sb + v * 8, acc[k]);
@@ -688,8 +850,24 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fold_bulk_kernel(const FoldPa
                     phase ^= 1u;
                 }
             }
+            if constexpr (TREE && LV > 0) {
+                // The counter's slots (set bits of the full-fill count) join
+                // the short fill's partial from the lowest level up.
+                const int nfull = W / RG;
 #pragma unroll
-            for (int k = 0; k < kBulkMaxVec; ++k) {
+                for (int k = 0; k < NV; ++k) {
+                    bool have = nfull * RG != W;
+#pragma unroll
+                    for (int l = 0; l < LV; ++l) {
+                        if ((nfull >> l) & 1) {
+                            if (have) add8(tx[k][l], acc[k]); else copy8(tx[k][l], acc[k]);
+                            have = true;
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
                 const int64_t v = ctid + int64_t(k) * NCT;
                 if (v < nv)
                     store8_onto<ACC>(dst + c + v * 8, acc[k], old[k], alpha, dst_vec);
@@ -700,32 +878,60 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fold_bulk_kernel(const FoldPa
     }
 }
 
-template <bool ACC>
-FoldKernel pick_bulk(int dtype, int order)
+template <bool ACC, typename E>
+FoldKernel pick_bulk_mode(int order, int fills, int full_fills)
 {
-    const bool grouped = order == TIDE_ORDER_NODES;
-    if (dtype == TIDE_DTYPE_F32)
-        return grouped ? fold_bulk_kernel<ACC, float, true> : fold_bulk_kernel<ACC, float, false>;
-    return grouped ? fold_bulk_kernel<ACC, uint16_t, true> : fold_bulk_kernel<ACC, uint16_t, false>;
+    if (order == TIDE_ORDER_NODES)
+        return fold_bulk_kernel<ACC, E, kModeNodes>;
+    if (order == TIDE_ORDER_TREE) {
+        if (fills == 1)
+            return fold_bulk_kernel<ACC, E, kModeTreeOne>;
+        if (full_fills < (1 << kTreeLevelsShallow))
+            return fold_bulk_kernel<ACC, E, kModeTree>;
+        return fold_bulk_kernel<ACC, E, kModeTreeDeep>;
+    }
+    return fold_bulk_kernel<ACC, E, kModeChain>;
+}
+
+// The tree counter's depth follows the stage fills per chunk: `fills` in
+// all, `full_fills` of them holding fill_ranks ranks.
+template <bool ACC>
+FoldKernel pick_bulk(int dtype, int order, int world, int fill_ranks)
+{
+    const int fills = (world + fill_ranks - 1) / fill_ranks, full_fills = world / fill_ranks;
+    return dtype == TIDE_DTYPE_F32 ? pick_bulk_mode<ACC, float>(order, fills, full_fills)
+                                   : pick_bulk_mode<ACC, uint16_t>(order, fills, full_fills);
 }
 
 }  // namespace
 
-BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_sm, int elem_bytes)
+BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_sm, int elem_bytes, int order)
 {
     // Default: 4 KB of each of up to 8 ranks per stage fill (32 KB stages),
     // three stages per CTA, two CTAs per SM.  Wider groups take several fills
     // per chunk; the consumers keep the partial sums in registers meanwhile.
+    // The tree order: fills of a power-of-two number of ranks (at most 8), so
+    // that every full fill is a complete subtree; with 8 or more full fills
+    // per chunk (the deep counter) one vector per consumer thread, so half
+    // the fill.
+    const bool tree = order == TIDE_ORDER_TREE;
     BulkShape b{};
+    int rg = fill_ranks > 0 ? fill_ranks : 8;
+    if (tree && rg > 8)
+        rg = 8;
+    if (rg >= world)
+        rg = world;
+    else if (tree)
+        while (rg & (rg - 1))
+            rg &= rg - 1;  // largest power of two not above it
+    const bool deep = tree && rg < world && world / rg >= (1 << kTreeLevelsShallow);
+    const int64_t max_fill = deep ? kBulkMaxFill / kBulkMaxVec : kBulkMaxFill;
     int64_t fill = fill_elems > 0 ? fill_elems : 4096 / elem_bytes;
-    if (fill > kBulkMaxFill)
-        fill = kBulkMaxFill;
+    if (fill > max_fill)
+        fill = max_fill;
     fill &= ~int64_t(7);
     if (fill < 8)
         fill = 8;
-    int rg = fill_ranks > 0 ? fill_ranks : 8;
-    if (rg > world)
-        rg = world;
     while (fill > 8 && fill * rg * elem_bytes * 2 > 200 * 1024)  // two stages must fit in shared memory
         fill = (fill / 2) & ~int64_t(7);
     const int64_t stage_bytes = fill * rg * elem_bytes;
@@ -742,14 +948,16 @@ BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_s
     return b;
 }
 
-size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems, int fill_ranks, bool whole_sm, int elem_bytes)
+size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems, int fill_ranks, bool whole_sm, int elem_bytes,
+                       int order)
 {
     if (kernel == TIDE_KERNEL_BULK)
-        return bulk_shape(world, fill_elems, fill_ranks, whole_sm, elem_bytes).smem_bytes;
+        return bulk_shape(world, fill_elems, fill_ranks, whole_sm, elem_bytes, order).smem_bytes;
     return size_t(world) * sizeof(uint64_t);
 }
 
-cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *blocks_per_sm, int dtype, int order)
+cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *blocks_per_sm, int dtype, int order,
+                           int fill_ranks)
 {
     if (kernel == TIDE_KERNEL_BULK) {
         // Allow the device maximum once per kernel instance: it serves every
@@ -762,14 +970,15 @@ cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *b
             return e;
         if (smem > size_t(optin))
             return cudaErrorInvalidValue;
+        const int rg = bulk_shape(world, 0, fill_ranks, false, dtype == TIDE_DTYPE_F32 ? 4 : 2, order).fill_ranks;
         for (int acc = 0; acc < 2; ++acc) {
-            FoldKernel k = acc ? pick_bulk<true>(dtype, order) : pick_bulk<false>(dtype, order);
+            FoldKernel k = acc ? pick_bulk<true>(dtype, order, world, rg) : pick_bulk<false>(dtype, order, world, rg);
             e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
             if (e != cudaSuccess)
                 return e;
         }
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, pick_bulk<false>(dtype, order), block,
-                                                             smem);
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            blocks_per_sm, pick_bulk<false>(dtype, order, world, rg), block, smem);
     }
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, pick_direct<false>(world), block, smem);
 }
@@ -779,7 +988,8 @@ cudaError_t launch_fold(const FoldParams &fp, int kernel, int accumulate, int gr
 {
     FoldKernel k;
     if (kernel == TIDE_KERNEL_BULK)
-        k = accumulate ? pick_bulk<true>(fp.dtype, fp.order) : pick_bulk<false>(fp.dtype, fp.order);
+        k = accumulate ? pick_bulk<true>(fp.dtype, fp.order, fp.world, fp.fill_ranks)
+                       : pick_bulk<false>(fp.dtype, fp.order, fp.world, fp.fill_ranks);
     else
         k = accumulate ? pick_direct<true>(fp.world) : pick_direct<false>(fp.world);
     k<<<grid, block, smem, stream>>>(fp);

@@ -95,7 +95,12 @@ struct BulkShape {
     size_t smem_bytes;
 };
 // fill_elems / fill_ranks 0 = default; whole_sm: the grid has at most one CTA per SM
-BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_sm, int elem_bytes);
+BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_sm, int elem_bytes,
+                     int order = TIDE_ORDER_RANK_ASC);
+// Tree order: partials of complete stage fills are kept per level of a
+// binary counter in registers, so a chunk holds at most 2^kTreeLevels - 1
+// full fills.
+constexpr int kTreeLevels = 8;
 
 struct AgParams {
     const Seg *segs;
@@ -113,9 +118,9 @@ struct AgParams {
 cudaError_t launch_fold(const FoldParams &fp, int kernel, int accumulate, int grid, int block, size_t smem,
                         cudaStream_t stream);
 cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *blocks_per_sm,
-                           int dtype = TIDE_DTYPE_BF16, int order = TIDE_ORDER_RANK_ASC);
+                           int dtype = TIDE_DTYPE_BF16, int order = TIDE_ORDER_RANK_ASC, int fill_ranks = 0);
 size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems, int fill_ranks, bool whole_sm,
-                       int elem_bytes = 2);
+                       int elem_bytes = 2, int order = TIDE_ORDER_RANK_ASC);
 cudaError_t launch_ag(const AgParams &ap, int grid, cudaStream_t stream);
 cudaError_t launch_ag_f32(const AgParams &ap, int grid, cudaStream_t stream);
 

@@ -100,7 +100,8 @@ tide_status_t check_flags(const tide_plan_flags_t &f)
     if (f.chunk_bytes != 0 && (f.chunk_bytes < 256 || f.chunk_bytes % 256 != 0 || f.chunk_bytes > (1 << 26)))
         return fail(TIDE_ERR_INVALID_ARG, "flags.chunk_bytes %d: need 0 or a multiple of 256 in [256, 2^26]",
                     f.chunk_bytes);
-    if (f.order != TIDE_ORDER_RANK_ASC && f.order != TIDE_ORDER_STAGED_OWN && f.order != TIDE_ORDER_NODES)
+    if (f.order != TIDE_ORDER_RANK_ASC && f.order != TIDE_ORDER_STAGED_OWN && f.order != TIDE_ORDER_NODES &&
+        f.order != TIDE_ORDER_TREE)
         return fail(TIDE_ERR_UNSUPPORTED, "flags.order %d is not implemented", f.order);
     if (f.order == TIDE_ORDER_NODES ? f.node_size < 1 : f.node_size != 0)
         return fail(TIDE_ERR_INVALID_ARG, "flags.node_size %d (positive with TIDE_ORDER_NODES only)", f.node_size);
@@ -310,6 +311,14 @@ static tide_status_t plan_build_impl(int32_t world, int32_t num_params, const ti
     plan->elem_bytes = f.grad_dtype == TIDE_DTYPE_F32 ? 4 : 2;
     if (f.order == TIDE_ORDER_NODES && world % f.node_size != 0)
         return bail(fail(TIDE_ERR_INVALID_ARG, "node_size %d does not divide world %d", f.node_size, world));
+    if (f.order == TIDE_ORDER_TREE) {
+        const tide::BulkShape bs =
+            tide::bulk_shape(world, f.fill_bytes / plan->elem_bytes, f.fill_ranks, false, plan->elem_bytes, f.order);
+        if (world / bs.fill_ranks >= (1 << tide::kTreeLevels))
+            return bail(fail(TIDE_ERR_INVALID_ARG,
+                             "tree order: %d full stage fills of %d ranks per chunk (at most %d); raise fill_ranks",
+                             world / bs.fill_ranks, bs.fill_ranks, (1 << tide::kTreeLevels) - 1));
+    }
     if (f.kernel == TIDE_KERNEL_AUTO && f.sched == TIDE_SCHED_DYNAMIC)
         plan->kernel = TIDE_KERNEL_DIRECT;  // only the direct kernel claims items dynamically
 
@@ -401,8 +410,8 @@ static tide_status_t plan_build_impl(int32_t world, int32_t num_params, const ti
         return bail(fail(TIDE_ERR_UNSUPPORTED, "too many work items; raise chunk_bytes"));
 
     plan->block = plan->kernel == TIDE_KERNEL_BULK ? tide::kBulkThreads : tide::kFoldThreads;
-    plan->fold_smem =
-        tide::fold_smem_bytes(plan->kernel, world, f.fill_bytes / plan->elem_bytes, f.fill_ranks, false, plan->elem_bytes);
+    plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, f.fill_bytes / plan->elem_bytes, f.fill_ranks,
+                                            false, plan->elem_bytes, f.order);
     if (plan->host_only) {
         plan->grid = f.cta_budget ? f.cta_budget : 0;
         *plan_out = plan;
@@ -421,9 +430,10 @@ static tide_status_t plan_build_impl(int32_t world, int32_t num_params, const ti
     plan->whole_sm = plan->kernel == TIDE_KERNEL_BULK && f.cta_budget > 0 && f.cta_budget <= sms;
     if (plan->whole_sm)
         plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, f.fill_bytes / plan->elem_bytes, f.fill_ranks,
-                                                true, plan->elem_bytes);
+                                                true, plan->elem_bytes, f.order);
     int per_sm = 0;
-    e = tide::fold_occupancy(plan->kernel, world, plan->block, plan->fold_smem, &per_sm, f.grad_dtype, f.order);
+    e = tide::fold_occupancy(plan->kernel, world, plan->block, plan->fold_smem, &per_sm, f.grad_dtype, f.order,
+                             f.fill_ranks);
     if (e != cudaSuccess)
         return bail(cuda_fail(e, "fold occupancy"));
     if (per_sm < 1)
@@ -560,7 +570,8 @@ tide_status_t tide_rs_fold(tide_plan_t *plan, float *out_base, int64_t out_slot_
     fp.debug = plan->flags.debug;
     fp.wait_budget_ns = (plan->flags.debug & TIDE_DEBUG_SHORT_WAIT) ? tide::kShortWaitBudgetNs : tide::kWaitBudgetNs;
     const tide::BulkShape bs = tide::bulk_shape(plan->world, plan->flags.fill_bytes / plan->elem_bytes,
-                                                plan->flags.fill_ranks, plan->whole_sm, plan->elem_bytes);
+                                                plan->flags.fill_ranks, plan->whole_sm, plan->elem_bytes,
+                                                plan->flags.order);
     fp.order = plan->flags.order;
     fp.node_size = plan->flags.node_size;
     fp.dtype = plan->flags.grad_dtype;

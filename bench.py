@@ -38,6 +38,9 @@ DEFAULT_WORKLOAD = "llama3.1_8b_block"
 SAMPLE_PARAMS = ("q_proj", "k_proj", "v_proj", "o_proj")  # CPU sample: the attention projections
 
 
+ORDERS = {"rank": 0, "staged": 1, "nodes": 2, "tree": 3}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -53,6 +56,9 @@ def parse():
     ap.add_argument("--fill-bytes", type=int, default=0, help="bulk kernel: bytes per rank per stage fill")
     ap.add_argument("--fill-ranks", type=int, default=0, help="bulk kernel: ranks per stage fill")
     ap.add_argument("--ce-streams", type=int, default=0, help="copy-engine placement: internal streams")
+    ap.add_argument("--order", choices=list(ORDERS), default="rank",
+                    help="summation order of the fold (rank order is the bit-exact contract)")
+    ap.add_argument("--node-size", type=int, default=0, help="two-level order: ranks per node (0: half the world)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-baseline", action="store_true", help="skip the two-pass GPU baseline")
@@ -386,7 +392,8 @@ def run_ours(args):
     flags = tide.make_flags(cta_budget=args.cta_budget, chunk_bytes=args.chunk_bytes, fill_bytes=args.fill_bytes,
                             fill_ranks=args.fill_ranks, ce_streams=args.ce_streams,
                             sched={"static": 0, "dynamic": 1}[args.sched],
-                            kernel={"auto": 0, "direct": 1, "bulk": 2}[args.kernel])
+                            kernel={"auto": 0, "direct": 1, "bulk": 2}[args.kernel], order=ORDERS[args.order],
+                            node_size=(args.node_size or max(1, w.world // 2)) if args.order == "nodes" else 0)
     plan = tide.Plan(gs.views, flags)
     S = plan.slot_numel
     cfg = plan.fold_config()
@@ -451,7 +458,7 @@ def run_ours(args):
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "world": w.world, "params": w.num_params, "elements": numel,
-                   "alpha": w.alpha, "accumulate": w.accumulate, "ag_mode": args.ag_mode,
+                   "alpha": w.alpha, "accumulate": w.accumulate, "ag_mode": args.ag_mode, "order": args.order,
                    "fold_grid": cfg["grid"], "fold_block": cfg["block"], "fold_items": cfg["items"],
                    "chunk_elems": cfg["chunk_elems"], "l2": "inputs larger than L2 (no flush)",
                    "step": "tide_rs_fold + tide_ag_place", "parallelism": f"weak: {world} independent replicas"},
@@ -463,13 +470,13 @@ def run_ours(args):
         "device": {"name": torch.cuda.get_device_name(dev),
                    "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profile_traffic(w.name),
+                     "frac": round(achieved / peak, 4), "traffic": profile_traffic(w.name) if args.order == "rank" else None,
                      "kernel": "tide_rs_fold", "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "frac_of_8tbs_nominal": round(achieved / 8000.0, 4)},
         "gpu_launches": int(launches),
         "clocks": clk,
-        "sm_time": profile_sm_time(w.name),
+        "sm_time": profile_sm_time(w.name) if args.order == "rank" else None,
     }
 
     # the other placement engines and the mixed-precision placement, timed alone after the step
@@ -525,7 +532,7 @@ def time_variants(plan, w, S, slots, full, dev, gs_views, steps: int = 20) -> di
         "ag_place ce2d (copy engines, one 2D copy per parameter)": (lambda: plan.ag_place(slots, full, "ce2d"), 4 * N),
         "ag_place ce1d (copy engines, one copy per piece)": (lambda: plan.ag_place(slots, full, "ce1d"), 4 * N),
     }
-    # the fold in the other Section 4.3 orders, and with fp32 gradients
+    # the fold in the other Section 4.3 orders, the tree order, and with fp32 gradients
     out_v = torch.zeros(w.world, S, device=dev)
     rs_b = w.world * N * 2 + N * 4 + (N * 4 if w.accumulate else 0)
     L = max(1, w.world // 2)
@@ -534,6 +541,7 @@ def time_variants(plan, w, S, slots, full, dev, gs_views, steps: int = 20) -> di
             gs_views, tide.make_flags(order=tide.TIDE_ORDER_STAGED_OWN)),
         f"rs_fold order=nodes node_size={L} (two-level order)": tide.Plan(
             gs_views, tide.make_flags(order=tide.TIDE_ORDER_NODES, node_size=L)),
+        "rs_fold order=tree (pairwise)": tide.Plan(gs_views, tide.make_flags(order=tide.TIDE_ORDER_TREE)),
     }
     for name, pl in plans.items():
         calls[name] = ((lambda pl=pl: pl.rs_fold(out_v, alpha=w.alpha, accumulate=w.accumulate)), rs_b)

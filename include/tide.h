@@ -99,10 +99,15 @@ enum {
     TIDE_ORDER_RANK_ASC = 0,   /* ((G0 + G1) + G2) + ... : the bit-exact contract */
     TIDE_ORDER_STAGED_OWN = 1, /* one node (Level 1): every rank except the destination r in
                                   ascending order, then r's own contribution */
-    TIDE_ORDER_NODES = 2       /* two levels: W = M nodes of node_size ranks; each node's partial
+    TIDE_ORDER_NODES = 2,      /* two levels: W = M nodes of node_size ranks; each node's partial
                                   adds its ranks except n*node_size + (r mod node_size) in
                                   ascending order, then that rank; the node partials are then
                                   added in node order */
+    TIDE_ORDER_TREE = 3        /* pairwise summation of ranks 0..W-1: neighbours added level by
+                                  level, an odd last value carried up (depth ceil(log2 W)).  Not
+                                  one of the paper's orders: the balanced alternative to its
+                                  chains.  Bulk kernel; stage fills of a power-of-two number of
+                                  ranks, at most 255 full fills per chunk (W / fill_ranks) */
 };
 
 /* Work distribution of the fold's persistent grid (bitwise identical results). */

@@ -140,7 +140,8 @@ def test_empty_group(tide):
     ("node_size_not_dividing", "TIDE_ERR_INVALID_ARG"), ("node_size_without_nodes", "TIDE_ERR_INVALID_ARG"),
     ("nodes_without_size", "TIDE_ERR_INVALID_ARG"), ("staged_direct", "TIDE_ERR_UNSUPPORTED"),
     ("f32_dynamic", "TIDE_ERR_UNSUPPORTED"), ("f32_misaligned", "TIDE_ERR_ALIGNMENT"),
-    ("ce_streams", "TIDE_ERR_INVALID_ARG"),
+    ("ce_streams", "TIDE_ERR_INVALID_ARG"), ("tree_direct", "TIDE_ERR_UNSUPPORTED"),
+    ("tree_node_size", "TIDE_ERR_INVALID_ARG"), ("tree_dynamic", "TIDE_ERR_UNSUPPORTED"),
 ])
 def test_build_validation(tide, case, status):
     W, dims = 4, [(8, 8), (5, 1)]
@@ -189,6 +190,12 @@ def test_build_validation(tide, case, status):
         kw.update(grad_dtype=tide.TIDE_DTYPE_F32, sched=tide.TIDE_SCHED_DYNAMIC)
     elif case == "ce_streams":
         kw.update(ce_streams=9)
+    elif case == "tree_direct":
+        kw.update(order=tide.TIDE_ORDER_TREE, kernel=tide.TIDE_KERNEL_DIRECT)
+    elif case == "tree_node_size":
+        kw.update(order=tide.TIDE_ORDER_TREE, node_size=2)
+    elif case == "tree_dynamic":
+        kw.update(order=tide.TIDE_ORDER_TREE, sched=tide.TIDE_SCHED_DYNAMIC)
     elif case == "f32_misaligned":
         kw.update(grad_dtype=tide.TIDE_DTYPE_F32)
         ptrs[1][1] += 2
@@ -205,6 +212,22 @@ def test_build_validation(tide, case, status):
         tide.tide_plan_build(world, params, flags, 0)
     assert tide.tide_status_string(e.value.status) == status, str(e.value)
     assert e.value.detail, "a failing call must leave a detail message"
+
+
+def test_tree_order_fill_limit(tide):
+    """The tree order keeps one partial per level of full stage fills in
+    registers: at most 255 full fills per chunk (W / fill_ranks, the fill
+    ranks rounded down to a power of two, at most 8)."""
+    W = 1024
+    dims = [(W, 1)]
+    for fill_ranks, ok in ((0, True), (8, True), (16, True), (5, False), (4, False), (1, False)):
+        if ok:
+            tide.tide_plan_destroy(_host_plan(tide, W, dims, order=tide.TIDE_ORDER_TREE, fill_ranks=fill_ranks))
+        else:
+            with pytest.raises(tide.TideError) as e:
+                _host_plan(tide, W, dims, order=tide.TIDE_ORDER_TREE, fill_ranks=fill_ranks)
+            assert e.value.status == tide.TIDE_ERR_INVALID_ARG, fill_ranks
+    tide.tide_plan_destroy(_host_plan(tide, 1020, [(1020, 1)], order=tide.TIDE_ORDER_TREE, fill_ranks=4))
 
 
 def test_host_only_plan_cannot_launch(tide):

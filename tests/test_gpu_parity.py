@@ -16,6 +16,8 @@ import workloads
 from bits import assert_same_bf16, assert_same_f32, assert_same_u16, bf16_bits_to_f32, f32_to_bf16_bits
 from gpu_helpers import (ag_expected, bits16, oracle_rs_full, sampled_rs_check, sentinel_slots)
 
+U = 2.0 ** -24  # half an ulp of 1.0 in binary32
+
 pytestmark = pytest.mark.gpu
 
 CANARY = float.fromhex("0x1.deadbep+100")
@@ -201,7 +203,10 @@ def test_determinism_across_launch_shapes():
 
 
 ORDER_CASES = [("staged", tide.TIDE_ORDER_STAGED_OWN, 0), ("nodes2", tide.TIDE_ORDER_NODES, 2),
-               ("nodes_w", tide.TIDE_ORDER_NODES, -1), ("nodes1", tide.TIDE_ORDER_NODES, 1)]
+               ("nodes_w", tide.TIDE_ORDER_NODES, -1), ("nodes1", tide.TIDE_ORDER_NODES, 1),
+               ("tree", tide.TIDE_ORDER_TREE, 0)]
+ORDER_NAMES = {tide.TIDE_ORDER_STAGED_OWN: "staged", tide.TIDE_ORDER_NODES: "nodes", tide.TIDE_ORDER_TREE: "tree",
+               tide.TIDE_ORDER_RANK_ASC: "rank"}
 
 
 def _ordered_fold(grads_uv, alpha, acc, out, order, node_size, f32=False, **kw):
@@ -225,9 +230,10 @@ def _host_grads(grads_uv, f32):
 @pytest.mark.parametrize("f32", [False, True], ids=["bf16", "fp32"])
 @pytest.mark.parametrize("world", [4, 6, 8, 32])
 def test_orders_and_fp32_grads(case, f32, world):
-    """Every Section 4.3 order, bf16 and fp32 gradients: bit-exact against the
-    oracle in the same order, and within 1e-6 (max-norm, per parameter and
-    rank) of the rank-order oracle."""
+    """Every Section 4.3 order and the tree order, bf16 and fp32 gradients:
+    bit-exact against the oracle in the same order, and within 1e-6 (max-norm,
+    per parameter and rank) of the rank-order oracle.  The fill_ranks = 3
+    launch runs the tree in fills of 2 ranks (the deep counter at W = 32)."""
     name, order, L = case
     L = world if L == -1 else L
     if order == tide.TIDE_ORDER_NODES and world % L:
@@ -242,7 +248,7 @@ def test_orders_and_fp32_grads(case, f32, world):
         views = [[v + torch.randn_like(v) * 1e-6 for v in vs] for vs in views]
     dims = w.dim0_rownumel()
     R, o, S = oracle.geometry(world, dims)
-    oname = {tide.TIDE_ORDER_STAGED_OWN: "staged", tide.TIDE_ORDER_NODES: "nodes"}[order]
+    oname = ORDER_NAMES[order]
     host = _host_grads(views, f32)
     for acc, kw in ((False, {}), (True, {"fill_bytes": 64, "fill_ranks": 3}), (False, {"chunk_bytes": 256})):
         init = torch.randn(world, S, device="cuda") if acc else None
@@ -293,12 +299,45 @@ def test_orders_misaligned_pieces(f32):
     _, _, S = oracle.geometry(world, dims)
     host = _host_grads(views, f32)
     for order, L, oname in ((tide.TIDE_ORDER_STAGED_OWN, 0, "staged"), (tide.TIDE_ORDER_NODES, 2, "nodes"),
-                            (tide.TIDE_ORDER_RANK_ASC, 0, "rank")):
+                            (tide.TIDE_ORDER_RANK_ASC, 0, "rank"), (tide.TIDE_ORDER_TREE, 0, "tree")):
         out = torch.zeros(world, S, device="cuda")
         _ordered_fold(views, 1.0, False, out, order, L, f32)
         want = np.zeros((world, S), np.float32)
         oracle.rs_ex(world, dims, host, 1.0, False, want, oname, L)
         assert_same_f32(out.cpu().numpy(), want, f"misaligned {oname} f32={f32}")
+
+
+TREE_PROBES = [([1.0, U, U], 1.0), ([U, U, 1.0], 1 + 2 ** -23), ([1.0, U, U, U], 1 + 2 ** -23),
+               ([1.0] + [U] * 4, 1 + 2 ** -22), ([1.0, 0.0, U, U, 0.0, 0.0], 1 + 2 ** -23),
+               ([1.0] + [U] * 6, 1 + 2 ** -22), ([1.0] + [U] * 7, 1 + 3 * 2 ** -23),
+               ([1.0] + [U] * 15, 1 + 7 * 2 ** -23), ([1.0] + [U] * 11, None)]
+
+
+@pytest.mark.parametrize("case", range(len(TREE_PROBES)))
+@pytest.mark.parametrize("fill_ranks", [0, 2, 4])
+def test_tree_order_probe(case, fill_ranks):
+    """Hand-worked pairwise sums of 1.0 and 2^-24 terms (rank q holds vals[q]
+    in every element): W = 3 .. 16, whole-vector, tail and padding elements,
+    stage fills of 8, 2 and 4 ranks; the last case (W = 12) is checked against
+    the oracle."""
+    vals, want = TREE_PROBES[case]
+    world = len(vals)
+    shapes = [(world * 300 + 5, 8), (world + 1, 3)]
+    w = workloads.custom(world, shapes, index=700 + world)
+    gs = workloads.make_grads(w, device="cuda", fill=lambda u, p, n, dev: torch.full((n,), vals[u], device=dev))
+    dims = w.dim0_rownumel()
+    R, o, S = oracle.geometry(world, dims)
+    out = torch.zeros(world, S, device="cuda")
+    _ordered_fold(gs.views, 1.0, False, out, tide.TIDE_ORDER_TREE, 0, fill_ranks=fill_ranks)
+    got = out.cpu().numpy()
+    if want is None:
+        ref = np.zeros((world, S), np.float32)
+        oracle.rs_ex(world, dims, _host_grads(gs.views, False), 1.0, False, ref, "tree", 0)
+        assert_same_f32(got, ref, "tree W=12 vs oracle")
+        return
+    for p, (d, k) in enumerate(dims):
+        flat = np.concatenate([got[r, o[p]:o[p] + R[p] * k] for r in range(world)])[:d * k]
+        assert_same_f32(flat, np.full(d * k, want, np.float32), f"tree probe W={world} p={p}")
 
 
 def test_bulk_wait_timeout_reports_status():
@@ -335,7 +374,8 @@ def test_maximum_and_odd_worlds(world):
     _, _, S = oracle.geometry(world, dims)
     host = _host_grads(gs.views, False)
     for kw, oname in (({"kernel": tide.TIDE_KERNEL_DIRECT}, "rank"), ({"kernel": tide.TIDE_KERNEL_BULK}, "rank"),
-                      ({"kernel": tide.TIDE_KERNEL_BULK, "order": tide.TIDE_ORDER_STAGED_OWN}, "staged")):
+                      ({"kernel": tide.TIDE_KERNEL_BULK, "order": tide.TIDE_ORDER_STAGED_OWN}, "staged"),
+                      ({"kernel": tide.TIDE_KERNEL_BULK, "order": tide.TIDE_ORDER_TREE}, "tree")):
         out = torch.zeros(world, S, device="cuda")
         with tide.Plan(gs.views, tide.make_flags(**kw)) as plan:
             plan.rs_fold(out, alpha=1.0 / world)
@@ -591,14 +631,15 @@ def test_full_size_sampled(index):
 
 @pytest.mark.parametrize("index", [2, 5])
 def test_full_size_orders_and_fp32(index):
-    """Full-size groups: the Section 4.3 orders and fp32 gradients, sampled
-    windows recomputed by the oracle in the same order."""
+    """Full-size groups: the Section 4.3 orders, the tree order and fp32
+    gradients, sampled windows recomputed by the oracle in the same order."""
     w = workloads.get(index)
     dims = w.dim0_rownumel()
     gs = workloads.make_grads(w, device="cuda")
     _, _, S = oracle.geometry(w.world, dims)
     L = w.world // 2
-    for order, oname, ns in ((tide.TIDE_ORDER_STAGED_OWN, "staged", 0), (tide.TIDE_ORDER_NODES, "nodes", L)):
+    for order, oname, ns in ((tide.TIDE_ORDER_STAGED_OWN, "staged", 0), (tide.TIDE_ORDER_NODES, "nodes", L),
+                             (tide.TIDE_ORDER_TREE, "tree", 0)):
         out = torch.empty(w.world, S, device="cuda")
         with tide.Plan(gs.views, tide.make_flags(order=order, node_size=ns)) as plan:
             plan.rs_fold(out, alpha=w.alpha)
