@@ -319,6 +319,90 @@ def cpu_oracle_sample(w, host_grads=None, min_seconds=10.0, max_reps=50):
                       f"({numel} elements per gradient set), reduce-scatter + placement, {reps} reps in {el:.1f} s"}
 
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model"):
+        for line in info.splitlines():
+            if line.startswith(key):
+                return line.split(":", 1)[1].strip()
+    impl = [ln.split(":", 1)[1].strip() for ln in info.splitlines() if ln.startswith("CPU implementer")]
+    part = [ln.split(":", 1)[1].strip() for ln in info.splitlines() if ln.startswith("CPU part")]
+    if not (impl and part):
+        return "unknown"
+    arm_parts = {"0xd0c": "Neoverse-N1", "0xd40": "Neoverse-V1", "0xd49": "Neoverse-N2", "0xd4f": "Neoverse-V2"}
+    name = arm_parts.get(part[0].lower(), "") if impl[0].lower() == "0x41" else ""
+    return f"{name} (implementer {impl[0]} part {part[0]})" if name else f"implementer {impl[0]} part {part[0]}"
+
+
+def cpu_oracle_all_cores(w, host_grads, min_seconds=5.0, max_reps=50, names=SAMPLE_PARAMS):
+    """The same oracle sample on every core this process may use: the
+    unchanged oracle functions run on independent windows (slices of one
+    (parameter, rank) piece, at most 2^20 elements) and per-parameter
+    placements in a thread pool; ctypes releases the GIL inside each call."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    import oracle
+    idx = [w.names.index(n) for n in names if n in w.names]
+    dims_all = w.dim0_rownumel()
+    dims = [dims_all[i] for i in idx]
+    orc = oracle.load()
+    W = w.world
+    R, o, S = orc.geometry(W, dims)
+    out = np.zeros((W, S), np.float32)
+    slots = np.random.default_rng(0).integers(0, 0x3F00, size=(W, S), dtype=np.uint16)
+    slot_parts = [np.ascontiguousarray(slots[:, o[p]:o[p] + R[p] * k]) for p, (_, k) in enumerate(dims)]
+    jobs = []
+    for p, (d, k) in enumerate(dims):
+        for r in range(W):
+            v = orc.valid_rows(d, R[p], r) * k
+            base = r * R[p] * k
+            for a in range(0, R[p] * k, 1 << 20):
+                b = min(a + (1 << 20), R[p] * k)
+                nv, npad = max(0, min(b, v) - a), (b - a) - max(0, min(b, v) - a)
+                srcs = [host_grads[p][u][base + a:base + a + nv] for u in range(W)]
+                jobs.append((srcs, nv, npad, r, o[p] + a))
+
+    def rs_job(j, dst):
+        srcs, nv, npad, r, pos = j
+        old = dst[r, pos:pos + nv + npad] if w.accumulate else None
+        dst[r, pos:pos + nv + npad] = orc.rs_window(srcs, nv, npad, w.alpha, w.accumulate, old)
+
+    def ag_job(p):
+        orc.ag(W, [dims[p]], slot_parts[p])
+
+    threads = len(os.sched_getaffinity(0))
+    numel = sum(d * k for d, k in dims)
+    rs_b, ag_b = alg_bytes(w, numel)
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        # the windows must reassemble the single-threaded oracle's result exactly
+        chk, want = np.zeros((W, S), np.float32), np.zeros((W, S), np.float32)
+        list(pool.map(lambda j: rs_job(j, chk), jobs))
+        orc.rs(W, dims, host_grads, w.alpha, w.accumulate, want)
+        if not np.array_equal(chk.view(np.uint32), want.view(np.uint32)):
+            raise AssertionError("parallel oracle windows differ from the single-threaded oracle")
+        del chk, want
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            list(pool.map(lambda j: rs_job(j, out), jobs))
+            list(pool.map(ag_job, range(len(dims))))
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= min_seconds or reps >= max_reps:
+                break
+    return {"value": round((rs_b + ag_b) * reps / el / 1e9, 4), "unit": UNIT, "cores": threads,
+            "cpu": cpu_model(), "matches_single_thread": True,
+            "sample": f"same sample, {len(jobs)} reduce-scatter windows + {len(dims)} "
+                      f"placements per rep over {threads} threads, {reps} reps in {el:.1f} s"}
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     import workloads
@@ -509,6 +593,8 @@ def run_ours(args):
             host.append([gs.views[u][i].reshape(-1).view(torch.int16).cpu().numpy().view(np.uint16)
                          for u in range(w.world)])
         result["cpu_baseline"] = cpu_oracle_sample(w, host)
+        result["cpu_baseline"]["cpu"] = cpu_model()
+        result["cpu_baseline"]["all_cores"] = cpu_oracle_all_cores(w, host)
 
     plan.close()
     if rank == 0:

@@ -1,0 +1,29 @@
+"""Host legs of bench.py that need no GPU: the all-cores run of the oracle
+(independent windows in a thread pool) reassembles the single-threaded
+oracle's reduce-scatter bit for bit, with and without accumulation and on
+ragged shapes whose pieces end in padding."""
+import os
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_cpu_oracle_all_cores_matches_single_thread(accumulate):
+    import bench
+    shapes = [(5497, 1000), (333, 17), (7, 5), (3000,)]  # the first: pieces of more than one 2^20 window
+    w = workloads.custom(5, shapes, index=41, alpha=0.5, accumulate=accumulate)
+    names = ("t0", "t1", "t2", "t3")
+    host = [[workloads.normal_fp32(w.numels()[p], workloads.grad_seed(w, u, p), w.sigma)
+             .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16) for u in range(w.world)]
+            for p in range(len(shapes))]
+    rec = bench.cpu_oracle_all_cores(w, host, min_seconds=0.0, max_reps=1, names=names)
+    assert rec["matches_single_thread"] and rec["cores"] >= 1 and rec["value"] > 0
+    assert "windows" in rec["sample"]
