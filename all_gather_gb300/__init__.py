@@ -27,7 +27,7 @@ from ._binding import (  # noqa: F401  (re-exported C-ABI names)
     tide_last_error, tide_launch_count, tide_plan_build, tide_plan_destroy, tide_plan_fold_config,
     tide_plan_num_segments, tide_plan_rebind, tide_plan_segment, tide_plan_slot_numel, tide_rs_fold,
     tide_rs_fold_noalloc, tide_status_string, tide_latin_square_gpu, tide_rs_wave_plan, tide_rs_wave_zero_mask,
-    tide_bruck_schedule, tide_sm_probe, tide_sm_probe_max_clusters)
+    tide_bruck_schedule, tide_sm_probe, tide_sm_probe_max_clusters, pointer_array)
 
 AG_MODES = {"sm": TIDE_AG_SM, "ce2d": TIDE_AG_CE_2D, "ce1d": TIDE_AG_CE_1D}
 
@@ -72,6 +72,23 @@ def _param_descs(grads, offsets=None, require_cuda=True, dtype=None):
     return descs
 
 
+class FullParams:
+    """The P full parameter tensors of a group, checked once and kept as the
+    pointer array the placements take (the paper registers the group's
+    tables once instead of building them per call, Section 6).  Holds
+    references to the tensors, so the pointers stay valid while it lives."""
+
+    def __init__(self, full: Sequence, shapes: Sequence[tuple]):
+        import torch
+        if len(full) != len(shapes):
+            raise ValueError(f"{len(full)} full tensors for {len(shapes)} parameters")
+        for p, f in enumerate(full):
+            if f.dtype != torch.bfloat16 or not f.is_contiguous() or tuple(f.shape) != shapes[p]:
+                raise ValueError(f"full[{p}] must be a contiguous bfloat16 tensor of shape {shapes[p]}")
+        self.tensors = list(full)
+        self.ptrs = pointer_array([f.data_ptr() for f in full])
+
+
 class Plan:
     """A built plan for one parameter group (owns the plan's device tables).
 
@@ -105,28 +122,35 @@ class Plan:
                      int(bool(accumulate)), _stream_handle(stream))
         return out
 
-    def ag_place(self, slots, full: List, mode: str = "sm", stream=None):
-        """slots: bf16 CUDA tensor [W, stride]; full[p]: contiguous bf16 tensor of parameter p's shape."""
+    def bind_full(self, full: Sequence) -> FullParams:
+        """Check the full parameter tensors once; pass the result to the
+        placements instead of the list to skip the per-call checks."""
+        return FullParams(full, self.shapes)
+
+    def _full_ptrs(self, full):
+        if isinstance(full, FullParams):
+            if len(full.tensors) != len(self.shapes):
+                raise ValueError("bound full tensors belong to another group")
+            return full.ptrs
+        return FullParams(full, self.shapes).ptrs
+
+    def ag_place(self, slots, full, mode: str = "sm", stream=None):
+        """slots: bf16 CUDA tensor [W, stride]; full: a list whose entry p is a
+        contiguous bf16 tensor of parameter p's shape, or bind_full(list)."""
         import torch
         if slots.dtype != torch.bfloat16 or slots.dim() != 2 or slots.shape[0] != self.world or slots.stride(1) != 1:
             raise ValueError("slots must be bfloat16 [W, stride] with unit inner stride")
-        for p, f in enumerate(full):
-            if f.dtype != torch.bfloat16 or not f.is_contiguous() or tuple(f.shape) != self.shapes[p]:
-                raise ValueError(f"full[{p}] must be a contiguous bfloat16 tensor of shape {self.shapes[p]}")
         tide_ag_place(self.handle, slots.data_ptr(), slots.stride(0) if self.world > 1 else slots.shape[1],
-                      [f.data_ptr() for f in full], AG_MODES[mode], _stream_handle(stream))
+                      self._full_ptrs(full), AG_MODES[mode], _stream_handle(stream))
         return full
 
-    def ag_place_f32(self, slots, full: List, stream=None):
-        """Mixed-precision placement: slots fp32 CUDA tensor [W, stride]; full[p] bf16 of parameter p's shape."""
+    def ag_place_f32(self, slots, full, stream=None):
+        """Mixed-precision placement: slots fp32 CUDA tensor [W, stride]; full as for ag_place."""
         import torch
         if slots.dtype != torch.float32 or slots.dim() != 2 or slots.shape[0] != self.world or slots.stride(1) != 1:
             raise ValueError("slots must be float32 [W, stride] with unit inner stride")
-        for p, f in enumerate(full):
-            if f.dtype != torch.bfloat16 or not f.is_contiguous() or tuple(f.shape) != self.shapes[p]:
-                raise ValueError(f"full[{p}] must be a contiguous bfloat16 tensor of shape {self.shapes[p]}")
         tide_ag_place_f32(self.handle, slots.data_ptr(), slots.stride(0) if self.world > 1 else slots.shape[1],
-                          [f.data_ptr() for f in full], _stream_handle(stream))
+                          self._full_ptrs(full), _stream_handle(stream))
         return full
 
     def fold_config(self) -> dict:

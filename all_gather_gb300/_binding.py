@@ -186,17 +186,27 @@ def tide_rs_fold(plan: int, out_base: int, out_slot_stride: int, alpha: float, a
            "tide_rs_fold")
 
 
-def tide_ag_place(plan: int, slots_base: int, slot_stride: int, full: Sequence[int], mode: int,
-                  stream: int = 0) -> None:
-    arr = (ctypes.c_void_p * max(len(full), 1))(*[ctypes.c_void_p(int(x) or None) for x in full])
+def pointer_array(ptrs: Sequence[int]):
+    """A C array of device pointers (void *const *) for the placements; build
+    it once and pass it again to skip the per-call conversion."""
+    return (ctypes.c_void_p * max(len(ptrs), 1))(*[int(x) or None for x in ptrs])
+
+
+def _as_pointer_array(full):
+    return full if isinstance(full, ctypes.Array) else pointer_array(full)
+
+
+def tide_ag_place(plan: int, slots_base: int, slot_stride: int, full, mode: int, stream: int = 0) -> None:
+    """full: device pointers of the P full tensors (a sequence, or pointer_array(...))."""
     _check(load_library().tide_ag_place(ctypes.c_void_p(plan), ctypes.c_void_p(slots_base or None), slot_stride,
-                                        arr, mode, ctypes.c_void_p(stream or None)), "tide_ag_place")
+                                        _as_pointer_array(full), mode, ctypes.c_void_p(stream or None)),
+           "tide_ag_place")
 
 
-def tide_ag_place_f32(plan: int, slots_base: int, slot_stride: int, full: Sequence[int], stream: int = 0) -> None:
-    arr = (ctypes.c_void_p * max(len(full), 1))(*[ctypes.c_void_p(int(x) or None) for x in full])
+def tide_ag_place_f32(plan: int, slots_base: int, slot_stride: int, full, stream: int = 0) -> None:
     _check(load_library().tide_ag_place_f32(ctypes.c_void_p(plan), ctypes.c_void_p(slots_base or None), slot_stride,
-                                            arr, ctypes.c_void_p(stream or None)), "tide_ag_place_f32")
+                                            _as_pointer_array(full), ctypes.c_void_p(stream or None)),
+           "tide_ag_place_f32")
 
 
 def tide_plan_destroy(plan: int) -> None:

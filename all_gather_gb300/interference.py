@@ -111,8 +111,9 @@ def measure(workload: str = "llama3.1_8b_block", budgets=(0, 64, 16), n_rs: int 
         slots = workloads.make_slots(w, S, device=dev)
         full = [torch.empty(s_, dtype=torch.bfloat16, device=dev) for s_ in w.shapes]
         pl = next(iter(plans.values()))
-        arms["placement_sm_kernel"] = lambda: pl.ag_place(slots, full, mode="sm")
-        arms["placement_copy_engines"] = lambda: pl.ag_place(slots, full, mode="ce2d")
+        full_b = pl.bind_full(full)
+        arms["placement_sm_kernel"] = lambda: pl.ag_place(slots, full_b, mode="sm")
+        arms["placement_copy_engines"] = lambda: pl.ag_place(slots, full_b, mode="ce2d")
 
     quiet = torch.cuda.Stream()
     rs_alone = {name: _time_alone(fn, 10, quiet) for name, fn in arms.items()}

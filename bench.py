@@ -484,11 +484,12 @@ def run_ours(args):
     out = workloads.make_out_init(w, S, device=dev) if w.accumulate else torch.zeros(w.world, S, device=dev)
     slots = workloads.make_slots(w, S, device=dev)
     full = [torch.empty(s, dtype=torch.bfloat16, device=dev) for s in w.shapes]
+    full_b = plan.bind_full(full)  # checked once, as a training loop would
     stream = torch.cuda.current_stream()
 
     def step():
         plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
-        plan.ag_place(slots, full, mode=args.ag_mode)
+        plan.ag_place(slots, full_b, mode=args.ag_mode)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -511,7 +512,7 @@ def run_ours(args):
         ev[i][0].record(stream)
         plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
         ev[i][1].record(stream)
-        plan.ag_place(slots, full, mode=args.ag_mode)
+        plan.ag_place(slots, full_b, mode=args.ag_mode)
         ev[i][2].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
@@ -566,6 +567,13 @@ def run_ours(args):
     # the other placement engines and the mixed-precision placement, timed alone after the step
     if rank == 0 and not args.no_variants:
         result["variants"] = time_variants(plan, w, S, slots, full, dev, gs.views, steps=min(K, 20))
+    if rank == 0:
+        result["host_issue_us"] = host_issue_us({
+            "tide_rs_fold": lambda: plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate),
+            "tide_ag_place sm": lambda: plan.ag_place(slots, full_b, mode="sm"),
+            "tide_ag_place sm, full tensors checked per call": lambda: plan.ag_place(slots, full, mode="sm"),
+            "tide_ag_place ce2d": lambda: plan.ag_place(slots, full_b, mode="ce2d"),
+            "tide_ag_place ce1d": lambda: plan.ag_place(slots, full_b, mode="ce1d")})
 
     # two-pass stock-FSDP2-style baseline (chunk_cat pack to fp32, then reduce), timed alone
     if not args.no_baseline and rank == 0:
@@ -604,6 +612,27 @@ def run_ours(args):
     return 0
 
 
+def host_issue_us(calls: dict, reps: int = 30) -> dict:
+    """Host time to enqueue each call (from the Python call to its return,
+    ctypes marshalling included; the device is idle before every call, so no
+    call waits for queue space): median and p90 in microseconds."""
+    import torch
+    res = {}
+    for name, fn in calls.items():
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            ts.append((time.perf_counter() - t0) * 1e6)
+        torch.cuda.synchronize()
+        ts.sort()
+        res[name] = {"p50": round(ts[len(ts) // 2], 1), "p90": round(ts[int(0.9 * (len(ts) - 1))], 1)}
+    return res
+
+
 def time_variants(plan, w, S, slots, full, dev, gs_views, steps: int = 20) -> dict:
     """Mean event time of each placement and fold variant over `steps` launches."""
     import torch
@@ -613,10 +642,12 @@ def time_variants(plan, w, S, slots, full, dev, gs_views, steps: int = 20) -> di
     N = w.total_numel()
     slots32 = torch.stack([workloads.normal_fp32(S, workloads.slot_seed(w, r), 0.02, dev) for r in range(w.world)])
     stream = torch.cuda.current_stream()
+    full_b = plan.bind_full(full)
     calls = {
-        "ag_place_f32 (fp32 master shards -> bf16, fused cast)": (lambda: plan.ag_place_f32(slots32, full), 6 * N),
-        "ag_place ce2d (copy engines, one 2D copy per parameter)": (lambda: plan.ag_place(slots, full, "ce2d"), 4 * N),
-        "ag_place ce1d (copy engines, one copy per piece)": (lambda: plan.ag_place(slots, full, "ce1d"), 4 * N),
+        "ag_place_f32 (fp32 master shards -> bf16, fused cast)": (lambda: plan.ag_place_f32(slots32, full_b), 6 * N),
+        "ag_place ce2d (copy engines, one 2D copy per parameter)": (lambda: plan.ag_place(slots, full_b, "ce2d"),
+                                                                    4 * N),
+        "ag_place ce1d (copy engines, one copy per piece)": (lambda: plan.ag_place(slots, full_b, "ce1d"), 4 * N),
     }
     # the fold in the other Section 4.3 orders, the tree order, and with fp32 gradients
     out_v = torch.zeros(w.world, S, device=dev)
@@ -681,6 +712,7 @@ def e2e(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world):
     plan2 = tide.Plan(gs2.views)
     sets.append((gs2.arenas, gs2.views, plan2, torch.empty_like(out), torch.empty_like(slots),
                  [torch.empty_like(f) for f in full]))
+    bound = [s_[2].bind_full(s_[5]) for s_ in sets]
     h2d = sum(a.numel() * a.element_size() for a in h_arenas) + h_slots.numel() * 2
     h2d += h_out0.numel() * 4 if w.accumulate else 0
     d2h = h_out0.numel() * 4 + sum(f.numel() * 2 for f in full)
@@ -704,7 +736,7 @@ def e2e(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world):
             if w.accumulate:
                 o.copy_(h_out0, non_blocking=True)
             pl.rs_fold(o, alpha=w.alpha, accumulate=w.accumulate, stream=s_comp)
-            pl.ag_place(sl, fu, mode=args.ag_mode, stream=s_comp)
+            pl.ag_place(sl, bound[b], mode=args.ag_mode, stream=s_comp)
             ev["comp"][b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev["comp"][b])

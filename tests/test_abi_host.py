@@ -260,6 +260,24 @@ def test_rebind_checks_geometry(tide):
         tide.tide_plan_destroy(plan)
 
 
+def test_bound_full_tensors_are_checked_once(tide):
+    """bind_full checks the full tensors' dtype, contiguity and shapes once and
+    keeps their pointers; a mismatched list is refused before any call."""
+    import torch
+    shapes = [(8, 3), (5,)]
+    plan = tide.Plan([[torch.zeros(s_, dtype=torch.bfloat16) for s_ in shapes] for _ in range(2)], host_only=True)
+    try:
+        full = [torch.empty(s_, dtype=torch.bfloat16) for s_ in shapes]
+        bound = plan.bind_full(full)
+        assert [bound.ptrs[i] for i in range(2)] == [f.data_ptr() for f in full]
+        for bad in ([full[0]], [full[0], torch.empty(6, dtype=torch.bfloat16)],
+                    [full[0].float(), full[1]], [torch.empty(3, 8, dtype=torch.bfloat16).t(), full[1]]):
+            with pytest.raises(ValueError):
+                plan.bind_full(bad)
+    finally:
+        plan.close()
+
+
 def test_launch_count_starts_at_zero_without_gpu(tide):
     import torch
     if torch.cuda.is_available():
