@@ -133,14 +133,38 @@ __global__ void __launch_bounds__(kAgThreads) ag_cast_kernel(const __grid_consta
 
 }  // namespace
 
+// Tuning knob (compile-time; default: leave the driver's choice): the
+// placements' preferred shared-memory carveout, in percent.  The fold runs
+// with two 98 KB rings per SM; a placement that asks for the same carveout
+// lets the SMs switch between the two kernels without reconfiguring.
+#ifndef TIDE_AG_CARVEOUT
+#define TIDE_AG_CARVEOUT -1
+#endif
+
+namespace {
+template <typename K>
+cudaError_t prefer_carveout(K kernel)
+{
+    if (TIDE_AG_CARVEOUT < 0)
+        return cudaSuccess;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, TIDE_AG_CARVEOUT);
+}
+}  // namespace
+
 cudaError_t launch_ag(const AgParams &ap, int grid, cudaStream_t stream)
 {
+    static const cudaError_t carve = prefer_carveout(ag_place_kernel);
+    if (carve != cudaSuccess)
+        return carve;
     ag_place_kernel<<<grid, kAgThreads, 0, stream>>>(ap);
     return cudaGetLastError();
 }
 
 cudaError_t launch_ag_f32(const AgParams &ap, int grid, cudaStream_t stream)
 {
+    static const cudaError_t carve = prefer_carveout(ag_cast_kernel);
+    if (carve != cudaSuccess)
+        return carve;
     ag_cast_kernel<<<grid, kAgThreads, 0, stream>>>(ap);
     return cudaGetLastError();
 }

@@ -534,6 +534,18 @@ def run_ours(args):
     def pct(xs, q):
         ys = sorted(xs)
         return round(ys[min(len(ys) - 1, int(q * len(ys)))], 4)
+
+    def thirds(xs):
+        """Medians of the first, middle and last third of the timed steps, the
+        median of those, and their spread (max - min) relative to it: drift or
+        a co-tenant on the shared GPU shows up here."""
+        n = len(xs) // 3
+        if n < 1:
+            return None
+        meds = [pct(xs[i * n:(i + 1) * n], 0.5) for i in range(3)]
+        mid = sorted(meds)[1]
+        return {"medians_ms": meds, "median_of_medians_ms": mid,
+                "spread_pct": round(100.0 * (max(meds) - min(meds)) / mid, 2) if mid > 0 else None}
     peak, peak_kind = measured_peak_gbs()
     achieved = rs_b / (rs_mean * 1e-3) / 1e9
     clk = clocks.summary(t_wall0, t_wall1)
@@ -548,10 +560,11 @@ def run_ours(args):
                    "chunk_elems": cfg["chunk_elems"], "l2": "inputs larger than L2 (no flush)",
                    "step": "tide_rs_fold + tide_ag_place", "parallelism": f"weak: {world} independent replicas"},
         "parts": {"rs_fold": {"ms": round(rs_mean, 4), "gbs": round(achieved, 1), "alg_bytes": rs_b,
-                              "p10_ms": pct(rs_ms, 0.1), "p50_ms": pct(rs_ms, 0.5), "p90_ms": pct(rs_ms, 0.9)},
+                              "p10_ms": pct(rs_ms, 0.1), "p50_ms": pct(rs_ms, 0.5), "p90_ms": pct(rs_ms, 0.9),
+                              "thirds": thirds(rs_ms)},
                   "ag_place": {"ms": round(ag_mean, 4), "gbs": round(ag_b / (ag_mean * 1e-3) / 1e9, 1),
                                "alg_bytes": ag_b, "p10_ms": pct(ag_ms, 0.1), "p50_ms": pct(ag_ms, 0.5),
-                               "p90_ms": pct(ag_ms, 0.9)}},
+                               "p90_ms": pct(ag_ms, 0.9), "thirds": thirds(ag_ms)}},
         "device": {"name": torch.cuda.get_device_name(dev),
                    "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
