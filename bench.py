@@ -680,6 +680,20 @@ def time_variants(plan, w, S, slots, full, dev, gs_views, steps: int = 20) -> di
     calls["rs_fold fp32 gradients (b_grad = 4)"] = (
         lambda: plan32.rs_fold(out_v, alpha=w.alpha, accumulate=w.accumulate),
         w.world * N * 4 + N * 4 + (N * 4 if w.accumulate else 0))
+    # the copy-engine placement captured once and replayed from a CUDA graph:
+    # no per-step host issue of the copy list
+    graphs = {}
+    for mode in ("ce2d", "ce1d"):
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):
+            plan.ag_place(slots, full_b, mode)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            plan.ag_place(slots, full_b, mode)
+        graphs[mode] = g
+    calls["ag_place ce2d from a CUDA graph (replay)"] = (graphs["ce2d"].replay, 4 * N)
+    calls["ag_place ce1d from a CUDA graph (replay)"] = (graphs["ce1d"].replay, 4 * N)
     res = {}
     for name, (fn, nbytes) in calls.items():
         for _ in range(3):
@@ -693,6 +707,7 @@ def time_variants(plan, w, S, slots, full, dev, gs_views, steps: int = 20) -> di
         torch.cuda.synchronize()
         ms = s.elapsed_time(e) / steps
         res[name] = {"ms": round(ms, 4), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "alg_bytes": nbytes}
+    del graphs
     for pl in list(plans.values()) + [plan32]:
         pl.close()
     del slots32, grads32, out_v

@@ -33,10 +33,13 @@
  *   - Streams are cudaStream_t values passed as void*; NULL is the legacy
  *     default stream.  Hot calls are asynchronous and stream-ordered; a plan
  *     must not be used on two streams at once without caller synchronisation.
- *     tide_rs_fold, tide_ag_place (SM mode) and tide_ag_place_f32 may be
- *     captured into a CUDA graph; the graph then reads the plan's tables, so
- *     the plan must outlive every replay (tide_plan_destroy of a plan that was
- *     captured synchronises the device before freeing).
+ *     tide_rs_fold, tide_ag_place (every mode) and tide_ag_place_f32 may be
+ *     captured into a CUDA graph; in the copy-engine modes the capture takes
+ *     in the plan's internal streams (forked from and joined back to the
+ *     capturing stream), and a replay issues the whole copy list at once.
+ *     The graph reads the plan's tables, so the plan must outlive every
+ *     replay (tide_plan_destroy of a plan that was captured synchronises the
+ *     device before freeing).
  *   - Errors are returned as tide_status_t, never thrown; on failure nothing
  *     was enqueued.  tide_last_error() gives a human-readable detail for the
  *     last failing call on the calling thread.

@@ -590,6 +590,55 @@ def test_graph_captured_step():
         del graph
 
 
+@pytest.mark.parametrize("mode", ["ce2d", "ce1d"])
+@pytest.mark.parametrize("index", [1, 5])
+def test_graph_captured_copy_engine_placement(mode, index):
+    """The copy-engine placement (copies spread over the plan's internal
+    streams, forked from and joined back to the caller's stream) captured once
+    in a CUDA graph and replayed on new slot contents: the replay places every
+    shard as the oracle does.  The MoE layer (389 parameters) is its largest
+    copy list."""
+    w = workloads.get(index)
+    dims = w.dim0_rownumel()
+    g = workloads.make_grads(w, device="cuda")
+    _, _, S = oracle.geometry(w.world, dims)
+    slots = workloads.make_slots(w, S, device="cuda")
+    full = [torch.empty(s_, dtype=torch.bfloat16, device="cuda") for s_ in w.shapes]
+    stream = torch.cuda.Stream()
+    with tide.Plan(g.views) as plan:
+        bound = plan.bind_full(full)
+        with torch.cuda.stream(stream):
+            plan.ag_place(slots, bound, mode=mode)  # warm-up outside the capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            plan.ag_place(slots, bound, mode=mode)
+        for step in range(3):
+            slots.copy_(slots.roll(step + 1, dims=0))
+            for f in full:
+                f.fill_(float("nan"))
+            graph.replay()
+            torch.cuda.synchronize()
+            host_slots = slots.cpu()
+            if index == 1:
+                want = ag_expected(w.world, dims, slots)
+                for p in range(len(dims)):
+                    assert_same_u16(bits16(full[p]), want[p], f"replayed {mode} placement p={p}")
+            else:  # every parameter, sampled rows: full row i of rank r is slot r at o_p + i K
+                R, o, _ = oracle.geometry(w.world, dims)
+                rnd = random.Random(step)
+                for p in rnd.sample(range(len(dims)), 40):
+                    d, k = dims[p]
+                    for row in rnd.sample(range(d), min(d, 8)):
+                        r, i = divmod(row, R[p])
+                        got = full[p].reshape(-1)[row * k:(row + 1) * k].cpu()
+                        ref = host_slots[r, o[p] + i * k:o[p] + (i + 1) * k]
+                        assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), (mode, p, row)
+        del graph
+    del g
+    torch.cuda.empty_cache()
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads in the benchmark's launch configuration
 @pytest.mark.parametrize("index", [2, 3, 4, 5])
