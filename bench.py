@@ -98,6 +98,66 @@ def alg_bytes(w, numel: int):
     return rs, ag
 
 
+def nvml_device(cuda_index: int):
+    """(NVML library, device handle) of the CUDA device, matched by UUID
+    (read-only use: nothing is set through it)."""
+    import ctypes
+    lib = ctypes.CDLL("libnvidia-ml.so.1")
+    if lib.nvmlInit_v2() != 0:
+        raise OSError("nvmlInit failed")
+    count = ctypes.c_uint(0)
+    lib.nvmlDeviceGetCount_v2(ctypes.byref(count))
+    want = ""
+    try:
+        import torch
+        want = str(torch.cuda.get_device_properties(cuda_index).uuid).lower().replace("gpu-", "")
+    except Exception:
+        pass
+    for i in range(count.value):
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(i, ctypes.byref(h)) != 0:
+            continue
+        buf = ctypes.create_string_buffer(96)
+        lib.nvmlDeviceGetUUID(h, buf, 96)
+        if want and want in buf.value.decode().lower():
+            return lib, h
+    h = ctypes.c_void_p()
+    if lib.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(h)) != 0:
+        raise OSError("no NVML handle")
+    return lib, h
+
+
+def gpu_local_cpus(cuda_index: int):
+    """The CPUs NVML names as closest to the GPU (its NUMA-local cores), or
+    None when NVML cannot tell."""
+    import ctypes
+    import os
+    try:
+        lib, h = nvml_device(cuda_index)
+        words = (os.cpu_count() or 64) // 64 + 1
+        mask = (ctypes.c_ulong * words)()
+        if lib.nvmlDeviceGetCpuAffinity(h, words, mask) != 0:
+            return None
+    except (OSError, AttributeError):
+        return None
+    bits = ctypes.sizeof(ctypes.c_ulong) * 8
+    cpus = {w * bits + b for w in range(words) for b in range(bits) if (mask[w] >> b) & 1}
+    return cpus or None
+
+
+def cpu_ranges(cpus) -> str:
+    """Compact text of a CPU set: 0-71,144-215."""
+    out, xs = [], sorted(cpus)
+    i = 0
+    while i < len(xs):
+        j = i
+        while j + 1 < len(xs) and xs[j + 1] == xs[j] + 1:
+            j += 1
+        out.append(f"{xs[i]}-{xs[j]}" if j > i else f"{xs[i]}")
+        i = j + 1
+    return ",".join(out)
+
+
 class ClockSampler:
     """SM clock, max clock, power and clock-event (throttle) reasons sampled
     every ~2 ms while the timed region runs.  Reads NVML through ctypes (read
@@ -115,33 +175,7 @@ class ClockSampler:
         self._smi = None
 
     def _nvml(self):
-        import ctypes
-        lib = ctypes.CDLL("libnvidia-ml.so.1")
-        if lib.nvmlInit_v2() != 0:
-            raise OSError("nvmlInit failed")
-        count = ctypes.c_uint(0)
-        lib.nvmlDeviceGetCount_v2(ctypes.byref(count))
-        handle = ctypes.c_void_p()
-        want = ""
-        try:
-            import torch
-            want = str(torch.cuda.get_device_properties(self.cuda_index).uuid).lower().replace("gpu-", "")
-        except Exception:
-            pass
-        chosen = None
-        for i in range(count.value):
-            h = ctypes.c_void_p()
-            if lib.nvmlDeviceGetHandleByIndex_v2(i, ctypes.byref(h)) != 0:
-                continue
-            buf = ctypes.create_string_buffer(96)
-            lib.nvmlDeviceGetUUID(h, buf, 96)
-            if want and want in buf.value.decode().lower():
-                chosen = h
-                break
-        if chosen is None:
-            if lib.nvmlDeviceGetHandleByIndex_v2(self.cuda_index, ctypes.byref(handle)) != 0:
-                raise OSError("no NVML handle")
-            chosen = handle
+        lib, chosen = nvml_device(self.cuda_index)
         reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
             lib.nvmlDeviceGetCurrentClocksThrottleReasons
         return lib, chosen, reasons_fn
@@ -599,8 +633,8 @@ def run_ours(args):
     if not args.no_interference and rank == 0:
         from all_gather_gb300 import interference
         result["interference"] = interference.summarize(
-            interference.measure(w.name, budgets=(0, 64, 16), n_rs=20, device=local, grads=gs))
-        result["interference"]["sm_probe"] = interference.sm_probe(w.name, budgets=(0, 152, 64, 16), windows=20,
+            interference.measure(w.name, budgets=(0, 128, 64, 32, 16, 8), n_rs=20, device=local, grads=gs))
+        result["interference"]["sm_probe"] = interference.sm_probe(w.name, budgets=(0, 152, 64, 32, 16, 8), windows=20,
                                                                    device=local, grads=gs)
 
     # end to end through the public API: pinned host inputs -> device -> fold + place -> host
@@ -725,8 +759,29 @@ def e2e(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world):
     import torch
     import torch.distributed as dist
 
+    import os
+
     import all_gather_gb300 as tide
     import workloads
+    # Host buffers on the GPU's own NUMA node: pinned pages are placed where
+    # the allocating thread runs, and a GB300 tray has two Grace CPUs, each
+    # attached to its own GPUs; buffers on the far one cross the CPU-to-CPU
+    # link on every copy.
+    saved = os.sched_getaffinity(0)
+    local = gpu_local_cpus(torch.device(dev).index or 0)
+    use = (local & saved) if local else None
+    if use:
+        os.sched_setaffinity(0, use)
+    try:
+        res = _e2e_run(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world, torch, dist, tide, workloads)
+    finally:
+        os.sched_setaffinity(0, saved)
+    res["host_cpus"] = {"gpu_local": cpu_ranges(local) if local else None,
+                        "used": cpu_ranges(use) if use else cpu_ranges(saved)}
+    return res
+
+
+def _e2e_run(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world, torch, dist, tide, workloads):
     K = max(2, args.e2e_steps)
     # pinned host inputs (one set: every step uploads the same bytes) and outputs (two sets)
     h_arenas = [a.cpu().pin_memory() for a in gs.arenas]

@@ -666,6 +666,15 @@ def test_full_size_sampled(index):
         want = ag_expected(w.world, dims, slots)
         for p, f in enumerate(full):
             assert_same_u16(bits16(f), want[p], f"{w.name} ag p={p}")
+        # the copy-engine placements, every element
+        bound = plan.bind_full(full)
+        for mode in ("ce2d", "ce1d"):
+            for f in full:
+                f.fill_(float("nan"))
+            plan.ag_place(slots, bound, mode=mode)
+            torch.cuda.synchronize()
+            for p, f in enumerate(full):
+                assert_same_u16(bits16(f), want[p], f"{w.name} ag {mode} p={p}")
         # mixed-precision placement from fp32 master shards, every element
         del slots
         slots32 = torch.stack([workloads.normal_fp32(S, workloads.slot_seed(w, r), 0.02, "cuda")
