@@ -228,7 +228,7 @@ def _host_grads(grads_uv, f32):
 
 @pytest.mark.parametrize("case", ORDER_CASES, ids=[c[0] for c in ORDER_CASES])
 @pytest.mark.parametrize("f32", [False, True], ids=["bf16", "fp32"])
-@pytest.mark.parametrize("world", [4, 6, 8, 32])
+@pytest.mark.parametrize("world", [1, 3, 4, 6, 8, 32])
 def test_orders_and_fp32_grads(case, f32, world):
     """Every Section 4.3 order and the tree order, bf16 and fp32 gradients:
     bit-exact against the oracle in the same order, and within 1e-6 (max-norm,
@@ -685,6 +685,51 @@ def test_full_size_sampled(index):
         for p, f in enumerate(full):
             assert_same_bf16(bits16(f), want[p], f"{w.name} ag_f32 p={p}")
     del gs
+    torch.cuda.empty_cache()
+
+
+def test_parameter_beyond_2g_elements():
+    """One parameter of 2,097,153 x 1,024 = 2^31 + 1,024 elements on 2 ranks
+    (about 26 GB with outputs): rank 1's rows start at element 1,073,742,848 and
+    end past 2^31, so every offset of the fold and the placements must be 64-bit.
+    Sampled windows (piece starts, ends, random rows) against the oracle, both
+    kernels and the tree order; the placements on sampled rows, every mode."""
+    world, shape = 2, (2_097_153, 1024)
+    w = workloads.custom(world, [shape, (5, 3)], index=77)
+    dims = w.dim0_rownumel()
+    gs = workloads.make_grads(w, device="cuda")
+    R, o, S = oracle.geometry(world, dims)
+    out = torch.empty(world, S, device="cuda")
+    for kw, oname in (({}, "rank"), ({"kernel": tide.TIDE_KERNEL_DIRECT}, "rank"),
+                      ({"order": tide.TIDE_ORDER_TREE}, "tree")):
+        out.fill_(float("nan"))
+        with tide.Plan(gs.views, tide.make_flags(**kw)) as plan:
+            plan.rs_fold(out, alpha=0.5)
+            torch.cuda.synchronize()
+            assert plan.device_status() == tide.TIDE_OK
+        n = sampled_rs_check(world, dims, gs.views, None, out, 0.5, False, seed=5, what=f"2G+ {kw}",
+                             order=oname)
+        assert n > 0
+    del out
+    torch.cuda.empty_cache()
+    slots = workloads.make_slots(w, S, device="cuda")
+    full = [torch.empty(s_, dtype=torch.bfloat16, device="cuda") for s_ in w.shapes]
+    with tide.Plan(gs.views) as plan:
+        bound = plan.bind_full(full)
+        for mode in ("sm", "ce2d", "ce1d"):
+            for f in full:
+                f.fill_(float("nan"))
+            plan.ag_place(slots, bound, mode=mode)
+            torch.cuda.synchronize()
+            rnd = random.Random(9)
+            d, k = dims[0]
+            rows = [0, R[0] - 1, R[0], d - 1] + rnd.sample(range(d), 12)
+            for row in rows:
+                r, i = divmod(row, R[0])
+                got = full[0].reshape(-1)[row * k:(row + 1) * k]
+                ref = slots[r, o[0] + i * k:o[0] + (i + 1) * k]
+                assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), (mode, row)
+    del gs, full, slots
     torch.cuda.empty_cache()
 
 
