@@ -340,6 +340,75 @@ def test_tree_order_probe(case, fill_ranks):
         assert_same_f32(flat, np.full(d * k, want, np.float32), f"tree probe W={world} p={p}")
 
 
+def _random_flags(rnd, world):
+    """A valid random flag set: orders other than rank order and fp32
+    gradients take the statically scheduled bulk kernel."""
+    order = rnd.choice([tide.TIDE_ORDER_RANK_ASC] * 3 + [tide.TIDE_ORDER_STAGED_OWN, tide.TIDE_ORDER_NODES,
+                                                         tide.TIDE_ORDER_TREE])
+    f32 = rnd.random() < 0.3
+    restricted = order != tide.TIDE_ORDER_RANK_ASC or f32
+    kernel = tide.TIDE_KERNEL_BULK if restricted else rnd.choice(
+        [tide.TIDE_KERNEL_AUTO, tide.TIDE_KERNEL_DIRECT, tide.TIDE_KERNEL_BULK])
+    sched = tide.TIDE_SCHED_DYNAMIC if kernel == tide.TIDE_KERNEL_DIRECT and rnd.random() < 0.5 else \
+        tide.TIDE_SCHED_STATIC
+    kw = dict(kernel=kernel, sched=sched, order=order,
+              grad_dtype=tide.TIDE_DTYPE_F32 if f32 else tide.TIDE_DTYPE_BF16,
+              cta_budget=rnd.choice([0, 0, 1, 3, rnd.randint(1, 400)]),
+              chunk_bytes=rnd.choice([0, 256, 256 * rnd.randint(1, 256)]),
+              fill_bytes=rnd.choice([0, 16, 16 * rnd.randint(1, 256)]),
+              fill_ranks=rnd.choice([0, 1, 2, rnd.randint(1, world + 2)]))
+    if order == tide.TIDE_ORDER_NODES:
+        kw["node_size"] = rnd.choice([d for d in range(1, world + 1) if world % d == 0])
+    oname = {tide.TIDE_ORDER_RANK_ASC: "rank", tide.TIDE_ORDER_STAGED_OWN: "staged",
+             tide.TIDE_ORDER_NODES: "nodes", tide.TIDE_ORDER_TREE: "tree"}[order]
+    return kw, oname, f32
+
+
+@pytest.mark.parametrize("seed", range(160))
+def test_random_flag_combinations(seed):
+    """Seeded random groups (1..40 ranks, ragged shapes, zero-size parameters)
+    under random valid flag sets and epilogues: the fold bit-exact against
+    the oracle in the same order, canary bands intact, and a random placement
+    mode bit-exact."""
+    rnd = random.Random(1000 + seed)
+    world = rnd.choice([1, 2, 3, 5, 7, 8, 12, 16, 31, 40])
+    shapes = []
+    for _ in range(rnd.randint(1, 6)):
+        d = rnd.choice([0, 1, world - 1 or 1, world, world + 1, rnd.randint(1, 9 * world + 5)])
+        shapes.append((d,) if rnd.random() < 0.2 else (d, rnd.choice([1, 2, 3, 8, 17, 64, 130])))
+    kw, oname, f32 = _random_flags(rnd, world)
+    w = workloads.custom(world, shapes, index=400 + seed)
+    gs = workloads.make_grads(w, device="cuda")
+    views = gs.views
+    if f32:
+        views = [[v.float() + 1e-6 * torch.randn_like(v.float()) for v in vs] for vs in views]
+    dims = w.dim0_rownumel()
+    _, _, S = oracle.geometry(world, dims)
+    alpha = rnd.choice([1.0, 0.5, -0.25, 1.0 / world, 3.0])
+    acc = rnd.random() < 0.4
+    init = torch.randn(world, S, device="cuda") if acc else None
+    buf, out = _guarded_out(world, S, rnd.choice([0, 1, 5, 64]), init)
+    before = out.clone()
+    flags = tide.make_flags(**kw)
+    with tide.Plan(views, flags) as plan:
+        plan.rs_fold(out, alpha=alpha, accumulate=acc)
+        torch.cuda.synchronize()
+        assert plan.device_status() == tide.TIDE_OK
+        want = before.cpu().numpy().copy()
+        oracle.rs_ex(world, dims, _host_grads(views, f32), alpha, acc, want, oname, kw.get("node_size", 0))
+        assert_same_f32(out.cpu().numpy()[:, :S], want[:, :S], f"seed {seed}: W={world} {kw} acc={acc}")
+        _check_canaries(buf, out, S)
+        # a placement in a random mode, from sentinel slots
+        mode = rnd.choice(["sm", "ce2d", "ce1d"])
+        slots = sentinel_slots(world, dims, S + rnd.choice([0, 3, 8]), seed=seed)
+        full = [torch.full(s_, float("nan"), dtype=torch.bfloat16, device="cuda") for s_ in w.shapes]
+        plan.ag_place(slots, full, mode=mode)
+        torch.cuda.synchronize()
+        wf = ag_expected(world, dims, slots)
+        for p, f in enumerate(full):
+            assert_same_u16(bits16(f), wf[p], f"seed {seed}: ag {mode} p={p}")
+
+
 def test_bulk_wait_timeout_reports_status():
     """A bounded device-side wait that expires is reported as TIMEOUT and the
     context stays usable: CTA 0 of the bulk kernel skips its first stage fill
