@@ -24,7 +24,8 @@ __device__ __forceinline__ uint4 ld_once_v4(const uint16_t *p)
 
 constexpr int kAgUnroll = 8;  // 16-byte vectors in flight per thread: enough to cover HBM latency
 
-__global__ void __launch_bounds__(kAgThreads) ag_place_kernel(const __grid_constant__ AgParams ap)
+template <int NP>
+__global__ void __launch_bounds__(kAgThreads) ag_place_kernel(const __grid_constant__ AgParamsT<NP> ap)
 {
     constexpr int NT = kAgThreads;
     const int tid = threadIdx.x;
@@ -83,7 +84,8 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float x)
 // Mixed-precision placement (fp32 master shards -> bf16 full tensors): the
 // same walk as ag_place_kernel, reading 32 bytes of fp32 and writing 16 bytes
 // of bf16 per vector when, after a common head, both sides are 16-byte aligned.
-__global__ void __launch_bounds__(kAgThreads) ag_cast_kernel(const __grid_constant__ AgParams ap)
+template <int NP>
+__global__ void __launch_bounds__(kAgThreads) ag_cast_kernel(const __grid_constant__ AgParamsT<NP> ap)
 {
     constexpr int NT = kAgThreads;
     constexpr int U = 4;  // 8-element vectors in flight per thread
@@ -149,23 +151,54 @@ cudaError_t prefer_carveout(K kernel)
         return cudaSuccess;
     return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, TIDE_AG_CARVEOUT);
 }
+
+AgParamsT<kAgParamsSmall> small_params(const AgParams &ap)
+{
+    AgParamsT<kAgParamsSmall> s;
+    s.segs = ap.segs;
+    s.items = ap.items;
+    s.item_begin = ap.item_begin;
+    s.item_end = ap.item_end;
+    s.slots = ap.slots;
+    s.slots_f32 = ap.slots_f32;
+    s.stride = ap.stride;
+    s.param_base = ap.param_base;
+    s.n_full = ap.n_full;
+    for (int i = 0; i < kAgParamsSmall; ++i)
+        s.full[i] = i < ap.n_full ? ap.full[i] : nullptr;
+    return s;
+}
 }  // namespace
 
 cudaError_t launch_ag(const AgParams &ap, int grid, cudaStream_t stream)
 {
-    static const cudaError_t carve = prefer_carveout(ag_place_kernel);
-    if (carve != cudaSuccess)
-        return carve;
-    ag_place_kernel<<<grid, kAgThreads, 0, stream>>>(ap);
+    if (ap.n_full <= kAgParamsSmall) {
+        static const cudaError_t carve = prefer_carveout(ag_place_kernel<kAgParamsSmall>);
+        if (carve != cudaSuccess)
+            return carve;
+        ag_place_kernel<kAgParamsSmall><<<grid, kAgThreads, 0, stream>>>(small_params(ap));
+    } else {
+        static const cudaError_t carve = prefer_carveout(ag_place_kernel<kAgParamsPerLaunch>);
+        if (carve != cudaSuccess)
+            return carve;
+        ag_place_kernel<kAgParamsPerLaunch><<<grid, kAgThreads, 0, stream>>>(ap);
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_ag_f32(const AgParams &ap, int grid, cudaStream_t stream)
 {
-    static const cudaError_t carve = prefer_carveout(ag_cast_kernel);
-    if (carve != cudaSuccess)
-        return carve;
-    ag_cast_kernel<<<grid, kAgThreads, 0, stream>>>(ap);
+    if (ap.n_full <= kAgParamsSmall) {
+        static const cudaError_t carve = prefer_carveout(ag_cast_kernel<kAgParamsSmall>);
+        if (carve != cudaSuccess)
+            return carve;
+        ag_cast_kernel<kAgParamsSmall><<<grid, kAgThreads, 0, stream>>>(small_params(ap));
+    } else {
+        static const cudaError_t carve = prefer_carveout(ag_cast_kernel<kAgParamsPerLaunch>);
+        if (carve != cudaSuccess)
+            return carve;
+        ag_cast_kernel<kAgParamsPerLaunch><<<grid, kAgThreads, 0, stream>>>(ap);
+    }
     return cudaGetLastError();
 }
 

@@ -102,7 +102,11 @@ BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_s
 // full fills.
 constexpr int kTreeLevels = 8;
 
-struct AgParams {
+// Placement kernel parameters, passed by value: NP destination pointers.
+// Launches for at most kAgParamsSmall parameters use the small form (a
+// 0.4 KB parameter block instead of 8 KB, which shortens every launch).
+template <int NP>
+struct AgParamsT {
     const Seg *segs;
     const Item *items;
     int64_t item_begin, item_end;  // this launch's item range
@@ -111,8 +115,10 @@ struct AgParams {
     int64_t stride;
     int32_t param_base;            // full[0] is parameter param_base
     int32_t n_full;
-    uint16_t *full[kAgParamsPerLaunch];
+    uint16_t *full[NP];
 };
+using AgParams = AgParamsT<kAgParamsPerLaunch>;
+constexpr int kAgParamsSmall = 32;
 
 // Launchers (rs_fold.cu / ag_place.cu).  Return cudaGetLastError() of the launch.
 cudaError_t launch_fold(const FoldParams &fp, int kernel, int accumulate, int grid, int block, size_t smem,
