@@ -7,8 +7,10 @@ the reduce-scatter window over the median duration of the victim alone,
 minus one.  Victims: a bf16 GEMM of 256 x 8192 x 8192 (the page's one-wave
 GEMM), a large 8192^3 bf16 GEMM, and a 256 MiB bf16 elementwise kernel.
 Arms: the fused fold at several CTA budgets, the two-pass stock-FSDP2
-baseline, and the all-gather placement on SMs and on the copy engines.  Set CUDA_DEVICE_MAX_CONNECTIONS=32 before CUDA starts (the page's
-setting) so the two streams get separate hardware queues.
+baseline, and the all-gather placement on SMs and on the copy engines (issued
+per call, or replayed from a CUDA graph).  Set CUDA_DEVICE_MAX_CONNECTIONS=32
+before CUDA starts (the page's setting) so the two streams get separate
+hardware queues.
 
     python -m all_gather_gb300.interference [--workload NAME] [--budgets 0,16,64]
 """
@@ -114,6 +116,15 @@ def measure(workload: str = "llama3.1_8b_block", budgets=(0, 64, 16), n_rs: int 
         full_b = pl.bind_full(full)
         arms["placement_sm_kernel"] = lambda: pl.ag_place(slots, full_b, mode="sm")
         arms["placement_copy_engines"] = lambda: pl.ag_place(slots, full_b, mode="ce2d")
+        # the same copies replayed from a CUDA graph (no host issue per call)
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):
+            pl.ag_place(slots, full_b, mode="ce2d")
+        torch.cuda.synchronize()
+        ce_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ce_graph, stream=side):
+            pl.ag_place(slots, full_b, mode="ce2d")
+        arms["placement_copy_engines_graph"] = ce_graph.replay
 
     quiet = torch.cuda.Stream()
     rs_alone = {name: _time_alone(fn, 10, quiet) for name, fn in arms.items()}
@@ -127,6 +138,7 @@ def measure(workload: str = "llama3.1_8b_block", budgets=(0, 64, 16), n_rs: int 
             r["slowdown"] = round(r["victim_ms"] / alone - 1.0, 4) if r["victim_ms"] else None
             entry["arms"][name] = r
         res["victims"][vname] = entry
+    arms.clear()  # the captured graph goes before the plans it reads
     for p in plans.values():
         p.close()
     del pack, out
