@@ -612,9 +612,12 @@ def run_ours(args):
     }
 
     # the other placement engines and the mixed-precision placement, timed alone after the step
-    if rank == 0 and not args.no_variants:
+    # the per-GPU extras (variants, enqueue times, baselines, interference) at N = 1 only:
+    # with N > 1 every rank is an independent replica of the same GPU work
+    single = world == 1
+    if single and not args.no_variants:
         result["variants"] = time_variants(plan, w, S, slots, full, dev, gs.views, steps=min(K, 20))
-    if rank == 0:
+    if single:
         result["host_issue_us"] = host_issue_us({
             "tide_rs_fold": lambda: plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate),
             "tide_ag_place sm": lambda: plan.ag_place(slots, full_b, mode="sm"),
@@ -623,14 +626,14 @@ def run_ours(args):
             "tide_ag_place ce1d": lambda: plan.ag_place(slots, full_b, mode="ce1d")})
 
     # two-pass stock-FSDP2-style baseline (chunk_cat pack to fp32, then reduce), timed alone
-    if not args.no_baseline and rank == 0:
+    if not args.no_baseline and single:
         result["baseline_two_pass"] = baselines.time_two_pass(w, gs.views, S, out, slots, full, steps=min(K, 10))
         b = result["baseline_two_pass"]
         b["fused_speedup_rs"] = round(b["rs_ms"] / rs_mean, 3)
         b["fused_speedup_ag"] = round(b["ag_ms"] / ag_mean, 3)
 
     # concurrent-compute interference (victim GEMMs / elementwise vs the RS arms)
-    if not args.no_interference and rank == 0:
+    if not args.no_interference and single:
         from all_gather_gb300 import interference
         result["interference"] = interference.summarize(
             interference.measure(w.name, budgets=(0, 128, 64, 32, 16, 8), n_rs=20, device=local, grads=gs))
@@ -641,7 +644,7 @@ def run_ours(args):
     if not args.no_e2e:
         result["e2e"] = e2e(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world)
 
-    if rank == 0 and not args.no_cpu_baseline:
+    if single and not args.no_cpu_baseline:
         host = []
         for name in SAMPLE_PARAMS:
             i = w.names.index(name)
