@@ -159,10 +159,14 @@ typedef struct {
     int32_t kernel;       /* TIDE_KERNEL_* */
     int32_t grad_dtype;   /* TIDE_DTYPE_* */
     uint32_t debug;       /* TIDE_DEBUG_* bits */
-    int32_t fill_bytes;   /* bulk kernel: bf16 bytes per rank in one shared-memory stage fill
-                             (multiple of 16, at most 4096); 0 = 4096 */
+    int32_t fill_bytes;   /* bulk kernel: gradient bytes per rank in one shared-memory stage fill
+                             (multiple of 16, at most 4096); 0 = 4096 (fp32 gradients and the
+                             tree order with 8 or more full fills per chunk: at most 2048
+                             elements' worth) */
     int32_t fill_ranks;   /* bulk kernel: ranks per stage fill (0 = min(W, 8)); wider groups take
-                             several fills per chunk, summed in registers in rank order */
+                             several fills per chunk, summed in registers in the plan's order.
+                             TIDE_ORDER_TREE: at most 8, rounded down to a power of two when
+                             below W, and W / fill_ranks <= 255 */
     int32_t node_size;    /* TIDE_ORDER_NODES: ranks per node, dividing the world; else 0 */
     int32_t ce_streams;   /* copy-engine placement: internal streams the copies are spread over,
                              so several copy engines work at once (0 = 8, at most 8) */
