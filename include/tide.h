@@ -160,9 +160,9 @@ typedef struct {
     int32_t grad_dtype;   /* TIDE_DTYPE_* */
     uint32_t debug;       /* TIDE_DEBUG_* bits */
     int32_t fill_bytes;   /* bulk kernel: gradient bytes per rank in one shared-memory stage fill
-                             (multiple of 16, at most 4096); 0 = 4096 (fp32 gradients and the
-                             tree order with 8 or more full fills per chunk: at most 2048
-                             elements' worth) */
+                             (multiple of 16, at most 4096); 0 = 4096.  A fill holds at most
+                             2,048 elements (1,024 for the tree order with 8 or more full fills
+                             per chunk) */
     int32_t fill_ranks;   /* bulk kernel: ranks per stage fill (0 = min(W, 8)); wider groups take
                              several fills per chunk, summed in registers in the plan's order.
                              TIDE_ORDER_TREE: at most 8, rounded down to a power of two when
