@@ -409,6 +409,11 @@ __host__ __device__ constexpr size_t bulk_ring_offset(int stages, int world)
 
 constexpr int kBulkMaxVec = 2;                               // vectors per consumer thread per chunk
 constexpr int64_t kBulkMaxFill = 8 * kBulkMaxVec * 32 * kBulkConsumerWarps;  // 2048 elements
+// Wide consumers (a CTA with the SM to itself): 4 vectors per thread, fills
+// of up to 8,192 elements (16 KB of bf16) per rank, so that each bulk copy
+// is larger (a copy costs a fixed ~60 ns per SM on top of its bytes).
+constexpr int kWideVec = 4;
+constexpr int64_t kBulkMaxFillWide = 8 * kWideVec * 32 * kBulkConsumerWarpsWide;  // 8192 elements
 
 constexpr int32_t kStatusConsumerTimeout = 1;
 constexpr int32_t kStatusProducerTimeout = 2;
@@ -499,6 +504,51 @@ __device__ __forceinline__ void lds8(const float *p, float (&f)[8])
     const float4 b = *reinterpret_cast<const float4 *>(p + 4);
     f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
     f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+// Tuning knob (compile-time, default on): add staged bf16 values into the
+// fp32 sums with the mixed-precision add of sm_100 and later (widening is
+// exact, the add rounds once to nearest even: the same result as widening
+// first), one instruction per element instead of two.
+#ifndef TIDE_BULK_MIXED_ADD
+#define TIDE_BULK_MIXED_ADD 1
+#endif
+
+// acc[2i] += lo bf16 of w_i, acc[2i+1] += hi bf16 of w_i for the 4 words of x.
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &x)
+{
+#if TIDE_BULK_MIXED_ADD
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+            : "+f"(acc[2 * i]), "+f"(acc[2 * i + 1])
+            : "r"(w[i]));
+#else
+    float f[8];
+    unpack8(x, f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        acc[e] = __fadd_rn(acc[e], f[e]);
+#endif
+}
+
+template <typename E>
+__device__ __forceinline__ void lds_add8(const E *p, float (&acc)[8]);
+template <>
+__device__ __forceinline__ void lds_add8<uint16_t>(const uint16_t *p, float (&acc)[8])
+{
+    add_bf16x8(acc, lds_v4(p));
+}
+template <>
+__device__ __forceinline__ void lds_add8<float>(const float *p, float (&acc)[8])
+{
+    float f[8];
+    lds8(p, f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        acc[e] = __fadd_rn(acc[e], f[e]);
 }
 
 __device__ __forceinline__ void add8(const float (&a)[8], float (&c)[8])
@@ -620,13 +670,16 @@ struct TreeShape {
 
 // ACC: accumulate into the existing shard.  E: gradient element (uint16_t =
 // bf16, float = fp32).  MODE: how the consumers combine the staged ranks.
-template <bool ACC, typename E, int MODE>
-__global__ void __launch_bounds__(kBulkThreads, 2) fold_bulk_kernel(const FoldParams fp)
+// CW: consumer warps (4, two CTAs per SM; or 8, one vector each, for a CTA
+// that has the SM to itself).
+template <bool ACC, typename E, int MODE, int CW = kBulkConsumerWarps>
+__global__ void __launch_bounds__(32 * (1 + CW), CW == kBulkConsumerWarps ? 2 : 1)
+    fold_bulk_kernel(const FoldParams fp)
 {
     constexpr bool GROUPED = MODE == kModeNodes;
     constexpr bool TREE = TreeShape<MODE>::tree;
     constexpr int LV = TreeShape<MODE>::levels;
-    constexpr int NV = TREE ? TreeShape<MODE>::vec : kBulkMaxVec;
+    constexpr int NV = TREE ? TreeShape<MODE>::vec : CW == kBulkConsumerWarps ? kBulkMaxVec : kWideVec;
     extern __shared__ __align__(128) unsigned char smem[];
     const int W = fp.world;
     const int RG = fp.fill_ranks;          // ranks per stage fill
@@ -645,7 +698,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fold_bulk_kernel(const FoldPa
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kBulkConsumerWarps);
+            mbar_init(&empty[s], CW);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -721,7 +774,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fold_bulk_kernel(const FoldPa
     // chunk and keeps their fp32 sums in registers across the chunk's NG
     // fills, so the contributions are added in the plan's sequence.
     const int ctid = threadIdx.x - 32;
-    constexpr int NCT = 32 * kBulkConsumerWarps;
+    constexpr int NCT = 32 * CW;
     uint32_t stage = 0, phase = 0;
     for (int64_t it = blockIdx.x; it < fp.n_items; it += gridDim.x) {
         const Item item = fp.items[it];
@@ -796,13 +849,8 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fold_bulk_kernel(const FoldPa
                                 j0 = 1;
                             }
 #pragma unroll 4
-                            for (int j = j0; j < nr; ++j) {
-                                float f[8];
-                                lds8(sb + size_t(j) * FILL + v * 8, f);
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    acc[k][e] = __fadd_rn(acc[k][e], f[e]);
-                            }
+                            for (int j = j0; j < nr; ++j)
+                                lds_add8(sb + size_t(j) * FILL + v * 8, acc[k]);
                         } else {
                             // The fill's ranks, as runs of consecutive ranks of one node.
                             const int kk = GROUPED ? k : 0;
@@ -894,10 +942,14 @@ FoldKernel pick_bulk_mode(int order, int fills, int full_fills)
 }
 
 // The tree counter's depth follows the stage fills per chunk: `fills` in
-// all, `full_fills` of them holding fill_ranks ranks.
+// all, `full_fills` of them holding fill_ranks ranks.  `cw`: consumer warps
+// (bulk_consumer_warps; the wide form exists for bf16 chains only).
 template <bool ACC>
-FoldKernel pick_bulk(int dtype, int order, int world, int fill_ranks)
+FoldKernel pick_bulk(int dtype, int order, int world, int fill_ranks, int cw = kBulkConsumerWarps)
 {
+    if (cw == kBulkConsumerWarpsWide && dtype == TIDE_DTYPE_BF16 &&
+        (order == TIDE_ORDER_RANK_ASC || order == TIDE_ORDER_STAGED_OWN))
+        return fold_bulk_kernel<ACC, uint16_t, kModeChain, kBulkConsumerWarpsWide>;
     const int fills = (world + fill_ranks - 1) / fill_ranks, full_fills = world / fill_ranks;
     return dtype == TIDE_DTYPE_F32 ? pick_bulk_mode<ACC, float>(order, fills, full_fills)
                                    : pick_bulk_mode<ACC, uint16_t>(order, fills, full_fills);
@@ -914,9 +966,14 @@ BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_s
     // that every full fill is a complete subtree; with 8 or more full fills
     // per chunk (the deep counter) one vector per consumer thread, so half
     // the fill.
+    // A CTA with the SM to itself and wide consumers (bf16 chains): 16 KB
+    // per rank per copy, 4 ranks per fill (64 KB stages, three in the ring):
+    // at small CTA budgets each SM is limited by its per-copy cost, not HBM.
     const bool tree = order == TIDE_ORDER_TREE;
+    const bool wide_sm = bulk_consumer_warps(whole_sm, order, elem_bytes == 4 ? TIDE_DTYPE_F32 : TIDE_DTYPE_BF16) ==
+                         kBulkConsumerWarpsWide;
     BulkShape b{};
-    int rg = fill_ranks > 0 ? fill_ranks : 8;
+    int rg = fill_ranks > 0 ? fill_ranks : wide_sm ? 4 : 8;
     if (tree && rg > 8)
         rg = 8;
     if (rg >= world)
@@ -925,8 +982,8 @@ BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_s
         while (rg & (rg - 1))
             rg &= rg - 1;  // largest power of two not above it
     const bool deep = tree && rg < world && world / rg >= (1 << kTreeLevelsShallow);
-    const int64_t max_fill = deep ? kBulkMaxFill / kBulkMaxVec : kBulkMaxFill;
-    int64_t fill = fill_elems > 0 ? fill_elems : 4096 / elem_bytes;
+    const int64_t max_fill = deep ? kBulkMaxFill / kBulkMaxVec : wide_sm ? kBulkMaxFillWide : kBulkMaxFill;
+    int64_t fill = fill_elems > 0 ? fill_elems : wide_sm ? kBulkMaxFillWide : 4096 / elem_bytes;
     if (fill > max_fill)
         fill = max_fill;
     fill &= ~int64_t(7);
@@ -957,7 +1014,7 @@ size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems, int fill_ranks
 }
 
 cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *blocks_per_sm, int dtype, int order,
-                           int fill_ranks)
+                           int fill_ranks, int consumer_warps)
 {
     if (kernel == TIDE_KERNEL_BULK) {
         // Allow the device maximum once per kernel instance: it serves every
@@ -971,14 +1028,16 @@ cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *b
         if (smem > size_t(optin))
             return cudaErrorInvalidValue;
         const int rg = bulk_shape(world, 0, fill_ranks, false, dtype == TIDE_DTYPE_F32 ? 4 : 2, order).fill_ranks;
+        const int cw = consumer_warps;
         for (int acc = 0; acc < 2; ++acc) {
-            FoldKernel k = acc ? pick_bulk<true>(dtype, order, world, rg) : pick_bulk<false>(dtype, order, world, rg);
+            FoldKernel k = acc ? pick_bulk<true>(dtype, order, world, rg, cw)
+                               : pick_bulk<false>(dtype, order, world, rg, cw);
             e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
             if (e != cudaSuccess)
                 return e;
         }
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            blocks_per_sm, pick_bulk<false>(dtype, order, world, rg), block, smem);
+            blocks_per_sm, pick_bulk<false>(dtype, order, world, rg, cw), block, smem);
     }
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, pick_direct<false>(world), block, smem);
 }
@@ -988,8 +1047,8 @@ cudaError_t launch_fold(const FoldParams &fp, int kernel, int accumulate, int gr
 {
     FoldKernel k;
     if (kernel == TIDE_KERNEL_BULK)
-        k = accumulate ? pick_bulk<true>(fp.dtype, fp.order, fp.world, fp.fill_ranks)
-                       : pick_bulk<false>(fp.dtype, fp.order, fp.world, fp.fill_ranks);
+        k = accumulate ? pick_bulk<true>(fp.dtype, fp.order, fp.world, fp.fill_ranks, fp.consumer_warps)
+                       : pick_bulk<false>(fp.dtype, fp.order, fp.world, fp.fill_ranks, fp.consumer_warps);
     else
         k = accumulate ? pick_direct<true>(fp.world) : pick_direct<false>(fp.world);
     k<<<grid, block, smem, stream>>>(fp);

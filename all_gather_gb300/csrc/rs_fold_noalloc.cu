@@ -223,6 +223,7 @@ extern "C" tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params,
     fp.fill_elems = bs.fill_elems;
     fp.fill_ranks = bs.fill_ranks;
     fp.stages = bs.stages;
+    fp.consumer_warps = tide::kBulkConsumerWarps;
     int per_sm = 0, sms = 0;
     e = tide::fold_occupancy(TIDE_KERNEL_BULK, world, tide::kBulkThreads, bs.smem_bytes, &per_sm);
     if (e == cudaSuccess)

@@ -28,6 +28,10 @@ constexpr int kMaxWorld = 1024;
 constexpr int kFoldThreads = 256;            // threads per fold CTA (direct kernel)
 constexpr int kBulkConsumerWarps = 4;        // bulk kernel: warp 0 produces, warps 1..4 consume
 constexpr int kBulkThreads = 32 * (1 + kBulkConsumerWarps);
+// A bulk CTA that has an SM to itself (small CTA budgets) runs 8 consumer
+// warps, one vector each, when it folds bf16 gradients in one chain (rank or
+// one-node order): twice the warps to hide each warp's latency.
+constexpr int kBulkConsumerWarpsWide = 8;
 #ifndef TIDE_BULK_RING_KB
 #define TIDE_BULK_RING_KB 96
 #endif
@@ -85,6 +89,7 @@ struct FoldParams {
     int32_t order;            // TIDE_ORDER_*
     int32_t node_size;        // ranks per node of TIDE_ORDER_NODES
     int32_t dtype;            // TIDE_DTYPE_* of the gradients
+    int32_t consumer_warps;   // kBulkConsumerWarps or kBulkConsumerWarpsWide (bulk_consumer_warps)
 };
 
 // Stage geometry of the bulk kernel for a world size.
@@ -124,7 +129,14 @@ constexpr int kAgParamsSmall = 32;
 cudaError_t launch_fold(const FoldParams &fp, int kernel, int accumulate, int grid, int block, size_t smem,
                         cudaStream_t stream);
 cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *blocks_per_sm,
-                           int dtype = TIDE_DTYPE_BF16, int order = TIDE_ORDER_RANK_ASC, int fill_ranks = 0);
+                           int dtype = TIDE_DTYPE_BF16, int order = TIDE_ORDER_RANK_ASC, int fill_ranks = 0,
+                           int consumer_warps = kBulkConsumerWarps);
+// Consumer warps of the bulk kernel for a launch shape.
+inline int bulk_consumer_warps(bool whole_sm, int order, int dtype)
+{
+    const bool chain = order == TIDE_ORDER_RANK_ASC || order == TIDE_ORDER_STAGED_OWN;
+    return whole_sm && chain && dtype == TIDE_DTYPE_BF16 ? kBulkConsumerWarpsWide : kBulkConsumerWarps;
+}
 size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems, int fill_ranks, bool whole_sm,
                        int elem_bytes = 2, int order = TIDE_ORDER_RANK_ASC);
 cudaError_t launch_ag(const AgParams &ap, int grid, cudaStream_t stream);
@@ -156,6 +168,7 @@ struct tide_plan {
     int kernel = TIDE_KERNEL_DIRECT;
     int elem_bytes = 2;                  // gradient element size (bf16 2, fp32 4)
     bool whole_sm = false;               // bulk kernel: at most one CTA per SM (deeper ring)
+    int consumer_warps = tide::kBulkConsumerWarps;  // bulk kernel: consumer warps per CTA
     bool host_only = false;
     int device = -1;
     uintptr_t src_lo = 0, src_hi = 0;    // hull of all gradient ranges

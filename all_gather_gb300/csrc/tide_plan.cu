@@ -90,8 +90,8 @@ tide_status_t check_flags(const tide_plan_flags_t &f)
         return fail(TIDE_ERR_INVALID_ARG, "flags.reserved[0] must be zero");
     if (f.ce_streams < 0 || f.ce_streams > 8)
         return fail(TIDE_ERR_INVALID_ARG, "flags.ce_streams %d outside [0, 8]", f.ce_streams);
-    if (f.fill_bytes != 0 && (f.fill_bytes < 16 || f.fill_bytes % 16 != 0 || f.fill_bytes > 4096))
-        return fail(TIDE_ERR_INVALID_ARG, "flags.fill_bytes %d: need 0 or a multiple of 16 in [16, 4096]",
+    if (f.fill_bytes != 0 && (f.fill_bytes < 16 || f.fill_bytes % 16 != 0 || f.fill_bytes > 16384))
+        return fail(TIDE_ERR_INVALID_ARG, "flags.fill_bytes %d: need 0 or a multiple of 16 in [16, 16384]",
                     f.fill_bytes);
     if (f.fill_ranks < 0 || f.fill_ranks > tide::kMaxWorld)
         return fail(TIDE_ERR_INVALID_ARG, "flags.fill_ranks %d", f.fill_ranks);
@@ -431,9 +431,12 @@ static tide_status_t plan_build_impl(int32_t world, int32_t num_params, const ti
     if (plan->whole_sm)
         plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, f.fill_bytes / plan->elem_bytes, f.fill_ranks,
                                                 true, plan->elem_bytes, f.order);
+    plan->consumer_warps = tide::bulk_consumer_warps(plan->whole_sm, f.order, f.grad_dtype);
+    if (plan->kernel == TIDE_KERNEL_BULK)
+        plan->block = 32 * (1 + plan->consumer_warps);
     int per_sm = 0;
     e = tide::fold_occupancy(plan->kernel, world, plan->block, plan->fold_smem, &per_sm, f.grad_dtype, f.order,
-                             f.fill_ranks);
+                             f.fill_ranks, plan->consumer_warps);
     if (e != cudaSuccess)
         return bail(cuda_fail(e, "fold occupancy"));
     if (per_sm < 1)
@@ -578,6 +581,7 @@ tide_status_t tide_rs_fold(tide_plan_t *plan, float *out_base, int64_t out_slot_
     fp.fill_elems = bs.fill_elems;
     fp.fill_ranks = bs.fill_ranks;
     fp.stages = bs.stages;
+    fp.consumer_warps = plan->consumer_warps;
     const int grid = int(std::min<int64_t>(plan->grid, fp.n_items));
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     cudaError_t e = tide::launch_fold(fp, plan->kernel, accumulate, grid, plan->block, plan->fold_smem, stream);

@@ -355,7 +355,7 @@ def _random_flags(rnd, world):
               grad_dtype=tide.TIDE_DTYPE_F32 if f32 else tide.TIDE_DTYPE_BF16,
               cta_budget=rnd.choice([0, 0, 1, 3, rnd.randint(1, 400)]),
               chunk_bytes=rnd.choice([0, 256, 256 * rnd.randint(1, 256)]),
-              fill_bytes=rnd.choice([0, 16, 16 * rnd.randint(1, 256)]),
+              fill_bytes=rnd.choice([0, 16, 16 * rnd.randint(1, 1024)]),
               fill_ranks=rnd.choice([0, 1, 2, rnd.randint(1, world + 2)]))
     if order == tide.TIDE_ORDER_NODES:
         kw["node_size"] = rnd.choice([d for d in range(1, world + 1) if world % d == 0])
