@@ -617,7 +617,7 @@ def run_ours(args):
     single = world == 1
     if single and not args.no_variants:
         result["variants"] = time_variants(plan, w, S, slots, full, dev, gs.views, steps=min(K, 20))
-    if single:
+    if single and not args.no_variants:
         result["host_issue_us"] = host_issue_us({
             "tide_rs_fold": lambda: plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate),
             "tide_ag_place sm": lambda: plan.ag_place(slots, full_b, mode="sm"),
