@@ -757,6 +757,35 @@ def test_full_size_sampled(index):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("index", [2, 3, 5])
+def test_full_size_bitwise_across_launch_shapes(index):
+    """Full-size groups: the rank-order fold is bitwise identical, over every
+    output element, at full wave (two CTAs per SM), with 152, 64, 16 and 7 CTAs
+    (one CTA per SM: eight consumer warps and 16 KB copies), with the
+    direct-load kernel, and with odd stage shapes."""
+    w = workloads.get(index)
+    gs = workloads.make_grads(w, device="cuda")
+    _, _, S = oracle.geometry(w.world, w.dim0_rownumel())
+    init = workloads.make_out_init(w, S, device="cuda") if w.accumulate else None
+    ref = None
+    for kw in ({}, {"cta_budget": 152}, {"cta_budget": 64}, {"cta_budget": 16}, {"cta_budget": 7},
+               {"kernel": tide.TIDE_KERNEL_DIRECT}, {"fill_bytes": 1008, "fill_ranks": 3},
+               {"cta_budget": 32, "fill_bytes": 12288, "fill_ranks": 5}):
+        out = init.clone() if init is not None else torch.zeros(w.world, S, device="cuda")
+        with tide.Plan(gs.views, tide.make_flags(**kw)) as plan:
+            plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
+            torch.cuda.synchronize()
+            assert plan.device_status() == tide.TIDE_OK
+        if ref is None:
+            ref = out
+        else:
+            same = torch.equal(out.view(torch.int32), ref.view(torch.int32))
+            assert same, f"{w.name}: {kw} differs from the full-wave fold"
+            del out
+    del gs, ref, init
+    torch.cuda.empty_cache()
+
+
 def test_parameter_beyond_2g_elements():
     """One parameter of 2,097,153 x 1,024 = 2^31 + 1,024 elements on 2 ranks
     (about 26 GB with outputs): rank 1's rows start at element 1,073,742,848 and
