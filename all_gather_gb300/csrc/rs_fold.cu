@@ -857,23 +857,13 @@ __global__ void __launch_bounds__(32 * (1 + CW), CW == kBulkConsumerWarps ? 2 : 
                             for (int j = 0; j < nr;) {
                                 const int q = u0 + j, l = q % L;
                                 const int run = nr - j < L - l ? nr - j : L - l;
-                                float f[8];
-                                lds8(sb + size_t(j) * FILL + v * 8, f);
-                                if (l == 0) {
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e)
-                                        part[kk][e] = f[e];
-                                } else {
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e)
-                                        part[kk][e] = __fadd_rn(part[kk][e], f[e]);
-                                }
-                                for (int t = 1; t < run; ++t) {
-                                    lds8(sb + size_t(j + t) * FILL + v * 8, f);
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e)
-                                        part[kk][e] = __fadd_rn(part[kk][e], f[e]);
-                                }
+                                if (l == 0)
+                                    lds8(sb + size_t(j) * FILL + v * 8, part[kk]);
+                                else
+                                    lds_add8(sb + size_t(j) * FILL + v * 8, part[kk]);
+#pragma unroll 4
+                                for (int t = 1; t < run; ++t)
+                                    lds_add8(sb + size_t(j + t) * FILL + v * 8, part[kk]);
                                 if (l + run == L) {  // node complete: add its partial
                                     if (q == l) {
 #pragma unroll
@@ -943,13 +933,13 @@ FoldKernel pick_bulk_mode(int order, int fills, int full_fills)
 
 // The tree counter's depth follows the stage fills per chunk: `fills` in
 // all, `full_fills` of them holding fill_ranks ranks.  `cw`: consumer warps
-// (bulk_consumer_warps; the wide form exists for bf16 chains only).
+// (bulk_consumer_warps; only chains have the wide form).
 template <bool ACC>
 FoldKernel pick_bulk(int dtype, int order, int world, int fill_ranks, int cw = kBulkConsumerWarps)
 {
-    if (cw == kBulkConsumerWarpsWide && dtype == TIDE_DTYPE_BF16 &&
-        (order == TIDE_ORDER_RANK_ASC || order == TIDE_ORDER_STAGED_OWN))
-        return fold_bulk_kernel<ACC, uint16_t, kModeChain, kBulkConsumerWarpsWide>;
+    if (cw == kBulkConsumerWarpsWide && (order == TIDE_ORDER_RANK_ASC || order == TIDE_ORDER_STAGED_OWN))
+        return dtype == TIDE_DTYPE_F32 ? fold_bulk_kernel<ACC, float, kModeChain, kBulkConsumerWarpsWide>
+                                       : fold_bulk_kernel<ACC, uint16_t, kModeChain, kBulkConsumerWarpsWide>;
     const int fills = (world + fill_ranks - 1) / fill_ranks, full_fills = world / fill_ranks;
     return dtype == TIDE_DTYPE_F32 ? pick_bulk_mode<ACC, float>(order, fills, full_fills)
                                    : pick_bulk_mode<ACC, uint16_t>(order, fills, full_fills);
@@ -966,9 +956,9 @@ BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_s
     // that every full fill is a complete subtree; with 8 or more full fills
     // per chunk (the deep counter) one vector per consumer thread, so half
     // the fill.
-    // A CTA with the SM to itself and wide consumers (bf16 chains): 16 KB
-    // per rank per copy, 4 ranks per fill (64 KB stages, three in the ring):
-    // at small CTA budgets each SM is limited by its per-copy cost, not HBM.
+    // A CTA with the SM to itself and wide consumers: 16 KB per rank per
+    // copy, 4 ranks per fill (64 KB stages, three in the ring): at small CTA
+    // budgets each SM is limited by its per-copy cost, not HBM.
     const bool tree = order == TIDE_ORDER_TREE;
     const bool wide_sm = bulk_consumer_warps(whole_sm, order, elem_bytes == 4 ? TIDE_DTYPE_F32 : TIDE_DTYPE_BF16) ==
                          kBulkConsumerWarpsWide;
@@ -983,7 +973,7 @@ BulkShape bulk_shape(int world, int64_t fill_elems, int fill_ranks, bool whole_s
             rg &= rg - 1;  // largest power of two not above it
     const bool deep = tree && rg < world && world / rg >= (1 << kTreeLevelsShallow);
     const int64_t max_fill = deep ? kBulkMaxFill / kBulkMaxVec : wide_sm ? kBulkMaxFillWide : kBulkMaxFill;
-    int64_t fill = fill_elems > 0 ? fill_elems : wide_sm ? kBulkMaxFillWide : 4096 / elem_bytes;
+    int64_t fill = fill_elems > 0 ? fill_elems : wide_sm ? 16384 / elem_bytes : 4096 / elem_bytes;
     if (fill > max_fill)
         fill = max_fill;
     fill &= ~int64_t(7);
