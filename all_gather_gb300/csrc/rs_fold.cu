@@ -822,60 +822,71 @@ __global__ void __launch_bounds__(32 * (1 + CW), CW == kBulkConsumerWarps ? 2 : 
                     return;
                 }
                 const E *sb = ring + size_t(stage) * RG * FILL;
+                if constexpr (GROUPED) {
+                    // The fill's ranks, as runs of consecutive ranks of one
+                    // node; the runs are the same for every vector, so they
+                    // are walked once, each run over all of this thread's
+                    // vectors.  After the first run, runs start on a node.
+                    int l = u0 % L;
+                    for (int j = 0; j < nr;) {
+                        const int run = nr - j < L - l ? nr - j : L - l;
+                        const bool node_end = l + run == L, first_node = u0 + j < L;
 #pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    const int64_t v = ctid + int64_t(k) * NCT;
-                    if (v < nv) {
-                        if constexpr (TREE) {
-                            float p[8];
-                            if (nr == 8)
-                                tree_fill_pow2<8>(sb, FILL, v, p);
-                            else if (nr == 4)
-                                tree_fill_pow2<4>(sb, FILL, v, p);
-                            else if (nr == 2)
-                                tree_fill_pow2<2>(sb, FILL, v, p);
-                            else
-                                tree_fill(sb, FILL, v, nr, p);
-                            if constexpr (LV == 0)
-                                copy8(p, acc[k]);  // the one fill holds every rank
-                            else if (nr == RG)
-                                tree_push<LV>(tx[k], g, p);
-                            else
-                                copy8(p, acc[k]);  // the last fill, short: its partial waits in acc
-                        } else if (!GROUPED) {
-                            int j0 = 0;
-                            if (g == 0) {
-                                lds8(sb + v * 8, acc[k]);
-                                j0 = 1;
-                            }
-#pragma unroll 4
-                            for (int j = j0; j < nr; ++j)
-                                lds_add8(sb + size_t(j) * FILL + v * 8, acc[k]);
-                        } else {
-                            // The fill's ranks, as runs of consecutive ranks of one node.
-                            const int kk = GROUPED ? k : 0;
-                            for (int j = 0; j < nr;) {
-                                const int q = u0 + j, l = q % L;
-                                const int run = nr - j < L - l ? nr - j : L - l;
+                        for (int k = 0; k < NV; ++k) {
+                            const int64_t v = ctid + int64_t(k) * NCT;
+                            if (v < nv) {
+                                const E *p0 = sb + size_t(j) * FILL + v * 8;
                                 if (l == 0)
-                                    lds8(sb + size_t(j) * FILL + v * 8, part[kk]);
+                                    lds8(p0, part[k]);
                                 else
-                                    lds_add8(sb + size_t(j) * FILL + v * 8, part[kk]);
+                                    lds_add8(p0, part[k]);
 #pragma unroll 4
                                 for (int t = 1; t < run; ++t)
-                                    lds_add8(sb + size_t(j + t) * FILL + v * 8, part[kk]);
-                                if (l + run == L) {  // node complete: add its partial
-                                    if (q == l) {
-#pragma unroll
-                                        for (int e = 0; e < 8; ++e)
-                                            acc[k][e] = part[kk][e];
+                                    lds_add8(p0 + size_t(t) * FILL, part[k]);
+                                if (node_end) {  // node complete: add its partial
+                                    if (first_node) {
+                                        copy8(part[k], acc[k]);
                                     } else {
 #pragma unroll
                                         for (int e = 0; e < 8; ++e)
-                                            acc[k][e] = __fadd_rn(acc[k][e], part[kk][e]);
+                                            acc[k][e] = __fadd_rn(acc[k][e], part[k][e]);
                                     }
                                 }
-                                j += run;
+                            }
+                        }
+                        j += run;
+                        l = 0;
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < NV; ++k) {
+                        const int64_t v = ctid + int64_t(k) * NCT;
+                        if (v < nv) {
+                            if constexpr (TREE) {
+                                float p[8];
+                                if (nr == 8)
+                                    tree_fill_pow2<8>(sb, FILL, v, p);
+                                else if (nr == 4)
+                                    tree_fill_pow2<4>(sb, FILL, v, p);
+                                else if (nr == 2)
+                                    tree_fill_pow2<2>(sb, FILL, v, p);
+                                else
+                                    tree_fill(sb, FILL, v, nr, p);
+                                if constexpr (LV == 0)
+                                    copy8(p, acc[k]);  // the one fill holds every rank
+                                else if (nr == RG)
+                                    tree_push<LV>(tx[k], g, p);
+                                else
+                                    copy8(p, acc[k]);  // the last fill, short: its partial waits in acc
+                            } else {
+                                int j0 = 0;
+                                if (g == 0) {
+                                    lds8(sb + v * 8, acc[k]);
+                                    j0 = 1;
+                                }
+#pragma unroll 4
+                                for (int j = j0; j < nr; ++j)
+                                    lds_add8(sb + size_t(j) * FILL + v * 8, acc[k]);
                             }
                         }
                     }
@@ -933,13 +944,17 @@ FoldKernel pick_bulk_mode(int order, int fills, int full_fills)
 
 // The tree counter's depth follows the stage fills per chunk: `fills` in
 // all, `full_fills` of them holding fill_ranks ranks.  `cw`: consumer warps
-// (bulk_consumer_warps; only chains have the wide form).
+// (bulk_consumer_warps; the tree order has no wide form).
 template <bool ACC>
 FoldKernel pick_bulk(int dtype, int order, int world, int fill_ranks, int cw = kBulkConsumerWarps)
 {
-    if (cw == kBulkConsumerWarpsWide && (order == TIDE_ORDER_RANK_ASC || order == TIDE_ORDER_STAGED_OWN))
-        return dtype == TIDE_DTYPE_F32 ? fold_bulk_kernel<ACC, float, kModeChain, kBulkConsumerWarpsWide>
-                                       : fold_bulk_kernel<ACC, uint16_t, kModeChain, kBulkConsumerWarpsWide>;
+    constexpr int CW = kBulkConsumerWarpsWide;
+    if (cw == CW && order == TIDE_ORDER_NODES)
+        return dtype == TIDE_DTYPE_F32 ? fold_bulk_kernel<ACC, float, kModeNodes, CW>
+                                       : fold_bulk_kernel<ACC, uint16_t, kModeNodes, CW>;
+    if (cw == CW && (order == TIDE_ORDER_RANK_ASC || order == TIDE_ORDER_STAGED_OWN))
+        return dtype == TIDE_DTYPE_F32 ? fold_bulk_kernel<ACC, float, kModeChain, CW>
+                                       : fold_bulk_kernel<ACC, uint16_t, kModeChain, CW>;
     const int fills = (world + fill_ranks - 1) / fill_ranks, full_fills = world / fill_ranks;
     return dtype == TIDE_DTYPE_F32 ? pick_bulk_mode<ACC, float>(order, fills, full_fills)
                                    : pick_bulk_mode<ACC, uint16_t>(order, fills, full_fills);

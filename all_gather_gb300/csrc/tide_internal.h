@@ -29,9 +29,8 @@ constexpr int kFoldThreads = 256;            // threads per fold CTA (direct ker
 constexpr int kBulkConsumerWarps = 4;        // bulk kernel: warp 0 produces, warps 1..4 consume
 constexpr int kBulkThreads = 32 * (1 + kBulkConsumerWarps);
 // A bulk CTA that has an SM to itself (small CTA budgets) runs 8 consumer
-// warps with 4 vectors each and copies 16 KB per rank when it adds one chain
-// (rank or one-node order, bf16 or fp32 gradients); the node-partial and
-// tree consumers gain nothing from it (their control flow is the cost).
+// warps with 4 vectors each and copies 16 KB per rank (every order but the
+// tree order, whose per-level partials take the registers).
 constexpr int kBulkConsumerWarpsWide = 8;
 #ifndef TIDE_BULK_RING_KB
 #define TIDE_BULK_RING_KB 96
@@ -136,8 +135,7 @@ cudaError_t fold_occupancy(int kernel, int world, int block, size_t smem, int *b
 inline int bulk_consumer_warps(bool whole_sm, int order, int dtype)
 {
     (void)dtype;
-    const bool chain = order == TIDE_ORDER_RANK_ASC || order == TIDE_ORDER_STAGED_OWN;
-    return whole_sm && chain ? kBulkConsumerWarpsWide : kBulkConsumerWarps;
+    return whole_sm && order != TIDE_ORDER_TREE ? kBulkConsumerWarpsWide : kBulkConsumerWarps;
 }
 size_t fold_smem_bytes(int kernel, int world, int64_t fill_elems, int fill_ranks, bool whole_sm,
                        int elem_bytes = 2, int order = TIDE_ORDER_RANK_ASC);
