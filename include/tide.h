@@ -152,7 +152,10 @@ enum {
                                       output of that fold is incomplete. */
 
 typedef struct {
-    int32_t cta_budget;   /* CTAs of the fold's persistent grid; 0 = one wave at full occupancy */
+    int32_t cta_budget;   /* CTAs of the fold's persistent grid; 0 = one wave at full occupancy (two
+                             bulk CTAs per SM).  A budget of at most the SM count gives each bulk
+                             CTA an SM: a 192 KB ring and, except in the tree order, 8 consumer
+                             warps and 16 KB copies per rank (the fastest shape per SM) */
     int32_t chunk_bytes;  /* bf16 bytes per rank in one work item (multiple of 256); 0 = default */
     int32_t order;        /* TIDE_ORDER_* */
     int32_t sched;        /* TIDE_SCHED_* */
@@ -160,10 +163,12 @@ typedef struct {
     int32_t grad_dtype;   /* TIDE_DTYPE_* */
     uint32_t debug;       /* TIDE_DEBUG_* bits */
     int32_t fill_bytes;   /* bulk kernel: gradient bytes per rank in one shared-memory stage fill
-                             (multiple of 16, at most 4096); 0 = 4096.  A fill holds at most
-                             2,048 elements (1,024 for the tree order with 8 or more full fills
-                             per chunk) */
-    int32_t fill_ranks;   /* bulk kernel: ranks per stage fill (0 = min(W, 8)); wider groups take
+                             (multiple of 16, at most 16384); 0 = 4096, or 16384 when each CTA
+                             has an SM (see cta_budget).  A fill holds at most 2,048 elements
+                             (8,192 with an SM per CTA; 1,024 for the tree order with 8 or more
+                             full fills per chunk), and two stages must fit in shared memory */
+    int32_t fill_ranks;   /* bulk kernel: ranks per stage fill (0 = min(W, 8), or min(W, 4) with
+                             an SM per CTA); wider groups take
                              several fills per chunk, summed in registers in the plan's order.
                              TIDE_ORDER_TREE: at most 8, rounded down to a power of two when
                              below W, and W / fill_ranks <= 255 */
