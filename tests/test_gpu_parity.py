@@ -786,6 +786,53 @@ def test_full_size_bitwise_across_launch_shapes(index):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("kernel", ["bulk", "direct"])
+def test_explicit_shard_offsets(kernel):
+    """Caller-chosen shard offsets (parameters in reverse order inside the
+    slot, odd gaps, so fp32 and bf16 windows start misaligned): every
+    parameter's fold window equals the oracle's window for that parameter,
+    the gaps keep their canaries, and every placement mode reads the shards
+    from those offsets."""
+    world = 5
+    shapes = [(23, 16), (9, 3), (64,), (11, 8)]
+    w = workloads.custom(world, shapes, index=510)
+    dims = w.dim0_rownumel()
+    R, o, S = oracle.geometry(world, dims)
+    sizes = [R[p] * k for p, (_, k) in enumerate(dims)]
+    offsets, cur = [0] * len(dims), 3
+    for p in reversed(range(len(dims))):
+        offsets[p] = cur
+        cur += sizes[p] + 5
+    stride = cur + 2
+    gs = workloads.make_grads(w, device="cuda")
+    kw = {"kernel": tide.TIDE_KERNEL_DIRECT} if kernel == "direct" else {}
+    want = oracle_rs_full(world, dims, gs.views, 0.5, False, torch.zeros(world, S))
+    with tide.Plan(gs.views, tide.make_flags(**kw), offsets=offsets) as plan:
+        assert plan.slot_numel == cur - 5
+        out = torch.full((world, stride), CANARY, device="cuda")
+        plan.rs_fold(out, alpha=0.5)
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        mask = np.ones((world, stride), bool)
+        for p in range(len(dims)):
+            assert_same_f32(got[:, offsets[p]:offsets[p] + sizes[p]], want[:, o[p]:o[p] + sizes[p]],
+                            f"{kernel} p={p} at offset {offsets[p]}")
+            mask[:, offsets[p]:offsets[p] + sizes[p]] = False
+        assert (got[mask] == np.float32(CANARY)).all(), "the fold wrote into a gap between shards"
+        # placement: slots hold each shard at its explicit offset
+        prefix = sentinel_slots(world, dims, S, seed=11)
+        slots = torch.full((world, stride), float("nan"), dtype=torch.bfloat16, device="cuda")
+        for p in range(len(dims)):
+            slots[:, offsets[p]:offsets[p] + sizes[p]] = prefix[:, o[p]:o[p] + sizes[p]]
+        wf = ag_expected(world, dims, prefix)
+        for mode in ("sm", "ce2d", "ce1d"):
+            full = [torch.full(s_, float("nan"), dtype=torch.bfloat16, device="cuda") for s_ in w.shapes]
+            plan.ag_place(slots, full, mode=mode)
+            torch.cuda.synchronize()
+            for p, f in enumerate(full):
+                assert_same_u16(bits16(f), wf[p], f"{mode} p={p} from offset {offsets[p]}")
+
+
 def test_parameter_beyond_2g_elements():
     """One parameter of 2,097,153 x 1,024 = 2^31 + 1,024 elements on 2 ranks
     (about 26 GB with outputs): rank 1's rows start at element 1,073,742,848 and
