@@ -105,8 +105,10 @@ tide_status_t check_flags(const tide_plan_flags_t &f)
         return fail(TIDE_ERR_UNSUPPORTED, "flags.order %d is not implemented", f.order);
     if (f.order == TIDE_ORDER_NODES ? f.node_size < 1 : f.node_size != 0)
         return fail(TIDE_ERR_INVALID_ARG, "flags.node_size %d (positive with TIDE_ORDER_NODES only)", f.node_size);
-    if (f.sched != TIDE_SCHED_STATIC && f.sched != TIDE_SCHED_DYNAMIC)
+    if (f.sched != TIDE_SCHED_STATIC && f.sched != TIDE_SCHED_DYNAMIC && f.sched != TIDE_SCHED_PER_ITEM)
         return fail(TIDE_ERR_INVALID_ARG, "flags.sched %d", f.sched);
+    if (f.sched == TIDE_SCHED_PER_ITEM && f.cta_budget != 0)
+        return fail(TIDE_ERR_INVALID_ARG, "TIDE_SCHED_PER_ITEM sizes the grid itself: cta_budget must be 0");
     if (f.kernel != TIDE_KERNEL_AUTO && f.kernel != TIDE_KERNEL_DIRECT && f.kernel != TIDE_KERNEL_BULK)
         return fail(TIDE_ERR_INVALID_ARG, "flags.kernel %d", f.kernel);
     if (f.grad_dtype != TIDE_DTYPE_BF16 && f.grad_dtype != TIDE_DTYPE_F32)
@@ -413,7 +415,7 @@ static tide_status_t plan_build_impl(int32_t world, int32_t num_params, const ti
     plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, f.fill_bytes / plan->elem_bytes, f.fill_ranks,
                                             false, plan->elem_bytes, f.order);
     if (plan->host_only) {
-        plan->grid = f.cta_budget ? f.cta_budget : 0;
+        plan->grid = f.sched == TIDE_SCHED_PER_ITEM ? int32_t(plan->rs_items.size()) : f.cta_budget ? f.cta_budget : 0;
         *plan_out = plan;
         return TIDE_OK;
     }
@@ -441,7 +443,8 @@ static tide_status_t plan_build_impl(int32_t world, int32_t num_params, const ti
         return bail(cuda_fail(e, "fold occupancy"));
     if (per_sm < 1)
         return bail(fail(TIDE_ERR_UNSUPPORTED, "fold kernel does not fit on an SM (world %d)", world));
-    plan->grid = f.cta_budget ? f.cta_budget : sms * per_sm;
+    plan->grid = f.sched == TIDE_SCHED_PER_ITEM ? int32_t(std::max<size_t>(plan->rs_items.size(), 1))
+                 : f.cta_budget ? f.cta_budget : sms * per_sm;
 
     size_t off = 0;
     auto carve = [&](size_t bytes) {

@@ -6,9 +6,11 @@ the slowdown is the median duration of the victims that ran entirely inside
 the reduce-scatter window over the median duration of the victim alone,
 minus one.  Victims: a bf16 GEMM of 256 x 8192 x 8192 (the page's one-wave
 GEMM), a large 8192^3 bf16 GEMM, and a 256 MiB bf16 elementwise kernel.
-Arms: the fused fold at several CTA budgets, the two-pass stock-FSDP2
-baseline, and the all-gather placement on SMs and on the copy engines (issued
-per call, or replayed from a CUDA graph).  Set CUDA_DEVICE_MAX_CONNECTIONS=32
+Arms: the fused fold at several CTA budgets and with one short-lived CTA per
+work item, the two-pass stock-FSDP2 baseline, and the all-gather placement on
+SMs and on the copy engines (issued per call, or replayed from a CUDA graph).
+Each pair runs twice: on streams of equal priority (the page's method) and
+with the victim's stream at the higher priority.  Set CUDA_DEVICE_MAX_CONNECTIONS=32
 before CUDA starts (the page's setting) so the two streams get separate
 hardware queues.
 
@@ -57,9 +59,14 @@ def _time_alone(fn, n: int, stream) -> float:
     return statistics.median(s.elapsed_time(e) for s, e in ev)
 
 
-def _co_run(rs_call: Callable[[], None], n_rs: int, victim, victim_ms: float, rs_ms_est: float) -> dict:
+def _co_run(rs_call: Callable[[], None], n_rs: int, victim, victim_ms: float, rs_ms_est: float,
+            victim_high: bool = False) -> dict:
+    """victim_high: the victim runs on a higher-priority stream than the
+    reduce-scatter (compute first, communication in the background), so the
+    block scheduler gives free SMs to the victim's CTAs first.  A persistent
+    grid holds its SMs either way; short-lived CTAs yield them as they retire."""
     import torch
-    s_rs, s_v = torch.cuda.Stream(), torch.cuda.Stream()
+    s_rs, s_v = torch.cuda.Stream(priority=0), torch.cuda.Stream(priority=-1 if victim_high else 0)
     n_v = int((rs_ms_est * n_rs) / max(victim_ms, 1e-3) * 1.5) + 20
     n_v = min(n_v, 4000)
     start = torch.cuda.Event(enable_timing=True)
@@ -103,6 +110,7 @@ def measure(workload: str = "llama3.1_8b_block", budgets=(0, 64, 16), n_rs: int 
     plans = {}
     for b in budgets:
         plans[f"fused_cta{b}" if b else "fused_full_wave"] = tide.Plan(gs.views, tide.make_flags(cta_budget=b))
+    plans["fused_per_item"] = tide.Plan(gs.views, tide.make_flags(sched=tide.TIDE_SCHED_PER_ITEM))
     S = next(iter(plans.values())).slot_numel
     out = torch.zeros(w.world, S, device=dev)
     pack = torch.empty(w.world, w.world * S, device=dev)
@@ -132,11 +140,12 @@ def measure(workload: str = "llama3.1_8b_block", budgets=(0, 64, 16), n_rs: int 
            "rs_alone_ms": {k: round(v, 4) for k, v in rs_alone.items()}, "victims": {}}
     for vname, vfn in victims.items():
         alone = _time_alone(vfn, 50, quiet)
-        entry = {"alone_ms": round(alone, 5), "arms": {}}
+        entry = {"alone_ms": round(alone, 5), "arms": {}, "arms_victim_high": {}}
         for name, fn in arms.items():
-            r = _co_run(fn, n_rs, vfn, alone, rs_alone[name])
-            r["slowdown"] = round(r["victim_ms"] / alone - 1.0, 4) if r["victim_ms"] else None
-            entry["arms"][name] = r
+            for key, high in (("arms", False), ("arms_victim_high", True)):
+                r = _co_run(fn, n_rs, vfn, alone, rs_alone[name], victim_high=high)
+                r["slowdown"] = round(r["victim_ms"] / alone - 1.0, 4) if r["victim_ms"] else None
+                entry[key][name] = r
         res["victims"][vname] = entry
     arms.clear()  # the captured graph goes before the plans it reads
     for p in plans.values():
@@ -199,7 +208,7 @@ def sm_probe(workload: str = "llama3.1_8b_block", budgets=(0, 152, 64, 16), wind
     nmax = max(PROBE_CLUSTERS * 4, n_sm)
     bufs = (torch.zeros(nmax, dtype=torch.int32, device=dev), torch.zeros(nmax, dtype=torch.int64, device=dev),
             torch.zeros(nmax, dtype=torch.int64, device=dev), torch.zeros(1, dtype=torch.int64, device=dev))
-    s_rs, s_pr = torch.cuda.Stream(), torch.cuda.Stream()
+    s_rs, s_pr = torch.cuda.Stream(priority=0), torch.cuda.Stream(priority=-1)  # the probe stands for compute
     hold = int(hold_us * 1000)
     # the probe alone: no displacement expected when it fits in one wave (the
     # first launch also loads the kernel, so it is a warm-up)
@@ -211,6 +220,7 @@ def sm_probe(workload: str = "llama3.1_8b_block", budgets=(0, 152, 64, 16), wind
     res["alone_blocked"] = _blocked(bufs[1], bufs[3], PROBE_CLUSTERS * 4)
     plans = {(f"fused_cta{b}" if b else "fused_full_wave"): tide.Plan(gs.views, tide.make_flags(cta_budget=b))
              for b in budgets}
+    plans["fused_per_item"] = tide.Plan(gs.views, tide.make_flags(sched=tide.TIDE_SCHED_PER_ITEM))
     S = next(iter(plans.values())).slot_numel
     out = torch.zeros(w.world, S, device=dev)
     pack = torch.empty(w.world, w.world * S, device=dev)
@@ -258,12 +268,16 @@ def sm_probe(workload: str = "llama3.1_8b_block", budgets=(0, 152, 64, 16), wind
 
 
 def summarize(res: dict) -> dict:
-    """victim -> {arm: slowdown} plus the RS times per arm."""
-    return {"slowdown": {v: {a: r["slowdown"] for a, r in e["arms"].items()} for v, e in res["victims"].items()},
+    """victim -> {arm: slowdown} (equal stream priorities, and the victim on a
+    higher-priority stream) plus the RS times per arm."""
+    def table(key, field):
+        return {v: {a: r[field] for a, r in e[key].items()} for v, e in res["victims"].items()}
+    return {"slowdown": table("arms", "slowdown"),
+            "slowdown_victim_high_priority": table("arms_victim_high", "slowdown"),
             "victim_alone_ms": {v: e["alone_ms"] for v, e in res["victims"].items()},
             "rs_alone_ms": res["rs_alone_ms"],
-            "rs_ms_while_corunning": {v: {a: r["rs_ms"] for a, r in e["arms"].items()}
-                                      for v, e in res["victims"].items()},
+            "rs_ms_while_corunning": table("arms", "rs_ms"),
+            "rs_ms_while_corunning_victim_high_priority": table("arms_victim_high", "rs_ms"),
             "method": "median victim duration fully inside the RS window / median alone - 1; "
                       "CUDA_DEVICE_MAX_CONNECTIONS=" + str(res["cuda_device_max_connections"])}
 

@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--ag-mode", choices=["sm", "ce2d", "ce1d"], default="sm")
     ap.add_argument("--kernel", choices=["auto", "direct", "bulk"], default="auto")
-    ap.add_argument("--sched", choices=["static", "dynamic"], default="static")
+    ap.add_argument("--sched", choices=["static", "dynamic", "per_item"], default="static")
     ap.add_argument("--cta-budget", type=int, default=0)
     ap.add_argument("--chunk-bytes", type=int, default=0)
     ap.add_argument("--fill-bytes", type=int, default=0, help="bulk kernel: bytes per rank per stage fill")
@@ -509,7 +509,7 @@ def run_ours(args):
     gs = workloads.make_grads(w, device=dev)
     flags = tide.make_flags(cta_budget=args.cta_budget, chunk_bytes=args.chunk_bytes, fill_bytes=args.fill_bytes,
                             fill_ranks=args.fill_ranks, ce_streams=args.ce_streams,
-                            sched={"static": 0, "dynamic": 1}[args.sched],
+                            sched={"static": 0, "dynamic": 1, "per_item": 2}[args.sched],
                             kernel={"auto": 0, "direct": 1, "bulk": 2}[args.kernel], order=ORDERS[args.order],
                             node_size=(args.node_size or max(1, w.world // 2)) if args.order == "nodes" else 0)
     plan = tide.Plan(gs.views, flags)

@@ -116,7 +116,13 @@ enum {
 /* Work distribution of the fold's persistent grid (bitwise identical results). */
 enum {
     TIDE_SCHED_STATIC = 0,   /* work item i goes to CTA i mod grid */
-    TIDE_SCHED_DYNAMIC = 1   /* CTAs claim items from a device counter that resets itself */
+    TIDE_SCHED_DYNAMIC = 1,  /* CTAs claim items from a device counter that resets itself */
+    TIDE_SCHED_PER_ITEM = 2  /* one short-lived CTA per work item (the grid is the work list; needs
+                                cta_budget 0).  Alone it runs as fast as the persistent grid; with
+                                the fold's stream at a lower priority than concurrent compute, the
+                                block scheduler hands SMs to the compute kernels as fold CTAs
+                                retire, so the fold yields without a fixed CTA budget (Section 2.2's
+                                SM interference) */
 };
 
 /* Reduce-scatter kernel family. */

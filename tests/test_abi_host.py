@@ -142,6 +142,7 @@ def test_empty_group(tide):
     ("f32_dynamic", "TIDE_ERR_UNSUPPORTED"), ("f32_misaligned", "TIDE_ERR_ALIGNMENT"),
     ("ce_streams", "TIDE_ERR_INVALID_ARG"), ("tree_direct", "TIDE_ERR_UNSUPPORTED"),
     ("tree_node_size", "TIDE_ERR_INVALID_ARG"), ("tree_dynamic", "TIDE_ERR_UNSUPPORTED"),
+    ("per_item_budget", "TIDE_ERR_INVALID_ARG"),
 ])
 def test_build_validation(tide, case, status):
     W, dims = 4, [(8, 8), (5, 1)]
@@ -196,6 +197,8 @@ def test_build_validation(tide, case, status):
         kw.update(order=tide.TIDE_ORDER_TREE, node_size=2)
     elif case == "tree_dynamic":
         kw.update(order=tide.TIDE_ORDER_TREE, sched=tide.TIDE_SCHED_DYNAMIC)
+    elif case == "per_item_budget":
+        kw.update(sched=tide.TIDE_SCHED_PER_ITEM, cta_budget=16)
     elif case == "f32_misaligned":
         kw.update(grad_dtype=tide.TIDE_DTYPE_F32)
         ptrs[1][1] += 2
@@ -228,6 +231,16 @@ def test_tree_order_fill_limit(tide):
                 _host_plan(tide, W, dims, order=tide.TIDE_ORDER_TREE, fill_ranks=fill_ranks)
             assert e.value.status == tide.TIDE_ERR_INVALID_ARG, fill_ranks
     tide.tide_plan_destroy(_host_plan(tide, 1020, [(1020, 1)], order=tide.TIDE_ORDER_TREE, fill_ranks=4))
+
+
+def test_per_item_schedule_grid(tide):
+    """TIDE_SCHED_PER_ITEM: the fold's grid is its work list, one CTA per item."""
+    plan = _host_plan(tide, 8, [(4096, 4096), (1024, 4096), (4096, 1)], sched=tide.TIDE_SCHED_PER_ITEM)
+    try:
+        cfg = tide.tide_plan_fold_config(plan)
+        assert cfg["grid"] == cfg["items"] > 1000
+    finally:
+        tide.tide_plan_destroy(plan)
 
 
 def test_host_only_plan_cannot_launch(tide):

@@ -67,7 +67,9 @@ KERNELS = {"direct": dict(kernel=tide.TIDE_KERNEL_DIRECT),
            "direct_dynamic": dict(kernel=tide.TIDE_KERNEL_DIRECT, sched=tide.TIDE_SCHED_DYNAMIC),
            "bulk": dict(kernel=tide.TIDE_KERNEL_BULK),
            # tiny fills and odd rank groups: many stage fills per chunk, groups of 3, 3, ..., remainder
-           "bulk_groups": dict(kernel=tide.TIDE_KERNEL_BULK, fill_bytes=64, fill_ranks=3)}
+           "bulk_groups": dict(kernel=tide.TIDE_KERNEL_BULK, fill_bytes=64, fill_ranks=3),
+           # one short-lived CTA per work item
+           "bulk_per_item": dict(kernel=tide.TIDE_KERNEL_BULK, sched=tide.TIDE_SCHED_PER_ITEM)}
 
 
 # ---------------------------------------------------------------------------
@@ -350,10 +352,10 @@ def _random_flags(rnd, world):
     kernel = tide.TIDE_KERNEL_BULK if restricted else rnd.choice(
         [tide.TIDE_KERNEL_AUTO, tide.TIDE_KERNEL_DIRECT, tide.TIDE_KERNEL_BULK])
     sched = tide.TIDE_SCHED_DYNAMIC if kernel == tide.TIDE_KERNEL_DIRECT and rnd.random() < 0.5 else \
-        tide.TIDE_SCHED_STATIC
+        tide.TIDE_SCHED_PER_ITEM if rnd.random() < 0.2 else tide.TIDE_SCHED_STATIC
     kw = dict(kernel=kernel, sched=sched, order=order,
               grad_dtype=tide.TIDE_DTYPE_F32 if f32 else tide.TIDE_DTYPE_BF16,
-              cta_budget=rnd.choice([0, 0, 1, 3, rnd.randint(1, 400)]),
+              cta_budget=0 if sched == tide.TIDE_SCHED_PER_ITEM else rnd.choice([0, 0, 1, 3, rnd.randint(1, 400)]),
               chunk_bytes=rnd.choice([0, 256, 256 * rnd.randint(1, 256)]),
               fill_bytes=rnd.choice([0, 16, 16 * rnd.randint(1, 1024)]),
               fill_ranks=rnd.choice([0, 1, 2, rnd.randint(1, world + 2)]))
@@ -761,15 +763,17 @@ def test_full_size_sampled(index):
 def test_full_size_bitwise_across_launch_shapes(index):
     """Full-size groups: the rank-order fold is bitwise identical, over every
     output element, at full wave (two CTAs per SM), with 152, 64, 16 and 7 CTAs
-    (one CTA per SM: eight consumer warps and 16 KB copies), with the
-    direct-load kernel, and with odd stage shapes."""
+    (one CTA per SM: eight consumer warps and 16 KB copies), with one CTA per
+    work item, with the direct-load kernel, and with odd stage shapes."""
     w = workloads.get(index)
     gs = workloads.make_grads(w, device="cuda")
     _, _, S = oracle.geometry(w.world, w.dim0_rownumel())
     init = workloads.make_out_init(w, S, device="cuda") if w.accumulate else None
     ref = None
     for kw in ({}, {"cta_budget": 152}, {"cta_budget": 64}, {"cta_budget": 16}, {"cta_budget": 7},
-               {"kernel": tide.TIDE_KERNEL_DIRECT}, {"fill_bytes": 1008, "fill_ranks": 3},
+               {"sched": tide.TIDE_SCHED_PER_ITEM}, {"kernel": tide.TIDE_KERNEL_DIRECT},
+               {"kernel": tide.TIDE_KERNEL_DIRECT, "sched": tide.TIDE_SCHED_PER_ITEM},
+               {"fill_bytes": 1008, "fill_ranks": 3},
                {"cta_budget": 32, "fill_bytes": 12288, "fill_ranks": 5}):
         out = init.clone() if init is not None else torch.zeros(w.world, S, device="cuda")
         with tide.Plan(gs.views, tide.make_flags(**kw)) as plan:
