@@ -118,11 +118,11 @@ enum {
     TIDE_SCHED_STATIC = 0,   /* work item i goes to CTA i mod grid */
     TIDE_SCHED_DYNAMIC = 1,  /* CTAs claim items from a device counter that resets itself */
     TIDE_SCHED_PER_ITEM = 2  /* one short-lived CTA per work item (the grid is the work list; needs
-                                cta_budget 0).  Alone it runs as fast as the persistent grid; with
-                                the fold's stream at a lower priority than concurrent compute, the
-                                block scheduler hands SMs to the compute kernels as fold CTAs
-                                retire, so the fold yields without a fixed CTA budget (Section 2.2's
-                                SM interference) */
+                                cta_budget 0), as the placement kernel always launches.  Alone it
+                                runs about as fast as the persistent grid; with the plan's stream at
+                                a lower priority than concurrent compute, the block scheduler hands
+                                SMs to the compute kernels as these CTAs retire, so the fold yields
+                                without a fixed CTA budget (Section 2.2's SM interference) */
 };
 
 /* Reduce-scatter kernel family. */
@@ -135,7 +135,8 @@ enum {
 
 /* All-gather placement engines. */
 enum {
-    TIDE_AG_SM = 0,      /* placement kernel: 16-byte vector copies per (parameter, rank) piece */
+    TIDE_AG_SM = 0,      /* placement kernel: 16-byte vector copies per (parameter, rank) piece,
+                            one short CTA per 16,384-element work item */
     TIDE_AG_CE_2D = 1,   /* copy engines: one 2D copy per parameter over its full-shard ranks
                             (source pitch = slot stride, destination pitch = R_p K_p) + 1 tail copy;
                             pieces of 1 MiB or more are copied one by one instead, and large 2D
