@@ -27,3 +27,27 @@ def test_cpu_oracle_all_cores_matches_single_thread(accumulate):
     rec = bench.cpu_oracle_all_cores(w, host, min_seconds=0.0, max_reps=1, names=names)
     assert rec["matches_single_thread"] and rec["cores"] >= 1 and rec["value"] > 0
     assert "windows" in rec["sample"]
+
+
+def test_cpu_ranges_and_model():
+    import bench
+    assert bench.cpu_ranges({0, 1, 2, 3, 5, 7, 8, 9}) == "0-3,5,7-9"
+    assert bench.cpu_ranges({4}) == "4"
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+def test_profile_readers_follow_the_kernel_source():
+    """The committed traffic and SM-time summaries are reported while their
+    recorded digest matches the fold source (comments excluded), and not at
+    all once the source has changed."""
+    import bench
+    digest = bench.kernel_digest()
+    traffic, sm_time = bench.profile_traffic("llama3.1_8b_block"), bench.profile_sm_time("llama3.1_8b_block")
+    for name, value in (("rs_fold_llama3.1_8b_block_traffic.txt", traffic),
+                        ("sm_time_llama3.1_8b_block.txt", sm_time)):
+        recorded = (bench._profile_kv(name) or {}).get("rs_fold_cu_sha256_16")
+        assert (value is not None) == (recorded == digest), name
+    if traffic is not None:
+        assert 4.0e9 < traffic < 5.0e9  # algorithmic bytes per launch: 4.36 GB
+    if sm_time is not None:
+        assert sm_time["ratio"] > 10
