@@ -27,7 +27,7 @@ from ._binding import (  # noqa: F401  (re-exported C-ABI names)
     tide_last_error, tide_launch_count, tide_plan_build, tide_plan_destroy, tide_plan_fold_config,
     tide_plan_num_segments, tide_plan_rebind, tide_plan_segment, tide_plan_slot_numel, tide_rs_fold,
     tide_rs_fold_noalloc, tide_status_string, tide_latin_square_gpu, tide_rs_wave_plan, tide_rs_wave_zero_mask,
-    tide_bruck_schedule, tide_sm_probe, tide_sm_probe_max_clusters, pointer_array)
+    tide_bruck_schedule, tide_sm_probe, tide_sm_probe_max_clusters, tide_corun_cta_budget, pointer_array)
 
 AG_MODES = {"sm": TIDE_AG_SM, "ce2d": TIDE_AG_CE_2D, "ce1d": TIDE_AG_CE_1D}
 

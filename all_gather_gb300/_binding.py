@@ -36,7 +36,8 @@ EXPORTED = ("tide_plan_build", "tide_plan_rebind", "tide_rs_fold", "tide_ag_plac
             "tide_plan_slot_numel", "tide_plan_num_segments", "tide_plan_segment", "tide_plan_fold_config",
             "tide_last_device_status", "tide_launch_count", "tide_status_string", "tide_last_error",
             "tide_rs_fold_noalloc", "tide_ag_place_f32", "tide_latin_square_gpu", "tide_rs_wave_plan",
-            "tide_rs_wave_zero_mask", "tide_bruck_schedule", "tide_sm_probe", "tide_sm_probe_max_clusters")
+            "tide_rs_wave_zero_mask", "tide_bruck_schedule", "tide_sm_probe", "tide_sm_probe_max_clusters",
+            "tide_corun_cta_budget")
 
 
 class WavePlan(ctypes.Structure):
@@ -125,6 +126,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tide_sm_probe.restype = st
     lib.tide_sm_probe_max_clusters.argtypes = [i32, i32]
     lib.tide_sm_probe_max_clusters.restype = i32
+    lib.tide_corun_cta_budget.argtypes = [i32, i32, i32]
+    lib.tide_corun_cta_budget.restype = i32
     _lib = lib
     return lib
 
@@ -301,3 +304,7 @@ def tide_sm_probe(ctas: int, cluster: int, smem_bytes: int, hold_ns: int, smid: 
 
 def tide_sm_probe_max_clusters(cluster: int, smem_bytes: int) -> int:
     return int(load_library().tide_sm_probe_max_clusters(cluster, smem_bytes))
+
+
+def tide_corun_cta_budget(cluster_slots: int, gemm_ctas: int, cluster: int) -> int:
+    return int(load_library().tide_corun_cta_budget(cluster_slots, gemm_ctas, cluster))

@@ -2,9 +2,10 @@
 // shard of parameter p sits in the rank-major input at slot r, offset o_p; its
 // v_{p,r} real rows land at rows [r R_p, r R_p + v_{p,r}) of the full tensor,
 // which is the contiguous element range starting at r R_p K_p.  Padding rows
-// are never read.  A pure HBM copy: one persistent grid walks (piece, chunk)
-// work items and moves 16-byte vectors when source and destination share
-// their alignment phase.
+// are never read.  A pure HBM copy: one short CTA per (piece, chunk) work
+// item moves 16-byte vectors.  When source and destination differ in 16-byte
+// phase, each aligned 16-byte store is assembled from the two aligned source
+// vectors that cover its eight elements (a shift by the phase difference).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -23,6 +24,75 @@ __device__ __forceinline__ uint4 ld_once_v4(const uint16_t *p)
 }
 
 constexpr int kAgUnroll = 8;  // 16-byte vectors in flight per thread: enough to cover HBM latency
+
+// Eight bf16 values starting `sh` (1..7) halfwords into the 32 bytes a, b
+// (two consecutive aligned source vectors): output word m is the 32 bits
+// starting sh halfwords past word m of the pair.  sh is uniform across the
+// CTA, so the switch does not diverge and every word index is a constant.
+__device__ __forceinline__ uint4 shift_halfwords(const uint4 &a, const uint4 &b, int sh)
+{
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+    switch (sh) {
+#define TIDE_SHIFT_CASE(S)                                                                     \
+    case S:                                                                                    \
+        _Pragma("unroll") for (int m = 0; m < 4; ++m) o[m] =                                   \
+            (S & 1) ? __byte_perm(w[S / 2 + m], w[S / 2 + m + 1], 0x5432) : w[S / 2 + m];      \
+        break;
+        TIDE_SHIFT_CASE(1)
+        TIDE_SHIFT_CASE(2)
+        TIDE_SHIFT_CASE(3)
+        TIDE_SHIFT_CASE(4)
+        TIDE_SHIFT_CASE(5)
+        TIDE_SHIFT_CASE(6)
+        default:
+        TIDE_SHIFT_CASE(7)
+#undef TIDE_SHIFT_CASE
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Copy `count` bf16 elements when source and destination differ in 16-byte
+// phase.  After the destination's head, destination vector v takes source
+// elements [8v, 8v + 8) past the head, which straddle the aligned source
+// vectors a_v and a_{v+1}; both are loaded (each aligned 16-byte load holds at
+// least one element of the range, so it stays inside the source's pages) and
+// shifted into place.  Heads and tails: batched scalar loads, then stores.
+template <int NT>
+__device__ __forceinline__ void place_shifted(const uint16_t *src, uint16_t *dst, int64_t count, int tid)
+{
+    const uintptr_t da = reinterpret_cast<uintptr_t>(dst);
+    int64_t h = int64_t(((16u - (da & 15u)) & 15u) >> 1);
+    if (h > count)
+        h = count;
+    const int64_t nv = (count - h) >> 3;
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src + h);
+    const uint16_t *sa = reinterpret_cast<const uint16_t *>(s0 & ~uintptr_t(15));
+    const int sh = int((s0 & 15u) >> 1);  // nonzero: the phases differ
+    uint4 *d8 = reinterpret_cast<uint4 *>(dst + h);
+    constexpr int U = 1;  // one pair of source vectors per thread per pass: keeps the kernel at 4 CTAs per SM
+    for (int64_t v = tid; v < nv; v += int64_t(NT) * U) {
+        uint4 a[U], b[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const int64_t vj = v + int64_t(j) * NT;
+            if (vj < nv) {
+                a[j] = ld_once_v4(sa + vj * 8);
+                b[j] = ld_once_v4(sa + vj * 8 + 8);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const int64_t vj = v + int64_t(j) * NT;
+            if (vj < nv)
+                d8[vj] = shift_halfwords(a[j], b[j], sh);
+        }
+    }
+    // head [0, h) and tail [h + 8 nv, count): at most 14 elements
+    const int64_t e = tid < h ? tid : h + nv * 8 + (tid - h);
+    if (tid < 16 && e < count)
+        dst[e] = src[e];
+}
 
 template <int NP>
 __global__ void __launch_bounds__(kAgThreads) ag_place_kernel(const __grid_constant__ AgParamsT<NP> ap)
@@ -63,8 +133,7 @@ __global__ void __launch_bounds__(kAgThreads) ag_place_kernel(const __grid_const
             for (int64_t e = h + nv * 8 + tid; e < count; e += NT)
                 dst[e] = src[e];
         } else {
-            for (int64_t e = tid; e < count; e += NT)
-                dst[e] = src[e];
+            place_shifted<NT>(src, dst, count, tid);
         }
     }
 }
@@ -127,8 +196,24 @@ __global__ void __launch_bounds__(kAgThreads) ag_cast_kernel(const __grid_consta
             for (int64_t e = h + nv * 8 + tid; e < count; e += NT)
                 dst[e] = to_bf16_bits(src[e]);
         } else {
-            for (int64_t e = tid; e < count; e += NT)
-                dst[e] = to_bf16_bits(src[e]);
+            // Phases differ: coalesced scalar loads, eight in flight per
+            // thread before their stores.
+            constexpr int B = 2;
+            for (int64_t e = tid; e < count; e += int64_t(NT) * B) {
+                float x[B];
+#pragma unroll
+                for (int j = 0; j < B; ++j) {
+                    const int64_t ej = e + int64_t(j) * NT;
+                    if (ej < count)
+                        x[j] = __ldcs(src + ej);
+                }
+#pragma unroll
+                for (int j = 0; j < B; ++j) {
+                    const int64_t ej = e + int64_t(j) * NT;
+                    if (ej < count)
+                        dst[ej] = to_bf16_bits(x[j]);
+                }
+            }
         }
     }
 }

@@ -113,4 +113,18 @@ int32_t tide_sm_probe_max_clusters(int32_t cluster, int32_t smem_bytes)
     return n;
 }
 
+// Section 2.2, Equation (4): n_gemm GEMM clusters on n_slot - n_blk free
+// slots take ceil(n_gemm / (n_slot - n_blk)) waves.  The GEMM keeps one wave
+// while the fold blocks at most n_slot - n_gemm slots; a fold CTA that has an
+// SM to itself fills one SM of a slot, so that many whole slots hold
+// (n_slot - n_gemm) * cluster fold CTAs.
+int32_t tide_corun_cta_budget(int32_t cluster_slots, int32_t gemm_ctas, int32_t cluster)
+{
+    if (cluster_slots < 1 || gemm_ctas < 1 || cluster < 1 || cluster > 16)
+        return -1;
+    const int64_t n_gemm = (int64_t(gemm_ctas) + cluster - 1) / cluster;
+    const int64_t spare = int64_t(cluster_slots) - n_gemm;
+    return spare > 0 ? int32_t(spare * cluster) : 0;
+}
+
 }  // extern "C"

@@ -399,12 +399,19 @@ __device__ __forceinline__ uint4 lds_v4(const uint16_t *p)
     return *reinterpret_cast<const uint4 *>(p);
 }
 
+// Dynamic schedule of the bulk kernel: the producer lane claims work items
+// from a device counter and hands them to the consumer warps through a queue
+// of kItemQueue slots (item index, or -1 when the list is exhausted), each
+// guarded by a "posted" and a "taken" mbarrier.
+constexpr int kItemQueue = 8;
+
 // Shared-memory layout of the bulk kernel: STAGES full + STAGES empty
-// mbarriers, the abort flag, the producer's W source pointers, then the
-// 128-byte aligned stage ring.
+// mbarriers, the abort flag, the item queue (posted and taken mbarriers,
+// item slots), the producer's W source pointers, then the 128-byte aligned
+// stage ring.
 __host__ __device__ constexpr size_t bulk_ring_offset(int stages, int world)
 {
-    return ((size_t(2 * stages + 1) * 8 + size_t(world) * 8 + 127) / 128) * 128;
+    return ((size_t(2 * stages + 1 + 3 * kItemQueue) * 8 + size_t(world) * 8 + 127) / 128) * 128;
 }
 
 constexpr int kBulkMaxVec = 2;                               // vectors per consumer thread per chunk
@@ -448,6 +455,17 @@ template <>
 __device__ __forceinline__ float ld_elem<float>(const float *p)
 {
     return __ldg(p);
+}
+
+// Elements of a work item before its first 16-byte aligned source element,
+// given the phase (elements past the last 16-byte boundary) that every
+// rank's row shares at the item's start; at most `count`.
+template <typename E>
+__device__ __forceinline__ int64_t aligned_head(int32_t phase, int64_t count)
+{
+    constexpr int VE = 16 / int(sizeof(E));
+    const int64_t h = (VE - phase) & (VE - 1);
+    return h < count ? h : count;
 }
 
 // One element from global memory (pieces or tails the producer does not
@@ -690,15 +708,23 @@ __global__ void __launch_bounds__(32 * (1 + CW), CW == kBulkConsumerWarps ? 2 : 
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + STAGES;
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(empty + STAGES);
-    const E **src_cache = reinterpret_cast<const E **>(empty + STAGES + 1);  // producer's W pointers, in order
+    uint64_t *q_posted = empty + STAGES + 1;
+    uint64_t *q_taken = q_posted + kItemQueue;
+    volatile int64_t *q_item = reinterpret_cast<volatile int64_t *>(q_taken + kItemQueue);
+    const E **src_cache = reinterpret_cast<const E **>(q_taken + 2 * kItemQueue);  // producer's W pointers, in order
     E *ring = reinterpret_cast<E *>(smem + bulk_ring_offset(STAGES, W));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float alpha = fp.alpha;
+    const bool dyn = fp.sched == TIDE_SCHED_DYNAMIC;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], CW);
+        }
+        for (int s = 0; s < kItemQueue; ++s) {
+            mbar_init(&q_posted[s], 1);
+            mbar_init(&q_taken[s], CW);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -715,14 +741,36 @@ __global__ void __launch_bounds__(32 * (1 + CW), CW == kBulkConsumerWarps ? 2 : 
         int64_t fills = 0, skipped = -1;
         bool stop = false;
         const uint64_t policy = TIDE_BULK_L2_EVICT_FIRST ? evict_first_policy() : 0;
-        for (int64_t it = blockIdx.x; it < fp.n_items && !stop; it += gridDim.x) {
+        uint32_t qk = 0;  // item-queue position (dynamic schedule)
+        for (int64_t it = blockIdx.x; !stop; it += gridDim.x) {
+            if (dyn) {
+                // claim the next item and post it (or -1) to the consumers
+                const uint32_t qs = qk % kItemQueue, qpar = (qk / kItemQueue) & 1u;
+                if (!mbar_wait_bounded(&q_taken[qs], qpar ^ 1u, fp.wait_budget_ns, abort_flag)) {
+                    if (!*abort_flag)
+                        atomicExch(fp.status, kStatusProducerTimeout);
+                    *abort_flag = 1;
+                    break;
+                }
+                const int64_t t = int64_t(atomicAdd(fp.counters, 1u));
+                it = t < fp.n_items ? t : -1;
+                q_item[qs] = it;
+                mbar_arrive(&q_posted[qs]);
+                ++qk;
+                if (it < 0)
+                    break;
+            } else if (it >= fp.n_items) {
+                break;
+            }
             const Item item = fp.items[it];
             const Seg seg = fp.segs[item.seg];
-            if ((item.count_kind & kItemPad) || seg.src_phase != 0)
+            if ((item.count_kind & kItemPad) || seg.src_phase < 0)
                 continue;
-            const int64_t count = int64_t(item.count_kind & ~kItemPad);
+            const int64_t total = int64_t(item.count_kind & ~kItemPad);
+            const int64_t head = aligned_head<E>(seg.src_phase, total);  // the consumers fold these directly
+            const int64_t count = total - head;
             const uint64_t *bp = fp.ptrs + int64_t(seg.param) * W;
-            const int64_t base = seg.src_elem + item.begin;
+            const int64_t base = seg.src_elem + item.begin + head;
             for (int q = 0; q < W; ++q)
                 src_cache[q] = reinterpret_cast<const E *>(bp[seq_rank(fp.order, q, seg.rank, W, fp.node_size)]) + base;
             for (int64_t c = 0; c < count && !stop; c += FILL) {
@@ -766,6 +814,16 @@ __global__ void __launch_bounds__(32 * (1 + CW), CW == kBulkConsumerWarps ? 2 : 
             if (!mbar_wait_bounded(&full[s], par, fp.wait_budget_ns, nullptr))
                 atomicExch(fp.status, kStatusDrainTimeout);
         }
+        if (dyn) {
+            // The last CTA to finish claiming resets the counters for the
+            // next launch (every producer lane gets here, even after a timeout).
+            __threadfence();
+            const unsigned done = atomicAdd(fp.counters + 1, 1u);
+            if (done == gridDim.x - 1) {
+                atomicExch(fp.counters, 0u);
+                atomicExch(fp.counters + 1, 0u);
+            }
+        }
         return;
     }
 
@@ -776,24 +834,51 @@ __global__ void __launch_bounds__(32 * (1 + CW), CW == kBulkConsumerWarps ? 2 : 
     const int ctid = threadIdx.x - 32;
     constexpr int NCT = 32 * CW;
     uint32_t stage = 0, phase = 0;
-    for (int64_t it = blockIdx.x; it < fp.n_items; it += gridDim.x) {
+    uint32_t qk = 0;  // item-queue position (dynamic schedule)
+    for (int64_t it = blockIdx.x;; it += gridDim.x) {
+        if (dyn) {
+            const uint32_t qs = qk % kItemQueue, qpar = (qk / kItemQueue) & 1u;
+            if (!mbar_wait_bounded(&q_posted[qs], qpar, fp.wait_budget_ns, abort_flag)) {
+                if (!*abort_flag)
+                    atomicExch(fp.status, kStatusConsumerTimeout);
+                *abort_flag = 1;
+                return;
+            }
+            it = q_item[qs];
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&q_taken[qs]);
+            ++qk;
+            if (it < 0)
+                break;
+        } else if (it >= fp.n_items) {
+            break;
+        }
         const Item item = fp.items[it];
         const Seg seg = fp.segs[item.seg];
-        const int64_t count = int64_t(item.count_kind & ~kItemPad);
+        const int64_t total = int64_t(item.count_kind & ~kItemPad);
         const bool pad = (item.count_kind & kItemPad) != 0;
-        float *dst = fp.out + int64_t(seg.rank) * fp.stride + seg.dst_elem + (pad ? seg.n_valid : 0) + item.begin;
+        float *dst0 = fp.out + int64_t(seg.rank) * fp.stride + seg.dst_elem + (pad ? seg.n_valid : 0) + item.begin;
         const uint64_t *bp = fp.ptrs + int64_t(seg.param) * W;
         if (pad) {
             const float y = __fmul_rn(alpha, 0.0f);
-            for (int64_t e = ctid; e < count; e += NCT)
-                __stcs(dst + e, ACC ? __fadd_rn(dst[e], y) : y);
+            for (int64_t e = ctid; e < total; e += NCT)
+                __stcs(dst0 + e, ACC ? __fadd_rn(dst0[e], y) : y);
             continue;
         }
-        if (seg.src_phase != 0) {
-            for (int64_t e = ctid; e < count; e += NCT)
-                fold_scalar_global<ACC, E>(bp, fp, seg.rank, seg.src_elem + item.begin + e, dst + e);
+        if (seg.src_phase < 0) {  // the ranks' rows differ in 16-byte phase: no bulk copies
+            for (int64_t e = ctid; e < total; e += NCT)
+                fold_scalar_global<ACC, E>(bp, fp, seg.rank, seg.src_elem + item.begin + e, dst0 + e);
             continue;
         }
+        // Every rank's row shares one phase: the elements before the first
+        // 16-byte boundary are folded from global memory, the rest is staged.
+        const int64_t head = aligned_head<E>(seg.src_phase, total);
+        for (int64_t e = ctid; e < head; e += NCT)
+            fold_scalar_global<ACC, E>(bp, fp, seg.rank, seg.src_elem + item.begin + e, dst0 + e);
+        const int64_t count = total - head;
+        const int64_t src_at = seg.src_elem + item.begin + head;
+        float *dst = dst0 + head;
         const bool dst_vec = (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
         for (int64_t c = 0; c < count; c += FILL) {
             const int64_t len = count - c < FILL ? count - c : FILL;
@@ -922,7 +1007,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), CW == kBulkConsumerWarps ? 2 : 
                     store8_onto<ACC>(dst + c + v * 8, acc[k], old[k], alpha, dst_vec);
             }
             for (int64_t e = nv * 8 + ctid; e < len; e += NCT)
-                fold_scalar_global<ACC, E>(bp, fp, seg.rank, seg.src_elem + item.begin + c + e, dst + c + e);
+                fold_scalar_global<ACC, E>(bp, fp, seg.rank, src_at + c + e, dst + c + e);
         }
     }
 }

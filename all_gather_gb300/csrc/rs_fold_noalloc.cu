@@ -21,9 +21,15 @@
 //     that overlap on the GPU (for example on two streams without ordering
 //     between them) race and may read each other's tables.  Calls on one
 //     stream are ordered and safe.
-// The first call on each device looks up the array's device address
-// (cudaGetSymbolAddress) with that device current; make that first call
-// before any stream capture.
+// The first call on each device (an empty one, with no parameters, will do)
+// looks up the array's device address (cudaGetSymbolAddress) with that
+// device current and loads the fold kernels; make that first call before any
+// stream capture, outside the context that cannot allocate.
+//
+// The first 256 bytes of the array hold the status word of the bounded
+// device-side waits; the tables follow.  Uploads never touch the status
+// word: an expired wait stays recorded until tide_last_device_status(NULL,
+// stream) reads and clears it on the current device.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -47,7 +53,9 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 // Host copy of the same tables, built in place so the call needs no heap.
 alignas(256) unsigned char g_host_tables[kScratchBytes];
 void *g_scratch_dev[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
 std::mutex g_lock;
+constexpr size_t kStatusBytes = 256;  // the status word's slot at the start of the array
 
 // Record the detail that tide_last_error() reports, without heap use.
 tide_status_t noalloc_fail(tide_status_t st, const char *fmt, ...)
@@ -63,7 +71,43 @@ tide_status_t noalloc_fail(tide_status_t st, const char *fmt, ...)
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Once per device, with it current (caller holds g_lock): the array's device
+// address, the SM count, and the fold kernels' shared-memory attribute (which
+// loads both of them), so that later calls load and look up nothing.
+tide_status_t noalloc_setup(int dev)
+{
+    if (g_scratch_dev[dev])
+        return TIDE_OK;
+    void *addr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+    if (e != cudaSuccess || !addr)
+        return noalloc_fail(TIDE_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) {
+        const tide::BulkShape bs = tide::bulk_shape(8, 0, 0, false, 2);
+        e = tide::fold_occupancy(TIDE_KERNEL_BULK, 8, tide::kBulkThreads, bs.smem_bytes, &per_sm);
+    }
+    if (e != cudaSuccess)
+        return noalloc_fail(TIDE_ERR_CUDA, "set-up: %s", cudaGetErrorString(e));
+    g_sms[dev] = sms;
+    g_scratch_dev[dev] = addr;
+    return TIDE_OK;
+}
+
 }  // namespace
+
+namespace tide {
+// Device address of the allocation-free fold's status word on device `dev`,
+// or NULL if that entry point has not been set up on it.
+int32_t *noalloc_status_word(int dev)
+{
+    std::lock_guard<std::mutex> guard(g_lock);
+    if (dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    return static_cast<int32_t *>(g_scratch_dev[dev]);
+}
+}  // namespace tide
 
 extern "C" tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params, const tide_param_desc_t *params,
                                               float *out_base, int64_t out_slot_stride, float alpha,
@@ -103,11 +147,10 @@ extern "C" tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params,
         }
     }
     const size_t n_pieces = size_t(num_params) * size_t(world);
-    const size_t o_ptrs = 0;
+    const size_t o_ptrs = kStatusBytes;
     const size_t o_segs = o_ptrs + round256(n_pieces * sizeof(uint64_t));
     const size_t o_items = o_segs + round256(n_pieces * sizeof(tide::Seg));
-    const size_t o_status = o_items + round256(size_t(n_items) * sizeof(tide::Item));
-    const size_t total = o_status + 256;
+    const size_t total = o_items + round256(size_t(n_items) * sizeof(tide::Item));
     if (total > kScratchBytes)
         return noalloc_fail(TIDE_ERR_INVALID_ARG,
                             "the call needs %zu bytes of tables; the allocation-free entry point holds %zu "
@@ -116,6 +159,17 @@ extern "C" tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params,
     if (out_slot_stride < S)
         return noalloc_fail(TIDE_ERR_INVALID_ARG, "out_slot_stride %lld < S %lld", (long long)out_slot_stride,
                             (long long)S);
+
+    std::lock_guard<std::mutex> guard(g_lock);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return noalloc_fail(TIDE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices)
+        return noalloc_fail(TIDE_ERR_UNSUPPORTED, "device %d beyond %d", dev, kMaxDevices);
+    const tide_status_t st = noalloc_setup(dev);  // before the early return: an empty call sets up the device
+    if (st != TIDE_OK)
+        return st;
     if (n_items == 0)
         return TIDE_OK;
     if (!out_base)
@@ -127,27 +181,12 @@ extern "C" tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params,
     const uintptr_t out_lo = reinterpret_cast<uintptr_t>(out_base);
     const uintptr_t out_hi = out_lo + uintptr_t((world - 1) * out_slot_stride + S) * 4u;
 
-    std::lock_guard<std::mutex> guard(g_lock);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return noalloc_fail(TIDE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices)
-        return noalloc_fail(TIDE_ERR_UNSUPPORTED, "device %d beyond %d", dev, kMaxDevices);
-    if (!g_scratch_dev[dev]) {  // once per device, with that device current
-        void *addr = nullptr;
-        e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
-        if (e != cudaSuccess || !addr)
-            return noalloc_fail(TIDE_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-        g_scratch_dev[dev] = addr;
-    }
     unsigned char *scratch = static_cast<unsigned char *>(g_scratch_dev[dev]);
 
     // Pass 2: fill the host tables (pointers, pieces, work items).
     auto *ptrs = reinterpret_cast<uint64_t *>(g_host_tables + o_ptrs);
     auto *segs = reinterpret_cast<tide::Seg *>(g_host_tables + o_segs);
     auto *items = reinterpret_cast<tide::Item *>(g_host_tables + o_items);
-    std::memset(g_host_tables + o_status, 0, 256);
     running = 0;
     int64_t it = 0;
     for (int32_t p = 0; p < num_params; ++p) {
@@ -198,7 +237,8 @@ extern "C" tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params,
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     // From pageable host memory: the call returns once the bytes have left
     // g_host_tables, so the next call may rewrite it.
-    e = cudaMemcpyAsync(scratch, g_host_tables, total, cudaMemcpyHostToDevice, stream);
+    // The status word's slot (the first kStatusBytes) is not part of the upload.
+    e = cudaMemcpyAsync(scratch + o_ptrs, g_host_tables + o_ptrs, total - o_ptrs, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess)
         return noalloc_fail(TIDE_ERR_CUDA, "table upload: %s", cudaGetErrorString(e));
 
@@ -213,7 +253,7 @@ extern "C" tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params,
     fp.world = world;
     fp.sched = TIDE_SCHED_STATIC;
     fp.counters = nullptr;
-    fp.status = reinterpret_cast<int32_t *>(scratch + o_status);
+    fp.status = reinterpret_cast<int32_t *>(scratch);
     fp.wait_budget_ns = tide::kWaitBudgetNs;
     fp.order = TIDE_ORDER_RANK_ASC;
     fp.node_size = 0;
@@ -224,10 +264,9 @@ extern "C" tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params,
     fp.fill_ranks = bs.fill_ranks;
     fp.stages = bs.stages;
     fp.consumer_warps = tide::kBulkConsumerWarps;
-    int per_sm = 0, sms = 0;
+    int per_sm = 0;
+    const int sms = g_sms[dev];
     e = tide::fold_occupancy(TIDE_KERNEL_BULK, world, tide::kBulkThreads, bs.smem_bytes, &per_sm);
-    if (e == cudaSuccess)
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
         return noalloc_fail(TIDE_ERR_CUDA, "launch geometry: %s", cudaGetErrorString(e));
     const int grid = int(std::min<int64_t>(int64_t(std::max(per_sm, 1)) * sms, n_items));

@@ -53,7 +53,7 @@ struct Seg {
     int64_t n_pad;
     int32_t param;
     int32_t rank;
-    int32_t src_phase;  // (address / 2) mod 8 of every rank's first element, -1 if ranks differ
+    int32_t src_phase;  // (address / element size) mod (16 / element size) of every rank's first element, -1 if ranks differ
     int32_t pad_;
 };
 static_assert(sizeof(Seg) == 48, "Seg layout");
@@ -143,6 +143,10 @@ cudaError_t launch_ag(const AgParams &ap, int grid, cudaStream_t stream);
 cudaError_t launch_ag_f32(const AgParams &ap, int grid, cudaStream_t stream);
 
 extern std::atomic<uint64_t> g_launches;
+
+// Device address of the allocation-free fold's status word on device `dev`
+// (rs_fold_noalloc.cu), or NULL before that entry point's first call there.
+int32_t *noalloc_status_word(int dev);
 
 // Set the detail message tide_last_error() returns on this thread.  The
 // message is copied into a fixed per-thread buffer, so callers may rely on

@@ -113,14 +113,10 @@ tide_status_t check_flags(const tide_plan_flags_t &f)
         return fail(TIDE_ERR_INVALID_ARG, "flags.kernel %d", f.kernel);
     if (f.grad_dtype != TIDE_DTYPE_BF16 && f.grad_dtype != TIDE_DTYPE_F32)
         return fail(TIDE_ERR_UNSUPPORTED, "flags.grad_dtype %d is not implemented", f.grad_dtype);
-    if ((f.order != TIDE_ORDER_RANK_ASC || f.grad_dtype != TIDE_DTYPE_BF16) &&
-        (f.kernel == TIDE_KERNEL_DIRECT || f.sched == TIDE_SCHED_DYNAMIC))
-        return fail(TIDE_ERR_UNSUPPORTED,
-                    "orders other than rank order and fp32 gradients run on the statically scheduled bulk kernel");
+    if ((f.order != TIDE_ORDER_RANK_ASC || f.grad_dtype != TIDE_DTYPE_BF16) && f.kernel == TIDE_KERNEL_DIRECT)
+        return fail(TIDE_ERR_UNSUPPORTED, "orders other than rank order and fp32 gradients run on the bulk kernel");
     if (f.debug & ~(TIDE_DEBUG_HOST_ONLY | TIDE_DEBUG_SHORT_WAIT | TIDE_DEBUG_SKIP_FILL))
         return fail(TIDE_ERR_INVALID_ARG, "unknown debug bits 0x%x", f.debug);
-    if (f.kernel == TIDE_KERNEL_BULK && f.sched == TIDE_SCHED_DYNAMIC)
-        return fail(TIDE_ERR_UNSUPPORTED, "the bulk-copy kernel schedules statically only");
     if ((f.debug & TIDE_DEBUG_SKIP_FILL) && f.kernel != TIDE_KERNEL_BULK)
         return fail(TIDE_ERR_INVALID_ARG, "TIDE_DEBUG_SKIP_FILL applies to the bulk-copy kernel only");
     return TIDE_OK;
@@ -321,8 +317,6 @@ static tide_status_t plan_build_impl(int32_t world, int32_t num_params, const ti
                              "tree order: %d full stage fills of %d ranks per chunk (at most %d); raise fill_ranks",
                              world / bs.fill_ranks, bs.fill_ranks, (1 << tide::kTreeLevels) - 1));
     }
-    if (f.kernel == TIDE_KERNEL_AUTO && f.sched == TIDE_SCHED_DYNAMIC)
-        plan->kernel = TIDE_KERNEL_DIRECT;  // only the direct kernel claims items dynamically
 
     // --- geometry (Section 2.1): R_p = ceil(D_p / W), o_p, S -------------
     plan->dim0.resize(num_params);
@@ -876,19 +870,29 @@ tide_status_t tide_plan_fold_config(const tide_plan_t *plan, int32_t *grid, int3
 tide_status_t tide_last_device_status(tide_plan_t *plan, void *stream_)
 {
     t_last_error[0] = '\0';
-    if (!plan)
-        return fail(TIDE_ERR_INVALID_ARG, "plan is NULL");
-    if (plan->host_only)
-        return TIDE_OK;
+    int32_t *status = nullptr;
+    if (plan) {
+        if (plan->host_only)
+            return TIDE_OK;
+        status = plan->d_status;
+    } else {  // the allocation-free fold's status word on the current device
+        int dev = -1;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetDevice");
+        status = tide::noalloc_status_word(dev);
+        if (!status)
+            return TIDE_OK;  // that entry point never ran on this device
+    }
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     int32_t word = 0;
-    cudaError_t e = cudaMemcpyAsync(&word, plan->d_status, sizeof word, cudaMemcpyDeviceToHost, stream);
+    cudaError_t e = cudaMemcpyAsync(&word, status, sizeof word, cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess)
         e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "read device status");
     if (word != 0) {
-        e = cudaMemsetAsync(plan->d_status, 0, sizeof(int32_t), stream);
+        e = cudaMemsetAsync(status, 0, sizeof(int32_t), stream);
         if (e != cudaSuccess)
             return cuda_fail(e, "clear device status");
         return fail(TIDE_ERR_TIMEOUT, "a bounded device wait expired (code %d)", word);

@@ -267,6 +267,74 @@ def sm_probe(workload: str = "llama3.1_8b_block", budgets=(0, 152, 64, 16), wind
     return res
 
 
+GEMM_CTAS, GEMM_CLUSTER = 128, 4  # the one-wave GEMM's launch: 32 four-CTA clusters of 213 KB CTAs
+
+
+def corun_budget() -> dict:
+    """The fold's CTA budget next to the one-wave GEMM on this device:
+    Equation (4)'s spare cluster slots (tide_corun_cta_budget) from the slots
+    the probe shape gets here (tide_sm_probe_max_clusters)."""
+    import all_gather_gb300 as tide
+    slots = tide.tide_sm_probe_max_clusters(GEMM_CLUSTER, PROBE_SMEM)
+    budget = tide.tide_corun_cta_budget(slots, GEMM_CTAS, GEMM_CLUSTER) if slots > 0 else -1
+    return {"cluster_slots": slots, "gemm_clusters": -(-GEMM_CTAS // GEMM_CLUSTER), "cta_budget": budget}
+
+
+def corun_target(workload: str, device: int = 0, grads=None, n_rs: int = 10, reps: int = 3) -> dict:
+    """One stated configuration against the two-pass baseline: the fused fold
+    at the co-run CTA budget (corun_budget) must finish at least 1.5x sooner
+    than the two-pass reduce-scatter and slow the one-wave GEMM less than the
+    two-pass reduce-scatter does, on streams of equal priority (Table 4's
+    method).  Each co-run is repeated `reps` times; the medians are reported."""
+    import torch
+
+    import all_gather_gb300 as tide
+    import workloads
+    from all_gather_gb300 import baselines
+
+    torch.cuda.set_device(device)
+    dev = torch.device("cuda", device)
+    w = workloads.get(workload)
+    gs = grads if grads is not None else workloads.make_grads(w, device=dev)
+    cb = corun_budget()
+    res = {"workload": w.name, "victim": "gemm_256x8192x8192 (bf16, one wave)", "priority": "equal", **cb}
+    if cb["cta_budget"] < 1:
+        res["met"] = False
+        res["why"] = "no spare cluster slot on this device: every resident fold CTA can displace GEMM CTAs"
+        return res
+    plans = {"fused_corun_budget": tide.Plan(gs.views, tide.make_flags(cta_budget=cb["cta_budget"])),
+             "fused_full_wave": tide.Plan(gs.views)}
+    S = plans["fused_full_wave"].slot_numel
+    out = torch.zeros(w.world, S, device=dev)
+    pack = torch.empty(w.world, w.world * S, device=dev)
+    arms = {name: (lambda p=p: p.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)) for name, p in plans.items()}
+    arms["two_pass_baseline"] = lambda: baselines.two_pass_rs(gs.views, pack, out, w.alpha, w.accumulate)
+    victim = _victims(dev)["gemm_256x8192x8192"]
+    quiet = torch.cuda.Stream()
+    gemm_alone = _time_alone(victim, 50, quiet)
+    rs_alone = {name: _time_alone(fn, 3, quiet) for name, fn in arms.items()}
+    slow, rs_co = {}, {}
+    for name, fn in arms.items():
+        runs = [_co_run(fn, n_rs, victim, gemm_alone, rs_alone[name]) for _ in range(reps)]
+        sd = [r["victim_ms"] / gemm_alone - 1.0 for r in runs if r["victim_ms"]]
+        slow[name] = round(statistics.median(sd), 4) if sd else None
+        rs_co[name] = round(statistics.median(r["rs_ms"] for r in runs), 4)
+    for p in plans.values():
+        p.close()
+    del pack, out
+    torch.cuda.empty_cache()
+    speedup = rs_alone["two_pass_baseline"] / rs_alone["fused_corun_budget"]
+    lower = (slow["fused_corun_budget"] is not None and slow["two_pass_baseline"] is not None
+             and slow["fused_corun_budget"] < slow["two_pass_baseline"])
+    res.update({"gemm_alone_ms": round(gemm_alone, 5), "rs_alone_ms": {k: round(v, 4) for k, v in rs_alone.items()},
+                "rs_ms_while_corunning": rs_co, "gemm_slowdown": slow,
+                "speedup_vs_two_pass": round(speedup, 3), "speedup_at_least_1_5x": bool(speedup >= 1.5),
+                "slowdown_below_two_pass": bool(lower), "met": bool(speedup >= 1.5 and lower),
+                "method": f"median of {reps} co-runs of {n_rs} reduce-scatters each; slowdown = median GEMM time "
+                          "fully inside the reduce-scatter window / GEMM alone - 1"})
+    return res
+
+
 def summarize(res: dict) -> dict:
     """victim -> {arm: slowdown} (equal stream priorities, and the victim on a
     higher-priority stream) plus the RS times per arm."""

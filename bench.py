@@ -1,18 +1,24 @@
-"""Benchmark of the layout-folded reduce-scatter + all-gather placement step.
+"""Benchmark of the layout-folded bf16 -> fp32 reduce-scatter fold and the
+all-gather placement.
 
 One step = one pass of the hot path over one gradient group: the fused
-bf16 -> fp32 reduce-scatter fold of W virtual ranks (tide_rs_fold) followed
-by the all-gather placement of W bf16 shard slots into the group's full
-parameter tensors (tide_ag_place).  Default workload: one Llama-3.1-8B
-decoder block, W = 8 (218,112,000 elements per gradient set).
+reduce-scatter fold of W virtual ranks (tide_rs_fold) followed by the
+all-gather placement of W bf16 shard slots into the group's full parameter
+tensors (tide_ag_place).  Default workload: the largest group that fits one
+GPU, one Qwen3-30B-A3B-style MoE layer with W = 32 (389 parameters,
+623,116,288 elements per gradient set, 42.37 GB of algorithmic reduce-scatter
+bytes).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints ONE JSON line (rank 0).  ``value`` is the whole-job effective
-bandwidth: algorithmic bytes of all steps on all GPUs / max-over-ranks time,
-with the RS fold counting W*N*2 read + N*4 written (+N*4 read when
-accumulating) and the placement N*2 read + N*2 written.  Inputs are larger
-than L2 (no flush needed); timing uses CUDA events on the launching stream.
+Prints ONE JSON line (rank 0).  ``value`` is the reduce-scatter's effective
+bandwidth, the metric: W*N*2 bytes read + N*4 written (+N*4 read when
+accumulating) per fold, summed over all GPUs, over the slowest rank's mean
+fold time (CUDA events around every fold of the timed steps).  The whole
+step (fold + placement, whose bytes are N*2 read + N*2 written) is reported
+under ``step``; ``per_config`` times the fold, the step and the two-pass
+baseline on all five workloads.  Inputs are larger than L2 (no flush
+needed); timing uses CUDA events on the launching stream.
 
 ``--impl reference`` times the CPU oracle (the plain two-pass definition) on
 a bounded sample of the same workload, on this host's cores.
@@ -34,8 +40,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fused bf16→fp32 reduce-scatter effective GB/s and % of GB300 HBM roofline"
 UNIT = "GB/s"
-DEFAULT_WORKLOAD = "llama3.1_8b_block"
-SAMPLE_PARAMS = ("q_proj", "k_proj", "v_proj", "o_proj")  # CPU sample: the attention projections
+DEFAULT_WORKLOAD = "qwen3_30b_a3b_moe_layer"
 
 
 ORDERS = {"rank": 0, "staged": 1, "nodes": 2, "tree": 3}
@@ -65,6 +70,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-interference", action="store_true", help="skip the concurrent-GEMM harness")
     ap.add_argument("--no-variants", action="store_true", help="skip timing the other placement variants")
+    ap.add_argument("--no-per-config", action="store_true", help="skip timing the five workloads one by one")
+    ap.add_argument("--interference-rs", type=int, default=10, help="reduce-scatters per interference co-run")
     return ap.parse_args()
 
 
@@ -316,41 +323,61 @@ def profile_traffic(workload: str):
 
 
 # ---------------------------------------------------------------------------
-def cpu_oracle_sample(w, host_grads=None, min_seconds=10.0, max_reps=50):
-    """Time the CPU oracle (reduce-scatter then placement) on the attention
-    projections of the workload.  host_grads[p][u]: uint16 arrays, or None to
-    generate them on the CPU with the same recipe."""
+def sample_params(w):
+    """The CPU sample of a workload: one parameter of each distinct shape, in
+    the group's order (every kind of tensor the group holds, each once)."""
+    seen, idx = set(), []
+    for p, shape in enumerate(w.shapes):
+        if shape not in seen:
+            seen.add(shape)
+            idx.append(p)
+    return idx
+
+
+def sample_text(w, idx) -> str:
+    numel = sum(w.numels()[i] for i in idx)
+    return (f"one parameter of each of the {len(idx)} distinct shapes of {w.name} "
+            f"({', '.join(w.names[i] for i in idx)}), all {w.world} ranks, {numel} elements per gradient set")
+
+
+def cpu_grads(w, idx):
+    """host_grads[j][u]: bf16 bits (uint16) of sample parameter idx[j] on rank u,
+    generated on the CPU with the same recipe as on the GPU."""
+    import numpy as np
+    import torch
+
+    import workloads
+    return [[workloads.normal_fp32(w.numels()[i], workloads.grad_seed(w, u, i), w.sigma, "cpu", w.outlier_rate,
+                                   w.outlier_scale).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+             for u in range(w.world)] for i in idx]
+
+
+def rs_alg_bytes(w, numel: int) -> int:
+    """The metric's bytes: W*N*2 read + N*4 written (+N*4 read when accumulating)."""
+    return alg_bytes(w, numel)[0]
+
+
+def cpu_oracle_sample(w, host_grads, idx, min_seconds=10.0, max_reps=50):
+    """Time the CPU oracle's reduce-scatter (the metric) on the sample
+    parameters, single-threaded.  host_grads[j][u]: uint16 bf16 bits."""
     import numpy as np
 
     import oracle
-    import workloads
-    idx = [w.names.index(n) for n in SAMPLE_PARAMS if n in w.names]
     dims_all = w.dim0_rownumel()
     dims = [dims_all[i] for i in idx]
-    if host_grads is None:
-        host_grads = []
-        for i in idx:
-            n = dims_all[i][0] * dims_all[i][1]
-            host_grads.append([workloads.normal_fp32(n, workloads.grad_seed(w, u, i), w.sigma, "cpu", w.outlier_rate,
-                                                     w.outlier_scale).to(__import__("torch").bfloat16)
-                               .view(__import__("torch").int16).numpy().view(np.uint16) for u in range(w.world)])
     orc = oracle.load()
     _, _, S = orc.geometry(w.world, dims)
     out = np.zeros((w.world, S), np.float32)
-    slots = np.random.default_rng(0).integers(0, 0x3F00, size=(w.world, S), dtype=np.uint16)
     numel = sum(d * k for d, k in dims)
-    rs_b, ag_b = alg_bytes(w, numel)
     reps, t0 = 0, time.perf_counter()
     while True:
         orc.rs(w.world, dims, host_grads, w.alpha, w.accumulate, out)
-        orc.ag(w.world, dims, slots)
         reps += 1
         el = time.perf_counter() - t0
         if el >= min_seconds or reps >= max_reps:
             break
-    return {"value": round((rs_b + ag_b) * reps / el / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{'+'.join(SAMPLE_PARAMS)} of {w.name}, all {w.world} ranks "
-                      f"({numel} elements per gradient set), reduce-scatter + placement, {reps} reps in {el:.1f} s"}
+    return {"value": round(rs_alg_bytes(w, numel) * reps / el / 1e9, 4), "unit": UNIT, "cores": 1,
+            "kind": "oracle", "sample": f"{sample_text(w, idx)}; reduce-scatter, {reps} reps in {el:.1f} s"}
 
 
 def cpu_model() -> str:
@@ -373,26 +400,24 @@ def cpu_model() -> str:
     return f"{name} (implementer {impl[0]} part {part[0]})" if name else f"implementer {impl[0]} part {part[0]}"
 
 
-def cpu_oracle_all_cores(w, host_grads, min_seconds=5.0, max_reps=50, names=SAMPLE_PARAMS):
+def cpu_oracle_all_cores(w, host_grads, idx, min_seconds=5.0, max_reps=50):
     """The same oracle sample on every core this process may use: the
-    unchanged oracle functions run on independent windows (slices of one
-    (parameter, rank) piece, at most 2^20 elements) and per-parameter
-    placements in a thread pool; ctypes releases the GIL inside each call."""
+    unchanged oracle function runs on independent windows (slices of one
+    (parameter, rank) piece, at most 2^20 elements) in a thread pool; ctypes
+    releases the GIL inside each call.  The windows are first checked to
+    reassemble the single-threaded result bit for bit."""
     import os
     from concurrent.futures import ThreadPoolExecutor
 
     import numpy as np
 
     import oracle
-    idx = [w.names.index(n) for n in names if n in w.names]
     dims_all = w.dim0_rownumel()
     dims = [dims_all[i] for i in idx]
     orc = oracle.load()
     W = w.world
     R, o, S = orc.geometry(W, dims)
     out = np.zeros((W, S), np.float32)
-    slots = np.random.default_rng(0).integers(0, 0x3F00, size=(W, S), dtype=np.uint16)
-    slot_parts = [np.ascontiguousarray(slots[:, o[p]:o[p] + R[p] * k]) for p, (_, k) in enumerate(dims)]
     jobs = []
     for p, (d, k) in enumerate(dims):
         for r in range(W):
@@ -409,14 +434,9 @@ def cpu_oracle_all_cores(w, host_grads, min_seconds=5.0, max_reps=50, names=SAMP
         old = dst[r, pos:pos + nv + npad] if w.accumulate else None
         dst[r, pos:pos + nv + npad] = orc.rs_window(srcs, nv, npad, w.alpha, w.accumulate, old)
 
-    def ag_job(p):
-        orc.ag(W, [dims[p]], slot_parts[p])
-
     threads = len(os.sched_getaffinity(0))
     numel = sum(d * k for d, k in dims)
-    rs_b, ag_b = alg_bytes(w, numel)
     with ThreadPoolExecutor(max_workers=threads) as pool:
-        # the windows must reassemble the single-threaded oracle's result exactly
         chk, want = np.zeros((W, S), np.float32), np.zeros((W, S), np.float32)
         list(pool.map(lambda j: rs_job(j, chk), jobs))
         orc.rs(W, dims, host_grads, w.alpha, w.accumulate, want)
@@ -426,44 +446,39 @@ def cpu_oracle_all_cores(w, host_grads, min_seconds=5.0, max_reps=50, names=SAMP
         reps, t0 = 0, time.perf_counter()
         while True:
             list(pool.map(lambda j: rs_job(j, out), jobs))
-            list(pool.map(ag_job, range(len(dims))))
             reps += 1
             el = time.perf_counter() - t0
             if el >= min_seconds or reps >= max_reps:
                 break
-    return {"value": round((rs_b + ag_b) * reps / el / 1e9, 4), "unit": UNIT, "cores": threads,
+    return {"value": round(rs_alg_bytes(w, numel) * reps / el / 1e9, 4), "unit": UNIT, "cores": threads,
             "cpu": cpu_model(), "matches_single_thread": True,
-            "sample": f"same sample, {len(jobs)} reduce-scatter windows + {len(dims)} "
-                      f"placements per rep over {threads} threads, {reps} reps in {el:.1f} s"}
+            "sample": f"same sample, {len(jobs)} reduce-scatter windows per rep over {threads} threads, "
+                      f"{reps} reps in {el:.1f} s"}
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle's reduce-scatter (the metric) on the
+    sample parameters of the same workload, single-threaded on this host, each
+    step one reduce-scatter of the sample."""
     world, rank, _ = dist_env()
     import workloads
     w = workloads.get(args.workload)
     if rank != 0:
         return 0
-    sample = None
     import numpy as np
 
     import oracle
-    idx = [w.names.index(n) for n in SAMPLE_PARAMS if n in w.names]
+    idx = sample_params(w)
     dims_all = w.dim0_rownumel()
     dims = [dims_all[i] for i in idx]
-    import torch
-    host = [[workloads.normal_fp32(dims_all[i][0] * dims_all[i][1], workloads.grad_seed(w, u, i), w.sigma, "cpu",
-                                   w.outlier_rate, w.outlier_scale).to(torch.bfloat16).view(torch.int16).numpy()
-             .view(np.uint16) for u in range(w.world)] for i in idx]
+    host = cpu_grads(w, idx)
     orc = oracle.load()
     _, _, S = orc.geometry(w.world, dims)
     out = np.zeros((w.world, S), np.float32)
-    slots = np.random.default_rng(0).integers(0, 0x3F00, size=(w.world, S), dtype=np.uint16)
     numel = sum(d * k for d, k in dims)
-    rs_b, ag_b = alg_bytes(w, numel)
 
     def step():
         orc.rs(w.world, dims, host, w.alpha, w.accumulate, out)
-        orc.ag(w.world, dims, slots)
 
     for _ in range(args.warmup):
         step()
@@ -471,20 +486,108 @@ def run_reference(args):
     for _ in range(args.steps):
         step()
     el = time.perf_counter() - t0
-    value = (rs_b + ag_b) * args.steps / el / 1e9
-    sample = (f"{'+'.join(SAMPLE_PARAMS)} of {w.name}, all {w.world} ranks ({numel} elements per gradient set), "
-              f"reduce-scatter + placement per step")
+    value = rs_alg_bytes(w, numel) * args.steps / el / 1e9
+    sample = f"{sample_text(w, idx)}; one reduce-scatter per step"
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": {"workload": w.name, "world": w.world, "sample": sample},
-            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+                             "cpu": cpu_model()},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
 # ---------------------------------------------------------------------------
+def pct(xs, q):
+    ys = sorted(xs)
+    return round(ys[min(len(ys) - 1, int(q * len(ys)))], 4)
+
+
+def thirds(xs):
+    """Medians of the first, middle and last third of the timed steps, the
+    median of those, and their spread (max - min) relative to it: drift or a
+    co-tenant on the shared GPU shows up here."""
+    n = len(xs) // 3
+    if n < 1:
+        return None
+    meds = [pct(xs[i * n:(i + 1) * n], 0.5) for i in range(3)]
+    mid = sorted(meds)[1]
+    return {"medians_ms": meds, "median_of_medians_ms": mid,
+            "spread_pct": round(100.0 * (max(meds) - min(meds)) / mid, 2) if mid > 0 else None}
+
+
+def timed_steps(plan, w, out, slots, full_b, ag_mode, K, stream):
+    """K steps of fold + placement with CUDA events around each part; returns
+    per-step fold and placement times (ms) and the whole region's time."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
+        ev[i][1].record(stream)
+        plan.ag_place(slots, full_b, mode=ag_mode)
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    rs_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    ag_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    return rs_ms, ag_ms, start.elapsed_time(end)
+
+
+def fold_record(w, rs_ms, peak):
+    numel = w.total_numel()
+    rs_b = rs_alg_bytes(w, numel)
+    mean = sum(rs_ms) / len(rs_ms)
+    gbs = rs_b / (mean * 1e-3) / 1e9
+    return {"ms": round(mean, 4), "gbs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+            "frac_of_8tbs_nominal": round(gbs / 8000.0, 4), "alg_bytes": rs_b, "p10_ms": pct(rs_ms, 0.1),
+            "p50_ms": pct(rs_ms, 0.5), "p90_ms": pct(rs_ms, 0.9), "thirds": thirds(rs_ms)}
+
+
+def measure_config(w, dev, steps, peak, gs=None, baseline=True):
+    """Fold, placement and step times of one workload in the benchmark's launch
+    configuration (default flags, SM placement), plus the two-pass baseline's
+    reduce-scatter.  Builds (and frees) the workload's inputs unless given."""
+    import torch
+
+    import all_gather_gb300 as tide
+    import workloads
+    from all_gather_gb300 import baselines
+    own = gs is None
+    gs = workloads.make_grads(w, device=dev) if own else gs
+    plan = tide.Plan(gs.views)
+    S = plan.slot_numel
+    out = workloads.make_out_init(w, S, device=dev) if w.accumulate else torch.zeros(w.world, S, device=dev)
+    slots = workloads.make_slots(w, S, device=dev)
+    full = [torch.empty(s, dtype=torch.bfloat16, device=dev) for s in w.shapes]
+    full_b = plan.bind_full(full)
+    stream = torch.cuda.current_stream()
+    timed_steps(plan, w, out, slots, full_b, "sm", 3, stream)
+    rs_ms, ag_ms, total = timed_steps(plan, w, out, slots, full_b, "sm", steps, stream)
+    numel = w.total_numel()
+    rs_b, ag_b = alg_bytes(w, numel)
+    ag_mean = sum(ag_ms) / steps
+    rec = {"world": w.world, "params": w.num_params, "elements": numel, "accumulate": w.accumulate,
+           "alpha": w.alpha, "steps": steps, "fold": fold_record(w, rs_ms, peak),
+           "placement": {"ms": round(ag_mean, 4), "gbs": round(ag_b / (ag_mean * 1e-3) / 1e9, 1), "alg_bytes": ag_b,
+                         "p50_ms": pct(ag_ms, 0.5)},
+           "step": {"ms": round(total / steps, 4), "gbs": round((rs_b + ag_b) / (total / steps * 1e-3) / 1e9, 1)}}
+    if baseline:
+        b = baselines.time_two_pass(w, gs.views, S, out, slots, full, steps=min(steps, 5))
+        b["fused_speedup_rs"] = round(b["rs_ms"] / rec["fold"]["p50_ms"], 3)
+        rec["two_pass_baseline"] = {k: b[k] for k in ("rs_ms", "rs_gbs", "fused_speedup_rs", "pack_buffer_bytes")}
+    plan.close()
+    del out, slots, full, full_b
+    if own:
+        del gs
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -520,20 +623,12 @@ def run_ours(args):
     full = [torch.empty(s, dtype=torch.bfloat16, device=dev) for s in w.shapes]
     full_b = plan.bind_full(full)  # checked once, as a training loop would
     stream = torch.cuda.current_stream()
-
-    def step():
-        plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
-        plan.ag_place(slots, full_b, mode=args.ag_mode)
-
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
+    W_UP = max(args.warmup, 3)
+    timed_steps(plan, w, out, slots, full_b, args.ag_mode, W_UP, stream)
 
     clocks = ClockSampler(local)
     clocks.start()
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -541,69 +636,47 @@ def run_ours(args):
     switch = sys.getswitchinterval()
     sys.setswitchinterval(1e-4)  # let the clock sampler thread run while this thread launches
     t_wall0 = time.time()
-    start.record(stream)
-    for i in range(K):
-        ev[i][0].record(stream)
-        plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
-        ev[i][1].record(stream)
-        plan.ag_place(slots, full_b, mode=args.ag_mode)
-        ev[i][2].record(stream)
-    end.record(stream)
-    torch.cuda.synchronize()
+    rs_ms, ag_ms, total_ms = timed_steps(plan, w, out, slots, full_b, args.ag_mode, K, stream)
     t_wall1 = time.time()
     sys.setswitchinterval(switch)
     if world > 1:
         dist.barrier()
     launches = tide.tide_launch_count() - launches0
     clocks.stop()
-    total_ms = start.elapsed_time(end)
-    rs_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    ag_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    total_ms = max_over_ranks(total_ms, world, dev)
-    ms_per_step = total_ms / K
-    value = whole_job_gbs(step_bytes, world, ms_per_step)
     rs_mean = sum(rs_ms) / K
     ag_mean = sum(ag_ms) / K
-
-    def pct(xs, q):
-        ys = sorted(xs)
-        return round(ys[min(len(ys) - 1, int(q * len(ys)))], 4)
-
-    def thirds(xs):
-        """Medians of the first, middle and last third of the timed steps, the
-        median of those, and their spread (max - min) relative to it: drift or
-        a co-tenant on the shared GPU shows up here."""
-        n = len(xs) // 3
-        if n < 1:
-            return None
-        meds = [pct(xs[i * n:(i + 1) * n], 0.5) for i in range(3)]
-        mid = sorted(meds)[1]
-        return {"medians_ms": meds, "median_of_medians_ms": mid,
-                "spread_pct": round(100.0 * (max(meds) - min(meds)) / mid, 2) if mid > 0 else None}
+    total_ms = max_over_ranks(total_ms, world, dev)
+    rs_mean_max = max_over_ranks(rs_mean, world, dev)
+    ms_per_step = total_ms / K
+    value = whole_job_gbs(rs_b, world, rs_mean_max)  # the metric: the fold's effective bandwidth
     peak, peak_kind = measured_peak_gbs()
     achieved = rs_b / (rs_mean * 1e-3) / 1e9
     clk = clocks.summary(t_wall0, t_wall1)
+    traffic = profile_traffic(w.name) if (args.order == "rank" and args.sched == "static" and args.cta_budget == 0
+                                          and args.kernel in ("auto", "bulk")) else None
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "warmup": W_UP, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "world": w.world, "params": w.num_params, "elements": numel,
                    "alpha": w.alpha, "accumulate": w.accumulate, "ag_mode": args.ag_mode, "order": args.order,
                    "fold_grid": cfg["grid"], "fold_block": cfg["block"], "fold_items": cfg["items"],
                    "chunk_elems": cfg["chunk_elems"], "l2": "inputs larger than L2 (no flush)",
+                   "value": "reduce-scatter fold: world * (W*N*2 + N*4 [+ N*4]) / max-over-ranks mean fold time",
                    "step": "tide_rs_fold + tide_ag_place", "parallelism": f"weak: {world} independent replicas"},
-        "parts": {"rs_fold": {"ms": round(rs_mean, 4), "gbs": round(achieved, 1), "alg_bytes": rs_b,
-                              "p10_ms": pct(rs_ms, 0.1), "p50_ms": pct(rs_ms, 0.5), "p90_ms": pct(rs_ms, 0.9),
-                              "thirds": thirds(rs_ms)},
+        "step": {"ms": round(ms_per_step, 4), "gbs": round(whole_job_gbs(step_bytes, world, ms_per_step), 2),
+                 "alg_bytes": step_bytes, "what": "tide_rs_fold + tide_ag_place, bytes of both"},
+        "parts": {"rs_fold": fold_record(w, rs_ms, peak),
                   "ag_place": {"ms": round(ag_mean, 4), "gbs": round(ag_b / (ag_mean * 1e-3) / 1e9, 1),
                                "alg_bytes": ag_b, "p10_ms": pct(ag_ms, 0.1), "p50_ms": pct(ag_ms, 0.5),
                                "p90_ms": pct(ag_ms, 0.9), "thirds": thirds(ag_ms)}},
         "device": {"name": torch.cuda.get_device_name(dev),
                    "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profile_traffic(w.name) if args.order == "rank" else None,
-                     "kernel": "tide_rs_fold", "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "tide_rs_fold (fold_bulk_kernel)",
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "frac_of_8tbs_nominal": round(achieved / 8000.0, 4)},
         "gpu_launches": int(launches),
@@ -611,13 +684,11 @@ def run_ours(args):
         "sm_time": profile_sm_time(w.name) if args.order == "rank" else None,
     }
 
-    # the other placement engines and the mixed-precision placement, timed alone after the step
-    # the per-GPU extras (variants, enqueue times, baselines, interference) at N = 1 only:
-    # with N > 1 every rank is an independent replica of the same GPU work
+    # the per-GPU extras at N = 1 only: with N > 1 every rank is an
+    # independent replica of the same GPU work
     single = world == 1
     if single and not args.no_variants:
         result["variants"] = time_variants(plan, w, S, slots, full, dev, gs.views, steps=min(K, 20))
-    if single and not args.no_variants:
         result["host_issue_us"] = host_issue_us({
             "tide_rs_fold": lambda: plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate),
             "tide_ag_place sm": lambda: plan.ag_place(slots, full_b, mode="sm"),
@@ -636,25 +707,38 @@ def run_ours(args):
     if not args.no_interference and single:
         from all_gather_gb300 import interference
         result["interference"] = interference.summarize(
-            interference.measure(w.name, budgets=(0, 128, 64, 32, 16, 8), n_rs=20, device=local, grads=gs))
+            interference.measure(w.name, budgets=(0, 128, 64, 32, 16, 8), n_rs=args.interference_rs, device=local,
+                                 grads=gs))
         result["interference"]["sm_probe"] = interference.sm_probe(w.name, budgets=(0, 152, 64, 32, 16, 8), windows=20,
                                                                    device=local, grads=gs)
+        result["interference"]["target"] = interference.corun_target(w.name, device=local, grads=gs,
+                                                                     n_rs=args.interference_rs)
 
-    # end to end through the public API: pinned host inputs -> device -> fold + place -> host
+    # end to end through the public API: pinned host gradients -> device -> fold -> host shards
     if not args.no_e2e:
-        result["e2e"] = e2e(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world)
+        result["e2e"] = e2e(args, w, gs, plan, S, out, dev, world)
 
     if single and not args.no_cpu_baseline:
-        host = []
-        for name in SAMPLE_PARAMS:
-            i = w.names.index(name)
-            host.append([gs.views[u][i].reshape(-1).view(torch.int16).cpu().numpy().view(np.uint16)
-                         for u in range(w.world)])
-        result["cpu_baseline"] = cpu_oracle_sample(w, host)
+        idx = sample_params(w)
+        host = [[gs.views[u][i].reshape(-1).view(torch.int16).cpu().numpy().view(np.uint16) for u in range(w.world)]
+                for i in idx]
+        result["cpu_baseline"] = cpu_oracle_sample(w, host, idx)
         result["cpu_baseline"]["cpu"] = cpu_model()
-        result["cpu_baseline"]["all_cores"] = cpu_oracle_all_cores(w, host)
+        result["cpu_baseline"]["all_cores"] = cpu_oracle_all_cores(w, host, idx)
 
     plan.close()
+    del out, slots, full, full_b
+    torch.cuda.empty_cache()
+
+    # every workload in the benchmark's launch configuration (N = 1 only)
+    if single and not args.no_per_config:
+        per = {}
+        for cw in workloads.WORKLOADS:
+            same = cw.name == w.name
+            per[cw.name] = measure_config(cw, dev, steps=min(K, 20), peak=peak, gs=gs if same else None,
+                                          baseline=not args.no_baseline)
+        result["per_config"] = per
+
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -752,20 +836,17 @@ def time_variants(plan, w, S, slots, full, dev, gs_views, steps: int = 20) -> di
     return res
 
 
-def e2e(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world):
-    """End to end through the public API with host buffers: every step uploads
-    its gradients and slots from pinned host memory, runs tide_rs_fold and
-    tide_ag_place, and reads the fp32 shards and full parameters back.  Steps
-    are pipelined over two device buffer sets on three streams (upload,
-    compute, read-back), so that step i's read-back overlaps step i+1's
-    upload: the host link carries both directions at once."""
-    import torch
-    import torch.distributed as dist
-
+def e2e(args, w, gs, plan, S, out, dev, world):
+    """The metric end to end through the public API with host buffers: every
+    step uploads its W gradient sets (and, when accumulating, the old fp32
+    shards) from pinned host memory, runs tide_rs_fold, and reads the fp32
+    shards back.  Steps are pipelined over two device buffer sets on three
+    streams (upload, fold, read-back), so the host link carries both
+    directions at once; the value is the reduce-scatter's algorithmic bytes
+    over the time per step."""
     import os
 
-    import all_gather_gb300 as tide
-    import workloads
+    import torch
     # Host buffers on the GPU's own NUMA node: pinned pages are placed where
     # the allocating thread runs, and a GB300 tray has two Grace CPUs, each
     # attached to its own GPUs; buffers on the far one cross the CPU-to-CPU
@@ -776,7 +857,7 @@ def e2e(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world):
     if use:
         os.sched_setaffinity(0, use)
     try:
-        res = _e2e_run(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world, torch, dist, tide, workloads)
+        res = _e2e_run(args, w, gs, plan, S, out, dev, world)
     finally:
         os.sched_setaffinity(0, saved)
     res["host_cpus"] = {"gpu_local": cpu_ranges(local) if local else None,
@@ -784,51 +865,51 @@ def e2e(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world):
     return res
 
 
-def _e2e_run(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world, torch, dist, tide, workloads):
+def _pinned_copy(t):
+    """A pinned host copy of a device tensor (allocated pinned, no pageable staging)."""
+    import torch
+    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    h.copy_(t)
+    return h
+
+
+def _e2e_run(args, w, gs, plan, S, out, dev, world):
+    import torch
+    import torch.distributed as dist
+
+    import all_gather_gb300 as tide
+    import workloads
     K = max(2, args.e2e_steps)
-    # pinned host inputs (one set: every step uploads the same bytes) and outputs (two sets)
-    h_arenas = [a.cpu().pin_memory() for a in gs.arenas]
-    h_slots = slots.cpu().pin_memory()
-    h_out0 = out.cpu().pin_memory()
-    h_outs = [torch.empty_like(h_out0).pin_memory() for _ in range(2)]
-    h_fulls = [[torch.empty(f.shape, dtype=f.dtype).pin_memory() for f in full] for _ in range(2)]
-    # two device buffer sets; the second set has its own arenas and plan
-    sets = [(gs.arenas, gs.views, plan, out, slots, full)]
-    gs2 = workloads.make_grads(w, device=dev)
+    h_arenas = [_pinned_copy(a) for a in gs.arenas]  # one set: every step uploads the same bytes
+    h_out0 = _pinned_copy(out)
+    h_outs = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+    gs2 = workloads.make_grads(w, device=dev)  # the second device buffer set has its own arenas and plan
     plan2 = tide.Plan(gs2.views)
-    sets.append((gs2.arenas, gs2.views, plan2, torch.empty_like(out), torch.empty_like(slots),
-                 [torch.empty_like(f) for f in full]))
-    bound = [s_[2].bind_full(s_[5]) for s_ in sets]
-    h2d = sum(a.numel() * a.element_size() for a in h_arenas) + h_slots.numel() * 2
-    h2d += h_out0.numel() * 4 if w.accumulate else 0
-    d2h = h_out0.numel() * 4 + sum(f.numel() * 2 for f in full)
+    sets = [(gs.arenas, plan, out), (gs2.arenas, plan2, torch.empty_like(out))]
+    h2d = sum(a.numel() * a.element_size() for a in h_arenas) + (h_out0.numel() * 4 if w.accumulate else 0)
+    d2h = h_out0.numel() * 4
     s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
 
     def step(i, first):
         b = i % 2
-        arenas, _, pl, o, sl, fu = sets[b]
+        arenas, pl, o = sets[b]
         with torch.cuda.stream(s_in):
             if not first[b]:
                 s_in.wait_event(ev["comp"][b])  # device inputs of set b are free again
+                s_in.wait_event(ev["out"][b])   # and its shards were read back
             for a, h in zip(arenas, h_arenas):
                 a.copy_(h, non_blocking=True)
-            sl.copy_(h_slots, non_blocking=True)
+            if w.accumulate:
+                o.copy_(h_out0, non_blocking=True)
             ev["in"][b].record(s_in)
         with torch.cuda.stream(s_comp):
             s_comp.wait_event(ev["in"][b])
-            if not first[b]:
-                s_comp.wait_event(ev["out"][b])  # outputs of set b were read back
-            if w.accumulate:
-                o.copy_(h_out0, non_blocking=True)
             pl.rs_fold(o, alpha=w.alpha, accumulate=w.accumulate, stream=s_comp)
-            pl.ag_place(sl, bound[b], mode=args.ag_mode, stream=s_comp)
             ev["comp"][b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev["comp"][b])
             h_outs[b].copy_(o, non_blocking=True)
-            for f, h in zip(fu, h_fulls[b]):
-                h.copy_(f, non_blocking=True)
             ev["out"][b].record(s_out)
         first[b] = False
 
@@ -847,13 +928,15 @@ def _e2e_run(args, w, gs, plan, S, out, slots, full, dev, step_bytes, world, tor
     end.record(s_out)
     torch.cuda.synchronize()
     ms = max_over_ranks(start.elapsed_time(end) / K, world, dev)
-    ok = torch.equal(h_outs[(K - 1) % 2], sets[(K - 1) % 2][3].cpu())  # read-back == on-device result
+    ok = torch.equal(h_outs[(K - 1) % 2], sets[(K - 1) % 2][2].cpu())  # read-back == on-device result
     plan2.close()
-    del gs2, sets
-    return {"value": round(whole_job_gbs(step_bytes, world, ms), 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "steps": K, "readback_matches_device": ok,
-            "note": "per step: pinned host grads+slots -> device, tide_rs_fold + tide_ag_place, fp32 shards + full "
-                    "params -> pinned host; two device buffer sets, upload / compute / read-back streams"}
+    del gs2, sets, h_arenas, h_outs, h_out0
+    torch.cuda.empty_cache()
+    return {"value": round(whole_job_gbs(rs_alg_bytes(w, w.total_numel()), world, ms), 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "steps": K,
+            "readback_matches_device": ok,
+            "note": "per step: pinned host gradients (+ old shards when accumulating) -> device, tide_rs_fold, "
+                    "fp32 shards -> pinned host; two device buffer sets, upload / fold / read-back streams"}
 
 
 def main():

@@ -116,7 +116,9 @@ enum {
 /* Work distribution of the fold's persistent grid (bitwise identical results). */
 enum {
     TIDE_SCHED_STATIC = 0,   /* work item i goes to CTA i mod grid */
-    TIDE_SCHED_DYNAMIC = 1,  /* CTAs claim items from a device counter that resets itself */
+    TIDE_SCHED_DYNAMIC = 1,  /* CTAs claim items from a device counter that resets itself (bulk
+                                kernel: the producer lane claims each item and posts it to the
+                                CTA's consumer warps), so faster SMs take more items */
     TIDE_SCHED_PER_ITEM = 2  /* one short-lived CTA per work item (the grid is the work list; needs
                                 cta_budget 0), as the placement kernel always launches.  Alone it
                                 runs about as fast as the persistent grid; with the plan's stream at
@@ -127,7 +129,7 @@ enum {
 
 /* Reduce-scatter kernel family. */
 enum {
-    TIDE_KERNEL_AUTO = 0,    /* the library's default: BULK (DIRECT when sched is DYNAMIC) */
+    TIDE_KERNEL_AUTO = 0,    /* the library's default: BULK */
     TIDE_KERNEL_DIRECT = 1,  /* 16-byte vector loads of the W rank rows straight into registers */
     TIDE_KERNEL_BULK = 2     /* warp-specialised: bulk async copies (cp.async.bulk + mbarrier)
                                 stage the W rank rows in shared memory */
@@ -206,7 +208,7 @@ typedef struct {
  * explicit offsets, nonzero reserved fields, node_size not dividing world),
  * ALIGNMENT (a gradient pointer not aligned to its element size),
  * UNSUPPORTED (a combination this build lacks: orders other than rank order
- * and fp32 gradients run on the bulk kernel with static scheduling only),
+ * and fp32 gradients run on the bulk kernel only),
  * OOM, CUDA.
  */
 TIDE_API tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_param_desc_t *params,
@@ -284,6 +286,11 @@ TIDE_API tide_status_t tide_plan_fold_config(const tide_plan_t *plan, int32_t *g
  * Read and clear the plan's device status word (synchronises `stream`).
  * Returns TIDE_ERR_TIMEOUT if a bounded device-side wait of an earlier fold
  * on this plan expired (that fold's output is then incomplete), else TIDE_OK.
+ * With plan = NULL, reads and clears the status word of the allocation-free
+ * fold (tide_rs_fold_noalloc) on the current device instead: TIDE_ERR_TIMEOUT
+ * if a wait of any of its folds there expired since the last such read
+ * (TIDE_OK if that entry point never ran on the device).  Neither form
+ * allocates device memory.
  */
 TIDE_API tide_status_t tide_last_device_status(tide_plan_t *plan, void *stream);
 
@@ -299,9 +306,9 @@ TIDE_API uint64_t tide_launch_count(void);
  * a memory pool or cap that forbids new device allocations, or that must not
  * leave allocations behind can use this call instead: it computes the same
  * result as tide_plan_build + tide_rs_fold + tide_plan_destroy with default
- * flags (bit for bit), but keeps its tables in one fixed device array owned
- * by the library and calls no cudaMalloc, cudaFree or other allocating
- * routine.
+ * flags (bit for bit, and equal to Equation (5) in rank order), but keeps its
+ * tables in one fixed device array owned by the library and calls no
+ * cudaMalloc, cudaFree or other allocating routine.
  *   Arguments: as tide_plan_build's (world, num_params, params) followed by
  *   tide_rs_fold's (out_base, out_slot_stride, alpha, accumulate, stream);
  *   S is computed from params the same way; explicit shard offsets must be
@@ -314,7 +321,15 @@ TIDE_API uint64_t tide_launch_count(void);
  *   Memory: the array occupies TIDE_NOALLOC_SCRATCH_BYTES on each GPU where
  *   the library is used, until the process exits.
  *   Set-up: the first call on each device looks up the array's device address
- *   with that device current; make that first call before any stream capture.
+ *   with that device current and loads the fold kernels (the runtime may
+ *   reserve device memory for them then); make that first call before any
+ *   stream capture and outside the context that cannot allocate.  A call with
+ *   num_params = 0 does only this set-up.  Later calls on the device allocate
+ *   nothing.
+ *   Errors: as tide_plan_build and tide_rs_fold; nothing is enqueued on
+ *   failure.  A bounded device-side wait that expires is recorded in the
+ *   array's status word, which later calls leave as it is:
+ *   tide_last_device_status(NULL, stream) reads and clears it.
  *   Sharing: every call uses the same array, which keeps the last call's
  *   tables.  Calls that overlap on the GPU (different streams without an
  *   ordering between them) race; calls on one stream are ordered.  Calls from
@@ -387,6 +402,24 @@ TIDE_API tide_status_t tide_sm_probe(int32_t ctas, int32_t cluster, int32_t smem
 /* Clusters of the probe's shape the current device can hold at once
  * (its "cluster slots"), or -1. */
 TIDE_API int32_t tide_sm_probe_max_clusters(int32_t cluster, int32_t smem_bytes);
+
+/*
+ * CTA budget for a fold that runs next to a clustered GEMM (Section 2.2,
+ * Equation (4): T_gemm ~ ceil(n_gemm / (n_slot - n_blk)) T_wave).  A GEMM of
+ * gemm_ctas CTAs in clusters of `cluster` CTAs has n_gemm = ceil(gemm_ctas /
+ * cluster) clusters; the device holds cluster_slots (n_slot, from
+ * tide_sm_probe_max_clusters with the GEMM's cluster size and per-CTA shared
+ * memory) of them at once.  The GEMM keeps a single wave while the fold blocks
+ * at most n_slot - n_gemm slots, so the budget is (n_slot - n_gemm) * cluster:
+ * fold CTAs with an SM each (any budget up to the SM count), filling that
+ * many spare slots.  Pass the result as tide_plan_flags_t.cta_budget.
+ * Host arithmetic only (no CUDA call).  Returns 0 when the GEMM needs every
+ * slot (then every resident fold CTA can push GEMM CTAs into a second wave),
+ * -1 for arguments out of range (any count < 1, cluster > 16).
+ * Example: GB300 holds 36 clusters of four 213 KB CTAs; the 256 x 8192 x 8192
+ * GEMM's 128 CTAs form 32, so the budget is (36 - 32) * 4 = 16 CTAs.
+ */
+TIDE_API int32_t tide_corun_cta_budget(int32_t cluster_slots, int32_t gemm_ctas, int32_t cluster);
 
 /* Human-readable name of a status code. */
 TIDE_API const char *tide_status_string(tide_status_t status);

@@ -1,7 +1,10 @@
-"""Helpers for the GPU parity tests: host copies, oracle runs, sampled checks."""
+"""Helpers for the GPU parity tests: host copies, oracle runs, sampled and
+every-element full-size checks."""
 from __future__ import annotations
 
+import os
 import random
+from concurrent.futures import ThreadPoolExecutor
 from typing import List, Sequence, Tuple
 
 import numpy as np
@@ -66,6 +69,47 @@ def sampled_rs_check(world: int, dims, grads_uv, out_before: torch.Tensor, out_a
                 got = out_after[r, o[p] + lo:o[p] + hi].cpu().numpy()
                 assert_same_f32(got, want, f"{what} p={p} r={r} rows [{i0},{i1})")
                 checked += hi - lo
+    return checked
+
+
+def full_rs_check(world: int, dims, grads_uv, out_before, out_after: torch.Tensor, alpha: float,
+                  accumulate: bool, what: str = "", window: int = 1 << 20) -> int:
+    """Compare EVERY output element of a fold with the oracle, one parameter at
+    a time (host memory stays at one parameter's W gradients): the W gradient
+    tensors and the W output windows come to the host, the unchanged oracle
+    (oracle.rs_window, Eq. (3) + (5)) recomputes each (rank, window of at most
+    `window` elements) on all host cores, and the two are compared bit for
+    bit.  Returns the number of elements compared (W * S for prefix offsets)."""
+    orc = oracle.load()
+    R, o, S = orc.geometry(world, dims)
+    threads = max(1, len(os.sched_getaffinity(0)))
+    checked = 0
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        for p, (d, k) in enumerate(dims):
+            n = R[p] * k
+            if n == 0:
+                continue
+            host = [bits16(grads_uv[u][p]) for u in range(world)]
+            got = out_after[:, o[p]:o[p] + n].cpu().numpy()
+            old = out_before[:, o[p]:o[p] + n].cpu().numpy() if accumulate else None
+            want = np.empty((world, n), dtype=np.float32)
+            jobs = []
+            for r in range(world):
+                v = orc.valid_rows(d, R[p], r) * k
+                for a in range(0, n, window):
+                    b = min(a + window, n)
+                    jobs.append((r, a, b, max(0, min(b, v) - a)))
+
+            def run(job):
+                r, a, b, nv = job
+                srcs = [h[r * n + a:r * n + a + nv] for h in host]
+                want[r, a:b] = orc.rs_window(srcs, nv, (b - a) - nv, alpha, accumulate,
+                                             old[r, a:b] if accumulate else None)
+
+            list(pool.map(run, jobs))
+            if not np.array_equal(got.view(np.uint32), want.view(np.uint32)):
+                assert_same_f32(got, want, f"{what} p={p} (every element)")  # NaN classes match
+            checked += world * n
     return checked
 
 

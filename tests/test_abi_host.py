@@ -135,13 +135,13 @@ def test_empty_group(tide):
     ("chunk", "TIDE_ERR_INVALID_ARG"), ("order", "TIDE_ERR_UNSUPPORTED"),
     ("dtype", "TIDE_ERR_UNSUPPORTED"), ("overflow", "TIDE_ERR_INVALID_ARG"),
     ("neg_offset", "TIDE_ERR_INVALID_ARG"), ("sched", "TIDE_ERR_INVALID_ARG"),
-    ("fill", "TIDE_ERR_INVALID_ARG"), ("bulk_dynamic", "TIDE_ERR_UNSUPPORTED"),
+    ("fill", "TIDE_ERR_INVALID_ARG"), ("nodes_direct", "TIDE_ERR_UNSUPPORTED"),
     ("skip_fill_direct", "TIDE_ERR_INVALID_ARG"), ("debug_bits", "TIDE_ERR_INVALID_ARG"),
     ("node_size_not_dividing", "TIDE_ERR_INVALID_ARG"), ("node_size_without_nodes", "TIDE_ERR_INVALID_ARG"),
     ("nodes_without_size", "TIDE_ERR_INVALID_ARG"), ("staged_direct", "TIDE_ERR_UNSUPPORTED"),
-    ("f32_dynamic", "TIDE_ERR_UNSUPPORTED"), ("f32_misaligned", "TIDE_ERR_ALIGNMENT"),
+    ("f32_direct", "TIDE_ERR_UNSUPPORTED"), ("f32_misaligned", "TIDE_ERR_ALIGNMENT"),
     ("ce_streams", "TIDE_ERR_INVALID_ARG"), ("tree_direct", "TIDE_ERR_UNSUPPORTED"),
-    ("tree_node_size", "TIDE_ERR_INVALID_ARG"), ("tree_dynamic", "TIDE_ERR_UNSUPPORTED"),
+    ("tree_node_size", "TIDE_ERR_INVALID_ARG"), ("tree_direct_dynamic", "TIDE_ERR_UNSUPPORTED"),
     ("per_item_budget", "TIDE_ERR_INVALID_ARG"),
 ])
 def test_build_validation(tide, case, status):
@@ -175,8 +175,8 @@ def test_build_validation(tide, case, status):
         kw["sched"] = 9
     elif case == "fill":
         kw["fill_bytes"] = 24
-    elif case == "bulk_dynamic":
-        kw.update(kernel=tide.TIDE_KERNEL_BULK, sched=tide.TIDE_SCHED_DYNAMIC)
+    elif case == "nodes_direct":
+        kw.update(order=tide.TIDE_ORDER_NODES, node_size=2, kernel=tide.TIDE_KERNEL_DIRECT)
     elif case == "skip_fill_direct":
         kw.update(kernel=tide.TIDE_KERNEL_DIRECT)
     elif case == "node_size_not_dividing":
@@ -187,16 +187,16 @@ def test_build_validation(tide, case, status):
         kw.update(order=tide.TIDE_ORDER_NODES)
     elif case == "staged_direct":
         kw.update(order=tide.TIDE_ORDER_STAGED_OWN, kernel=tide.TIDE_KERNEL_DIRECT)
-    elif case == "f32_dynamic":
-        kw.update(grad_dtype=tide.TIDE_DTYPE_F32, sched=tide.TIDE_SCHED_DYNAMIC)
+    elif case == "f32_direct":
+        kw.update(grad_dtype=tide.TIDE_DTYPE_F32, kernel=tide.TIDE_KERNEL_DIRECT, sched=tide.TIDE_SCHED_DYNAMIC)
     elif case == "ce_streams":
         kw.update(ce_streams=9)
     elif case == "tree_direct":
         kw.update(order=tide.TIDE_ORDER_TREE, kernel=tide.TIDE_KERNEL_DIRECT)
     elif case == "tree_node_size":
         kw.update(order=tide.TIDE_ORDER_TREE, node_size=2)
-    elif case == "tree_dynamic":
-        kw.update(order=tide.TIDE_ORDER_TREE, sched=tide.TIDE_SCHED_DYNAMIC)
+    elif case == "tree_direct_dynamic":
+        kw.update(order=tide.TIDE_ORDER_TREE, kernel=tide.TIDE_KERNEL_DIRECT, sched=tide.TIDE_SCHED_DYNAMIC)
     elif case == "per_item_budget":
         kw.update(sched=tide.TIDE_SCHED_PER_ITEM, cta_budget=16)
     elif case == "f32_misaligned":
@@ -296,3 +296,29 @@ def test_launch_count_starts_at_zero_without_gpu(tide):
     if torch.cuda.is_available():
         pytest.skip("only meaningful before any GPU work")
     assert tide.tide_launch_count() == 0
+
+
+def test_corun_cta_budget(tide):
+    """Section 2.2, Equation (4): (n_slot - n_gemm) * cluster CTAs keep the
+    GEMM in one wave; worked values, and the documented edge cases."""
+    f = tide.tide_corun_cta_budget
+    assert f(36, 128, 4) == 16      # GB300: 36 slots, 32 four-CTA clusters
+    assert f(33, 128, 4) == 4       # the paper's GPU: one spare slot
+    assert f(32, 128, 4) == 0       # no spare slot
+    assert f(20, 128, 4) == 0
+    assert f(36, 129, 4) == 12      # a partial 33rd cluster takes a slot too
+    assert f(10, 3, 1) == 7
+    assert f(1, 16, 16) == 0 and f(2, 16, 16) == 16 and f(8, 8, 16) == 7 * 16
+    for bad in ((0, 128, 4), (36, 0, 4), (36, 128, 0), (36, 128, 17), (-1, 1, 1)):
+        assert f(*bad) == -1, bad
+
+
+@pytest.mark.parametrize("order", [0, 1, 2, 3])
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_bulk_kernel_schedules_dynamically(tide, order, dtype):
+    """The bulk kernel claims work items dynamically in every order and for
+    both gradient types; the default kernel is the bulk kernel."""
+    W, dims = 4, [(8, 8), (5, 1)]
+    plan = _host_plan(tide, W, dims, sched=tide.TIDE_SCHED_DYNAMIC, order=order, grad_dtype=dtype,
+                      node_size=2 if order == tide.TIDE_ORDER_NODES else 0)
+    tide.tide_plan_destroy(plan)

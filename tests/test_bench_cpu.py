@@ -20,13 +20,29 @@ def test_cpu_oracle_all_cores_matches_single_thread(accumulate):
     import bench
     shapes = [(5497, 1000), (333, 17), (7, 5), (3000,)]  # the first: pieces of more than one 2^20 window
     w = workloads.custom(5, shapes, index=41, alpha=0.5, accumulate=accumulate)
-    names = ("t0", "t1", "t2", "t3")
     host = [[workloads.normal_fp32(w.numels()[p], workloads.grad_seed(w, u, p), w.sigma)
              .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16) for u in range(w.world)]
             for p in range(len(shapes))]
-    rec = bench.cpu_oracle_all_cores(w, host, min_seconds=0.0, max_reps=1, names=names)
+    rec = bench.cpu_oracle_all_cores(w, host, [0, 1, 2, 3], min_seconds=0.0, max_reps=1)
     assert rec["matches_single_thread"] and rec["cores"] >= 1 and rec["value"] > 0
     assert "windows" in rec["sample"]
+    one = bench.cpu_oracle_sample(w, host, [0, 1, 2, 3], min_seconds=0.0, max_reps=1)
+    assert one["cores"] == 1 and one["value"] > 0 and one["kind"] == "oracle"
+
+
+def test_cpu_sample_takes_each_distinct_shape_once():
+    import bench
+    moe = workloads.get("qwen3_30b_a3b_moe_layer")
+    idx = bench.sample_params(moe)
+    assert [moe.names[i] for i in idx] == ["experts.0.gate_proj", "experts.0.down_proj", "router", "q_proj",
+                                           "k_proj", "o_proj"]
+    assert len({moe.shapes[i] for i in idx}) == len(idx) == len(set(moe.shapes))
+    toy = workloads.get(1)
+    assert bench.sample_params(toy) == list(range(toy.num_params))
+    assert "6 distinct shapes" in bench.sample_text(moe, idx)
+    # the metric's bytes: W*N*2 read + N*4 written (+ N*4 read when accumulating)
+    l70 = workloads.get("llama3.1_70b_block")
+    assert bench.rs_alg_bytes(l70, 10) == 8 * 10 * 2 + 10 * 4 + 10 * 4
 
 
 def test_cpu_ranges_and_model():

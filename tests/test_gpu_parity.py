@@ -69,7 +69,11 @@ KERNELS = {"direct": dict(kernel=tide.TIDE_KERNEL_DIRECT),
            # tiny fills and odd rank groups: many stage fills per chunk, groups of 3, 3, ..., remainder
            "bulk_groups": dict(kernel=tide.TIDE_KERNEL_BULK, fill_bytes=64, fill_ranks=3),
            # one short-lived CTA per work item
-           "bulk_per_item": dict(kernel=tide.TIDE_KERNEL_BULK, sched=tide.TIDE_SCHED_PER_ITEM)}
+           "bulk_per_item": dict(kernel=tide.TIDE_KERNEL_BULK, sched=tide.TIDE_SCHED_PER_ITEM),
+           # persistent CTAs claiming items from the device counter
+           "bulk_dynamic": dict(kernel=tide.TIDE_KERNEL_BULK, sched=tide.TIDE_SCHED_DYNAMIC),
+           "bulk_dynamic_groups": dict(kernel=tide.TIDE_KERNEL_BULK, sched=tide.TIDE_SCHED_DYNAMIC, fill_bytes=64,
+                                       fill_ranks=3, cta_budget=5)}
 
 
 # ---------------------------------------------------------------------------
@@ -194,7 +198,10 @@ def test_determinism_across_launch_shapes():
                {"kernel": tide.TIDE_KERNEL_BULK, "chunk_bytes": 512},
                {"kernel": tide.TIDE_KERNEL_BULK, "fill_bytes": 16, "fill_ranks": 1},
                {"kernel": tide.TIDE_KERNEL_BULK, "fill_bytes": 4096, "fill_ranks": 4},
-               {"kernel": tide.TIDE_KERNEL_BULK, "cta_budget": 9}):
+               {"kernel": tide.TIDE_KERNEL_BULK, "cta_budget": 9},
+               {"kernel": tide.TIDE_KERNEL_BULK, "sched": tide.TIDE_SCHED_DYNAMIC},
+               {"kernel": tide.TIDE_KERNEL_BULK, "sched": tide.TIDE_SCHED_DYNAMIC, "cta_budget": 2},
+               {"kernel": tide.TIDE_KERNEL_BULK, "sched": tide.TIDE_SCHED_DYNAMIC, "cta_budget": 100}):
         out = torch.zeros(w.world, S, device="cuda")
         _fold(w, gs.views, 0.25, False, out, **kw)
         got = out.cpu().numpy()
@@ -344,15 +351,15 @@ def test_tree_order_probe(case, fill_ranks):
 
 def _random_flags(rnd, world):
     """A valid random flag set: orders other than rank order and fp32
-    gradients take the statically scheduled bulk kernel."""
+    gradients take the bulk kernel (any schedule)."""
     order = rnd.choice([tide.TIDE_ORDER_RANK_ASC] * 3 + [tide.TIDE_ORDER_STAGED_OWN, tide.TIDE_ORDER_NODES,
                                                          tide.TIDE_ORDER_TREE])
     f32 = rnd.random() < 0.3
     restricted = order != tide.TIDE_ORDER_RANK_ASC or f32
     kernel = tide.TIDE_KERNEL_BULK if restricted else rnd.choice(
         [tide.TIDE_KERNEL_AUTO, tide.TIDE_KERNEL_DIRECT, tide.TIDE_KERNEL_BULK])
-    sched = tide.TIDE_SCHED_DYNAMIC if kernel == tide.TIDE_KERNEL_DIRECT and rnd.random() < 0.5 else \
-        tide.TIDE_SCHED_PER_ITEM if rnd.random() < 0.2 else tide.TIDE_SCHED_STATIC
+    sched = tide.TIDE_SCHED_DYNAMIC if rnd.random() < 0.35 else \
+        tide.TIDE_SCHED_PER_ITEM if rnd.random() < 0.25 else tide.TIDE_SCHED_STATIC
     kw = dict(kernel=kernel, sched=sched, order=order,
               grad_dtype=tide.TIDE_DTYPE_F32 if f32 else tide.TIDE_DTYPE_BF16,
               cta_budget=0 if sched == tide.TIDE_SCHED_PER_ITEM else rnd.choice([0, 0, 1, 3, rnd.randint(1, 400)]),
@@ -771,7 +778,8 @@ def test_full_size_bitwise_across_launch_shapes(index):
     init = workloads.make_out_init(w, S, device="cuda") if w.accumulate else None
     ref = None
     for kw in ({}, {"cta_budget": 152}, {"cta_budget": 64}, {"cta_budget": 16}, {"cta_budget": 7},
-               {"sched": tide.TIDE_SCHED_PER_ITEM}, {"kernel": tide.TIDE_KERNEL_DIRECT},
+               {"sched": tide.TIDE_SCHED_PER_ITEM}, {"sched": tide.TIDE_SCHED_DYNAMIC},
+               {"sched": tide.TIDE_SCHED_DYNAMIC, "cta_budget": 16}, {"kernel": tide.TIDE_KERNEL_DIRECT},
                {"kernel": tide.TIDE_KERNEL_DIRECT, "sched": tide.TIDE_SCHED_PER_ITEM},
                {"fill_bytes": 1008, "fill_ranks": 3},
                {"cta_budget": 32, "fill_bytes": 12288, "fill_ranks": 5}):

@@ -1,14 +1,24 @@
-"""The allocation-free fold (tide_rs_fold_noalloc) against the plan-based one.
+"""The allocation-free fold (tide_rs_fold_noalloc) against the oracle and the
+plan-based fold.
 
 Some callers cannot allocate GPU memory (code running inside an allocator or
 an out-of-memory handler, under a pool or cap that forbids new device
 allocations), so they cannot build a plan, whose device tables come from
 cudaMalloc.  tide_rs_fold_noalloc serves them from a fixed device array owned
-by the library.  This test calls it through the C ABI twice in a row, with
-different groups, and checks that each result equals the plan-based
-tide_rs_fold's bit for bit (the same tolerance as every fold parity test:
-none).  It also checks that an oversized request is refused.  The file sorts
-last so that a run stopping at the first failure has run everything else.
+by the library.  These tests call it through the C ABI and check:
+
+* two calls in a row, with different groups, each equal to the oracle
+  (Equation (5) in rank order) and to the plan-based tide_rs_fold bit for bit
+  (the tolerance of every fold parity test: none);
+* a group whose ranks' rows differ in 16-byte phase (the fold's scalar path)
+  and a 32-rank group (several shared-memory stage fills per chunk);
+* that after a warm-up call, further calls leave the device's free memory and
+  torch's allocation count unchanged, and that the entry point's device
+  status word reads TIDE_OK through tide_last_device_status(NULL, stream);
+* that an oversized request is refused before any GPU work.
+
+The file sorts last so that a run stopping at the first failure has run
+everything else; every test here also passes in a fresh process.
 """
 import pytest
 import torch
@@ -16,6 +26,7 @@ import torch
 import all_gather_gb300 as tide
 import workloads
 from bits import assert_same_f32
+from gpu_helpers import oracle_rs_full
 
 pytestmark = pytest.mark.gpu
 
@@ -30,38 +41,88 @@ def _descs(grads_uv):
     return out
 
 
-def _both(w, gs, alpha, accumulate, stride_extra=0):
-    """(plan-based result, allocation-free result) on identical inputs."""
-    init = None
-    with tide.Plan(gs.views) as plan:
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _noalloc(world, views, out, stride, alpha, accumulate):
+    tide.tide_rs_fold_noalloc(world, _descs(views), out.data_ptr(), stride, alpha, int(accumulate), _stream())
+
+
+def _check(world, views, alpha, accumulate, stride_extra=0, what=""):
+    """Allocation-free result vs the plan-based fold and vs the oracle."""
+    dims = [(t.shape[0], t.numel() // t.shape[0] if t.shape[0] else 0) for t in views[0]]
+    with tide.Plan(views) as plan:
         S = plan.slot_numel
         stride = S + stride_extra
-        if accumulate:
-            init = torch.randn(w.world, stride, device="cuda")
-        ref = init.clone() if accumulate else torch.zeros(w.world, stride, device="cuda")
+        init = torch.randn(world, stride, device="cuda") if accumulate else None
+        ref = init.clone() if accumulate else torch.full((world, stride), 7.0, device="cuda")
         plan.rs_fold(ref, alpha=alpha, accumulate=accumulate)
-    got = init.clone() if accumulate else torch.full((w.world, stride), 7.0, device="cuda")
+    got = init.clone() if accumulate else torch.full((world, stride), 7.0, device="cuda")
     if not accumulate:
         got[:, :S] = -1.0  # every element up to S must be overwritten
-        ref[:, S:] = 7.0
-    tide.tide_rs_fold_noalloc(w.world, _descs(gs.views), got.data_ptr(), stride, alpha, int(accumulate),
-                              torch.cuda.current_stream().cuda_stream)
+    _noalloc(world, views, got, stride, alpha, accumulate)
     torch.cuda.synchronize()
-    return ref, got
+    assert tide.tide_last_device_status(0, _stream()) == tide.TIDE_OK
+    assert_same_f32(got.cpu().numpy(), ref.cpu().numpy(), f"{what}: allocation-free vs plan-based fold")
+    before = init if accumulate else torch.zeros(world, stride, device="cuda")
+    want = oracle_rs_full(world, dims, views, alpha, accumulate, before)
+    assert_same_f32(got[:, :S].cpu().numpy(), want[:, :S], f"{what}: allocation-free fold vs the oracle")
+    if not accumulate:
+        assert (got[:, S:] == 7.0).all(), f"{what}: wrote past S"
 
 
-def test_noalloc_matches_plan_fold_two_calls_in_a_row():
+def test_noalloc_matches_oracle_and_plan_fold_two_calls_in_a_row():
     torch.cuda.set_device(0)
-    # call 1: the toy group (W = 4, ragged shapes, padding, scale 1/W)
+    # call 1: the toy group (W = 4, ragged shapes, padding, scale 1/W; pieces
+    # whose ranks share a non-zero 16-byte phase)
     w1 = workloads.get(1)
     g1 = workloads.make_grads(w1, device="cuda")
-    ref1, got1 = _both(w1, g1, w1.alpha, False, stride_extra=3)
-    assert_same_f32(got1.cpu().numpy(), ref1.cpu().numpy(), "allocation-free fold, call 1")
+    _check(w1.world, g1.views, w1.alpha, False, stride_extra=3, what="call 1 (toy group)")
     # call 2, straight after: a different group (W = 8) in accumulate mode
     w2 = workloads.custom(8, [(1000, 33), (17,), (4096, 64), (5, 3)], index=123)
     g2 = workloads.make_grads(w2, device="cuda")
-    ref2, got2 = _both(w2, g2, 0.5, True)
-    assert_same_f32(got2.cpu().numpy(), ref2.cpu().numpy(), "allocation-free fold, call 2")
+    _check(w2.world, g2.views, 0.5, True, what="call 2 (W = 8, accumulate)")
+
+
+def test_noalloc_ranks_in_different_phases_and_32_ranks():
+    torch.cuda.set_device(0)
+    # every rank's tensors start at a different 2-byte offset: the ranks' rows
+    # differ in 16-byte phase, so the fold reads them element by element
+    w = workloads.custom(5, [(301, 17), (64,), (40, 129)], index=124)
+    g = workloads.make_grads(w, device="cuda")
+    views = []
+    for u in range(w.world):
+        vs = []
+        for t in g.views[u]:
+            base = torch.empty(t.numel() + 8, dtype=torch.bfloat16, device="cuda")
+            v = base[u % 8:u % 8 + t.numel()].view(t.shape)
+            v.copy_(t)
+            vs.append(v)
+        views.append(vs)
+    _check(w.world, views, 1.0, False, what="mixed phases")
+    # 32 ranks: four stage fills of eight ranks per chunk, summed in order
+    w32 = workloads.custom(32, [(1000, 33), (4096,), (64, 128), (33, 7)], index=125)
+    g32 = workloads.make_grads(w32, device="cuda")
+    _check(w32.world, g32.views, 1.0 / 32, False, stride_extra=5, what="W = 32")
+    _check(w32.world, g32.views, 1.0, True, what="W = 32, accumulate")
+
+
+def test_noalloc_allocates_nothing_after_set_up():
+    torch.cuda.set_device(0)
+    w = workloads.custom(8, [(1000, 64), (4096,), (129, 128)], index=126)
+    g = workloads.make_grads(w, device="cuda")
+    out = torch.zeros(w.world, 200_000, device="cuda")
+    tide.tide_rs_fold_noalloc(w.world, [], 0, 0, 1.0, 0, _stream())  # empty call: the per-device set-up
+    _noalloc(w.world, g.views, out, out.shape[1], 1.0, False)         # warm-up call
+    torch.cuda.synchronize()
+    free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    for i in range(4):
+        _noalloc(w.world, g.views, out, out.shape[1], 0.5 * (i + 1), i % 2)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0, "device free memory changed across allocation-free calls"
+    assert torch.cuda.memory_allocated() == alloc0
+    assert tide.tide_last_device_status(0, _stream()) == tide.TIDE_OK
 
 
 def test_noalloc_rejects_tables_beyond_its_array():

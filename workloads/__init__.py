@@ -113,14 +113,14 @@ def _wan_block():
                     notes="10 norm/modulation vectors of [5120] assumed")
 
 
-def _qwen3_moe_layer():
+def _qwen3_moe_layer(experts=128, index=5, name="qwen3_30b_a3b_moe_layer"):
     names, shapes = [], []
-    for e in range(128):
+    for e in range(experts):
         names += [f"experts.{e}.gate_proj", f"experts.{e}.up_proj", f"experts.{e}.down_proj"]
         shapes += [(768, 2048), (768, 2048), (2048, 768)]
     names += ["router", "q_proj", "k_proj", "v_proj", "o_proj"]
     shapes += [(128, 2048), (4096, 2048), (512, 2048), (512, 2048), (2048, 4096)]
-    return Workload(5, "qwen3_30b_a3b_moe_layer", 32, tuple(names), tuple(shapes), sigma=1e-3)
+    return Workload(index, name, 32, tuple(names), tuple(shapes), sigma=1e-3)
 
 
 WORKLOADS: Tuple[Workload, ...] = (
@@ -135,14 +135,18 @@ WORKLOADS: Tuple[Workload, ...] = (
     _qwen3_moe_layer(),
 )
 
-# A reduced case of the Llama-3.1-8B block (its attention projections and
-# norms only, ~0.7 GB of gradients) for full-set profiler captures, which
-# replay a kernel dozens of times and so want a few GB on the device at most.
+# Reduced cases for profiler captures, which replay a kernel dozens of times
+# and so want a few GB on the device at most: the Llama-3.1-8B block's
+# attention projections and norms (~0.7 GB of gradients), and the MoE layer
+# with 8 of its 128 experts (same W = 32 and shapes, 56.9 M elements per
+# gradient set, 3.6 GB of gradients; its per-element traffic scales to the
+# full layer).
 PROFILE_CASES: Tuple[Workload, ...] = (
     Workload(6, "llama3.1_8b_attn", 8,
              ("q_proj", "k_proj", "v_proj", "o_proj", "input_layernorm", "post_attention_layernorm"),
              ((4096, 4096), (1024, 4096), (1024, 4096), (4096, 4096), (4096,), (4096,)),
              sigma=1e-3, outlier_rate=1e-3, outlier_scale=100.0),
+    _qwen3_moe_layer(experts=8, index=7, name="qwen3_moe_8experts"),
 )
 
 BY_NAME = {w.name: w for w in WORKLOADS + PROFILE_CASES}
