@@ -22,7 +22,7 @@ from ._binding import (  # noqa: F401  (re-exported C-ABI names)
     TIDE_ERR_ALIGNMENT, TIDE_ERR_CUDA, TIDE_ERR_INVALID_ARG, TIDE_ERR_OOM, TIDE_ERR_TIMEOUT, TIDE_ERR_UNSUPPORTED,
     TIDE_KERNEL_AUTO, TIDE_KERNEL_BULK, TIDE_KERNEL_DIRECT, TIDE_OK, TIDE_ORDER_NODES, TIDE_ORDER_RANK_ASC,
     TIDE_ORDER_STAGED_OWN, TIDE_ORDER_TREE, TIDE_DTYPE_F32, TIDE_SCHED_DYNAMIC,
-    TIDE_SCHED_STATIC, TIDE_SCHED_PER_ITEM, PlanFlags, TideError, load_library, make_flags, tide_ag_place, tide_ag_place_f32,
+    TIDE_SCHED_AUTO, TIDE_SCHED_STATIC, TIDE_SCHED_PER_ITEM, PlanFlags, TideError, load_library, make_flags, tide_ag_place, tide_ag_place_f32,
     tide_last_device_status,
     tide_last_error, tide_launch_count, tide_plan_build, tide_plan_destroy, tide_plan_fold_config,
     tide_plan_num_segments, tide_plan_rebind, tide_plan_segment, tide_plan_slot_numel, tide_rs_fold,

@@ -24,7 +24,7 @@ TIDE_ERR_CUDA = 5
 TIDE_ERR_TIMEOUT = 6
 # enums
 TIDE_ORDER_RANK_ASC, TIDE_ORDER_STAGED_OWN, TIDE_ORDER_NODES, TIDE_ORDER_TREE = 0, 1, 2, 3
-TIDE_SCHED_STATIC, TIDE_SCHED_DYNAMIC, TIDE_SCHED_PER_ITEM = 0, 1, 2
+TIDE_SCHED_AUTO, TIDE_SCHED_DYNAMIC, TIDE_SCHED_PER_ITEM, TIDE_SCHED_STATIC = 0, 1, 2, 3
 TIDE_KERNEL_AUTO, TIDE_KERNEL_DIRECT, TIDE_KERNEL_BULK = 0, 1, 2
 TIDE_AG_SM, TIDE_AG_CE_2D, TIDE_AG_CE_1D = 0, 1, 2
 TIDE_DTYPE_BF16, TIDE_DTYPE_F32 = 0, 1
@@ -156,7 +156,7 @@ def _descs(params: Sequence[Tuple[Sequence[int], int, int, int]]):
     return arr, keep
 
 
-def make_flags(cta_budget=0, chunk_bytes=0, order=TIDE_ORDER_RANK_ASC, sched=TIDE_SCHED_STATIC,
+def make_flags(cta_budget=0, chunk_bytes=0, order=TIDE_ORDER_RANK_ASC, sched=TIDE_SCHED_AUTO,
                kernel=TIDE_KERNEL_AUTO, grad_dtype=TIDE_DTYPE_BF16, debug=0, fill_bytes=0,
                fill_ranks=0, node_size=0, ce_streams=0) -> PlanFlags:
     f = PlanFlags()

@@ -27,9 +27,11 @@
 // stream capture, outside the context that cannot allocate.
 //
 // The first 256 bytes of the array hold the status word of the bounded
-// device-side waits; the tables follow.  Uploads never touch the status
-// word: an expired wait stays recorded until tide_last_device_status(NULL,
-// stream) reads and clears it on the current device.
+// device-side waits (offset 0) and the dynamic schedule's two counters
+// (offsets 8 and 12, zero at load; every fold resets them as it finishes);
+// the tables follow.  Uploads never touch this slot: an expired wait stays
+// recorded until tide_last_device_status(NULL, stream) reads and clears it
+// on the current device.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -55,7 +57,8 @@ alignas(256) unsigned char g_host_tables[kScratchBytes];
 void *g_scratch_dev[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 std::mutex g_lock;
-constexpr size_t kStatusBytes = 256;  // the status word's slot at the start of the array
+constexpr size_t kStatusBytes = 256;  // status word and schedule counters at the start of the array
+constexpr size_t kCountersAt = 8;     // byte offset of the two schedule counters in that slot
 
 // Record the detail that tide_last_error() reports, without heap use.
 tide_status_t noalloc_fail(tide_status_t st, const char *fmt, ...)
@@ -251,8 +254,8 @@ extern "C" tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params,
     fp.stride = out_slot_stride;
     fp.alpha = alpha;
     fp.world = world;
-    fp.sched = TIDE_SCHED_STATIC;
-    fp.counters = nullptr;
+    fp.sched = TIDE_SCHED_DYNAMIC;  // the default schedule, as tide_plan_build resolves it
+    fp.counters = reinterpret_cast<uint32_t *>(scratch + kCountersAt);
     fp.status = reinterpret_cast<int32_t *>(scratch);
     fp.wait_budget_ns = tide::kWaitBudgetNs;
     fp.order = TIDE_ORDER_RANK_ASC;

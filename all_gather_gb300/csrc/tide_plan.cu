@@ -105,7 +105,8 @@ tide_status_t check_flags(const tide_plan_flags_t &f)
         return fail(TIDE_ERR_UNSUPPORTED, "flags.order %d is not implemented", f.order);
     if (f.order == TIDE_ORDER_NODES ? f.node_size < 1 : f.node_size != 0)
         return fail(TIDE_ERR_INVALID_ARG, "flags.node_size %d (positive with TIDE_ORDER_NODES only)", f.node_size);
-    if (f.sched != TIDE_SCHED_STATIC && f.sched != TIDE_SCHED_DYNAMIC && f.sched != TIDE_SCHED_PER_ITEM)
+    if (f.sched != TIDE_SCHED_AUTO && f.sched != TIDE_SCHED_STATIC && f.sched != TIDE_SCHED_DYNAMIC &&
+        f.sched != TIDE_SCHED_PER_ITEM)
         return fail(TIDE_ERR_INVALID_ARG, "flags.sched %d", f.sched);
     if (f.sched == TIDE_SCHED_PER_ITEM && f.cta_budget != 0)
         return fail(TIDE_ERR_INVALID_ARG, "TIDE_SCHED_PER_ITEM sizes the grid itself: cta_budget must be 0");
@@ -300,6 +301,8 @@ static tide_status_t plan_build_impl(int32_t world, int32_t num_params, const ti
         delete plan;
         return s;
     };
+    if (f.sched == TIDE_SCHED_AUTO)
+        f.sched = TIDE_SCHED_DYNAMIC;  // faster than the static split on every benchmark group
     plan->world = world;
     plan->nparams = num_params;
     plan->flags = f;

@@ -55,7 +55,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--ag-mode", choices=["sm", "ce2d", "ce1d"], default="sm")
     ap.add_argument("--kernel", choices=["auto", "direct", "bulk"], default="auto")
-    ap.add_argument("--sched", choices=["static", "dynamic", "per_item"], default="static")
+    ap.add_argument("--sched", choices=["auto", "static", "dynamic", "per_item"], default="auto",
+                    help="fold schedule (auto: the library default, dynamic)")
     ap.add_argument("--cta-budget", type=int, default=0)
     ap.add_argument("--chunk-bytes", type=int, default=0)
     ap.add_argument("--fill-bytes", type=int, default=0, help="bulk kernel: bytes per rank per stage fill")
@@ -548,6 +549,37 @@ def fold_record(w, rs_ms, peak):
             "p50_ms": pct(rs_ms, 0.5), "p90_ms": pct(rs_ms, 0.9), "thirds": thirds(rs_ms)}
 
 
+def graph_step(plan, w, out, slots, full_b, steps, step_bytes):
+    """The step (fold + placement) captured once in a CUDA graph and replayed:
+    the time of the two kernels without the host's per-call enqueue, which
+    bounds small groups when launched one call at a time."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside the capture
+        plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
+        plan.ag_place(slots, full_b, mode="sm")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
+        plan.ag_place(slots, full_b, mode="sm")
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        g.replay()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    mean = sum(ms) / steps
+    del g
+    return {"ms": round(mean, 4), "p50_ms": pct(ms, 0.5), "gbs": round(step_bytes / (mean * 1e-3) / 1e9, 1),
+            "what": "tide_rs_fold + tide_ag_place captured once, graph replayed"}
+
+
 def measure_config(w, dev, steps, peak, gs=None, baseline=True):
     """Fold, placement and step times of one workload in the benchmark's launch
     configuration (default flags, SM placement), plus the two-pass baseline's
@@ -576,6 +608,7 @@ def measure_config(w, dev, steps, peak, gs=None, baseline=True):
            "placement": {"ms": round(ag_mean, 4), "gbs": round(ag_b / (ag_mean * 1e-3) / 1e9, 1), "alg_bytes": ag_b,
                          "p50_ms": pct(ag_ms, 0.5)},
            "step": {"ms": round(total / steps, 4), "gbs": round((rs_b + ag_b) / (total / steps * 1e-3) / 1e9, 1)}}
+    rec["step_graph"] = graph_step(plan, w, out, slots, full_b, steps, rs_b + ag_b)
     if baseline:
         b = baselines.time_two_pass(w, gs.views, S, out, slots, full, steps=min(steps, 5))
         b["fused_speedup_rs"] = round(b["rs_ms"] / rec["fold"]["p50_ms"], 3)
@@ -612,7 +645,7 @@ def run_ours(args):
     gs = workloads.make_grads(w, device=dev)
     flags = tide.make_flags(cta_budget=args.cta_budget, chunk_bytes=args.chunk_bytes, fill_bytes=args.fill_bytes,
                             fill_ranks=args.fill_ranks, ce_streams=args.ce_streams,
-                            sched={"static": 0, "dynamic": 1, "per_item": 2}[args.sched],
+                            sched={"auto": 0, "dynamic": 1, "per_item": 2, "static": 3}[args.sched],
                             kernel={"auto": 0, "direct": 1, "bulk": 2}[args.kernel], order=ORDERS[args.order],
                             node_size=(args.node_size or max(1, w.world // 2)) if args.order == "nodes" else 0)
     plan = tide.Plan(gs.views, flags)
@@ -652,7 +685,7 @@ def run_ours(args):
     peak, peak_kind = measured_peak_gbs()
     achieved = rs_b / (rs_mean * 1e-3) / 1e9
     clk = clocks.summary(t_wall0, t_wall1)
-    traffic = profile_traffic(w.name) if (args.order == "rank" and args.sched == "static" and args.cta_budget == 0
+    traffic = profile_traffic(w.name) if (args.order == "rank" and args.sched == "auto" and args.cta_budget == 0
                                           and args.kernel in ("auto", "bulk")) else None
 
     result = {

@@ -115,16 +115,19 @@ enum {
 
 /* Work distribution of the fold's persistent grid (bitwise identical results). */
 enum {
-    TIDE_SCHED_STATIC = 0,   /* work item i goes to CTA i mod grid */
+    TIDE_SCHED_AUTO = 0,     /* the library's default: TIDE_SCHED_DYNAMIC */
     TIDE_SCHED_DYNAMIC = 1,  /* CTAs claim items from a device counter that resets itself (bulk
                                 kernel: the producer lane claims each item and posts it to the
-                                CTA's consumer warps), so faster SMs take more items */
-    TIDE_SCHED_PER_ITEM = 2  /* one short-lived CTA per work item (the grid is the work list; needs
+                                CTA's consumer warps), so faster SMs take more items: 2-6% faster
+                                than TIDE_SCHED_STATIC on the benchmark groups.  The counter
+                                lives in the plan, so one plan's folds must not overlap */
+    TIDE_SCHED_PER_ITEM = 2, /* one short-lived CTA per work item (the grid is the work list; needs
                                 cta_budget 0), as the placement kernel always launches.  Alone it
                                 runs about as fast as the persistent grid; with the plan's stream at
                                 a lower priority than concurrent compute, the block scheduler hands
                                 SMs to the compute kernels as these CTAs retire, so the fold yields
                                 without a fixed CTA budget (Section 2.2's SM interference) */
+    TIDE_SCHED_STATIC = 3    /* work item i goes to CTA i mod grid */
 };
 
 /* Reduce-scatter kernel family. */
@@ -331,9 +334,10 @@ TIDE_API uint64_t tide_launch_count(void);
  *   array's status word, which later calls leave as it is:
  *   tide_last_device_status(NULL, stream) reads and clears it.
  *   Sharing: every call uses the same array, which keeps the last call's
- *   tables.  Calls that overlap on the GPU (different streams without an
- *   ordering between them) race; calls on one stream are ordered.  Calls from
- *   several host threads are serialised by a lock.
+ *   tables and the schedule's work counter.  Calls that overlap on the GPU
+ *   (different streams without an ordering between them) race; calls on one
+ *   stream are ordered.  Calls from several host threads are serialised by a
+ *   lock.
  */
 #define TIDE_NOALLOC_SCRATCH_BYTES ((size_t)4 * 1024 * 1024)
 TIDE_API tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params, const tide_param_desc_t *params,

@@ -63,17 +63,19 @@ def _check_canaries(buf, out, S):
     assert (tail == np.float32(CANARY)).all(), "wrote past S inside a slot"
 
 
-KERNELS = {"direct": dict(kernel=tide.TIDE_KERNEL_DIRECT),
-           "direct_dynamic": dict(kernel=tide.TIDE_KERNEL_DIRECT, sched=tide.TIDE_SCHED_DYNAMIC),
+KERNELS = {"direct": dict(kernel=tide.TIDE_KERNEL_DIRECT),  # the default schedule: dynamic
+           "direct_static": dict(kernel=tide.TIDE_KERNEL_DIRECT, sched=tide.TIDE_SCHED_STATIC),
            "bulk": dict(kernel=tide.TIDE_KERNEL_BULK),
+           "bulk_static": dict(kernel=tide.TIDE_KERNEL_BULK, sched=tide.TIDE_SCHED_STATIC),
            # tiny fills and odd rank groups: many stage fills per chunk, groups of 3, 3, ..., remainder
            "bulk_groups": dict(kernel=tide.TIDE_KERNEL_BULK, fill_bytes=64, fill_ranks=3),
            # one short-lived CTA per work item
            "bulk_per_item": dict(kernel=tide.TIDE_KERNEL_BULK, sched=tide.TIDE_SCHED_PER_ITEM),
-           # persistent CTAs claiming items from the device counter
-           "bulk_dynamic": dict(kernel=tide.TIDE_KERNEL_BULK, sched=tide.TIDE_SCHED_DYNAMIC),
+           # persistent CTAs claiming items from the device counter, few CTAs and odd fills
            "bulk_dynamic_groups": dict(kernel=tide.TIDE_KERNEL_BULK, sched=tide.TIDE_SCHED_DYNAMIC, fill_bytes=64,
-                                       fill_ranks=3, cta_budget=5)}
+                                       fill_ranks=3, cta_budget=5),
+           "bulk_static_groups": dict(kernel=tide.TIDE_KERNEL_BULK, sched=tide.TIDE_SCHED_STATIC, fill_bytes=64,
+                                      fill_ranks=3, cta_budget=5)}
 
 
 # ---------------------------------------------------------------------------
@@ -97,7 +99,7 @@ def test_toy_full_parity(acc, alpha, kname):
 
 @pytest.mark.parametrize("world", [1, 2, 3, 5, 8, 16, 32])
 @pytest.mark.parametrize("chunk", [256, 0])
-@pytest.mark.parametrize("kname", ["direct", "bulk", "bulk_groups"])
+@pytest.mark.parametrize("kname", ["direct", "bulk", "bulk_groups", "bulk_static"])
 def test_ragged_shapes(world, chunk, kname):
     rnd = random.Random(world * 101 + chunk)
     shapes = [(rnd.randint(1, 3 * world + 7), rnd.choice([1, 3, 8, 17, 64, 129])) for _ in range(5)]
@@ -199,9 +201,10 @@ def test_determinism_across_launch_shapes():
                {"kernel": tide.TIDE_KERNEL_BULK, "fill_bytes": 16, "fill_ranks": 1},
                {"kernel": tide.TIDE_KERNEL_BULK, "fill_bytes": 4096, "fill_ranks": 4},
                {"kernel": tide.TIDE_KERNEL_BULK, "cta_budget": 9},
-               {"kernel": tide.TIDE_KERNEL_BULK, "sched": tide.TIDE_SCHED_DYNAMIC},
-               {"kernel": tide.TIDE_KERNEL_BULK, "sched": tide.TIDE_SCHED_DYNAMIC, "cta_budget": 2},
-               {"kernel": tide.TIDE_KERNEL_BULK, "sched": tide.TIDE_SCHED_DYNAMIC, "cta_budget": 100}):
+               {"kernel": tide.TIDE_KERNEL_BULK, "sched": tide.TIDE_SCHED_STATIC},
+               {"kernel": tide.TIDE_KERNEL_BULK, "sched": tide.TIDE_SCHED_STATIC, "cta_budget": 2},
+               {"kernel": tide.TIDE_KERNEL_BULK, "sched": tide.TIDE_SCHED_STATIC, "cta_budget": 100},
+               {"kernel": tide.TIDE_KERNEL_DIRECT, "sched": tide.TIDE_SCHED_STATIC}):
         out = torch.zeros(w.world, S, device="cuda")
         _fold(w, gs.views, 0.25, False, out, **kw)
         got = out.cpu().numpy()
@@ -358,8 +361,8 @@ def _random_flags(rnd, world):
     restricted = order != tide.TIDE_ORDER_RANK_ASC or f32
     kernel = tide.TIDE_KERNEL_BULK if restricted else rnd.choice(
         [tide.TIDE_KERNEL_AUTO, tide.TIDE_KERNEL_DIRECT, tide.TIDE_KERNEL_BULK])
-    sched = tide.TIDE_SCHED_DYNAMIC if rnd.random() < 0.35 else \
-        tide.TIDE_SCHED_PER_ITEM if rnd.random() < 0.25 else tide.TIDE_SCHED_STATIC
+    sched = rnd.choice([tide.TIDE_SCHED_AUTO, tide.TIDE_SCHED_DYNAMIC, tide.TIDE_SCHED_STATIC,
+                        tide.TIDE_SCHED_STATIC, tide.TIDE_SCHED_PER_ITEM])
     kw = dict(kernel=kernel, sched=sched, order=order,
               grad_dtype=tide.TIDE_DTYPE_F32 if f32 else tide.TIDE_DTYPE_BF16,
               cta_budget=0 if sched == tide.TIDE_SCHED_PER_ITEM else rnd.choice([0, 0, 1, 3, rnd.randint(1, 400)]),
@@ -778,8 +781,8 @@ def test_full_size_bitwise_across_launch_shapes(index):
     init = workloads.make_out_init(w, S, device="cuda") if w.accumulate else None
     ref = None
     for kw in ({}, {"cta_budget": 152}, {"cta_budget": 64}, {"cta_budget": 16}, {"cta_budget": 7},
-               {"sched": tide.TIDE_SCHED_PER_ITEM}, {"sched": tide.TIDE_SCHED_DYNAMIC},
-               {"sched": tide.TIDE_SCHED_DYNAMIC, "cta_budget": 16}, {"kernel": tide.TIDE_KERNEL_DIRECT},
+               {"sched": tide.TIDE_SCHED_PER_ITEM}, {"sched": tide.TIDE_SCHED_STATIC},
+               {"sched": tide.TIDE_SCHED_STATIC, "cta_budget": 16}, {"kernel": tide.TIDE_KERNEL_DIRECT},
                {"kernel": tide.TIDE_KERNEL_DIRECT, "sched": tide.TIDE_SCHED_PER_ITEM},
                {"fill_bytes": 1008, "fill_ranks": 3},
                {"cta_budget": 32, "fill_bytes": 12288, "fill_ranks": 5}):
