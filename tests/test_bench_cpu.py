@@ -58,12 +58,13 @@ def test_profile_readers_follow_the_kernel_source():
     all once the source has changed."""
     import bench
     digest = bench.kernel_digest()
-    traffic, sm_time = bench.profile_traffic("llama3.1_8b_block"), bench.profile_sm_time("llama3.1_8b_block")
-    for name, value in (("rs_fold_llama3.1_8b_block_traffic.txt", traffic),
-                        ("sm_time_llama3.1_8b_block.txt", sm_time)):
+    traffic = bench.profile_traffic("qwen3_30b_a3b_moe_layer")
+    sm_time = bench.profile_sm_time("qwen3_30b_a3b_moe_layer")  # falls back to the reduced case
+    for name, value in (("rs_fold_qwen3_30b_a3b_moe_layer_traffic.txt", traffic),
+                        ("sm_time_llama3.1_8b_attn.txt", sm_time)):
         recorded = (bench._profile_kv(name) or {}).get("rs_fold_cu_sha256_16")
         assert (value is not None) == (recorded == digest), name
     if traffic is not None:
-        assert 4.0e9 < traffic < 5.0e9  # algorithmic bytes per launch: 4.36 GB
+        assert 40.0e9 < traffic < 45.0e9  # algorithmic bytes per launch: 42.37 GB
     if sm_time is not None:
-        assert sm_time["ratio"] > 10
+        assert sm_time["workload"] == "llama3.1_8b_attn" and sm_time["ratio"] > 5
