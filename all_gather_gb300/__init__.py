@@ -63,8 +63,8 @@ def _param_descs(grads, offsets=None, require_cuda=True, dtype=None):
                 raise ValueError(f"gradient [{u}][{p}] shape {tuple(t.shape)} != rank 0's {tuple(t0.shape)}")
             if not t.is_contiguous():
                 raise ValueError(f"gradient [{u}][{p}] is not contiguous")
-            if require_cuda and t.numel() and not t.is_cuda:
-                raise ValueError(f"gradient [{u}][{p}] is not on a CUDA device")
+            if require_cuda and t.numel() and not (t.is_cuda or t.is_pinned()):
+                raise ValueError(f"gradient [{u}][{p}] is neither on a CUDA device nor in page-locked host memory")
             ptrs.append(t.data_ptr())
         d0 = t0.shape[0]
         k = t0.numel() // d0 if d0 else int(torch.Size(t0.shape[1:]).numel())
@@ -92,8 +92,9 @@ class FullParams:
 class Plan:
     """A built plan for one parameter group (owns the plan's device tables).
 
-    ``grads[u][p]``: bf16 gradient of parameter p on virtual rank u (CUDA,
-    contiguous, same shape on every rank).
+    ``grads[u][p]``: bf16 gradient of parameter p on virtual rank u (CUDA or
+    page-locked host memory, contiguous, same shape on every rank; gradients in
+    host memory are read in place over the host link).
     """
 
     def __init__(self, grads: Sequence[Sequence], flags: Optional[PlanFlags] = None, stream=None,

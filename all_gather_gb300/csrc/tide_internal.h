@@ -174,6 +174,7 @@ struct tide_plan {
     bool whole_sm = false;               // bulk kernel: at most one CTA per SM (deeper ring)
     int consumer_warps = tide::kBulkConsumerWarps;  // bulk kernel: consumer warps per CTA
     bool host_only = false;
+    bool host_grads = false;             // some gradients are page-locked host memory (direct kernel only)
     int device = -1;
     uintptr_t src_lo = 0, src_hi = 0;    // hull of all gradient ranges
     // device side

@@ -154,6 +154,48 @@ tide_status_t load_pointers(tide_plan_t *plan, const tide_param_desc_t *params)
     return TIDE_OK;
 }
 
+// Where the gradients live.  Device memory of the plan's device and managed
+// memory are read by either kernel; page-locked host memory mapped into the
+// device's address space is read in place over the host link (NVLink-C2C on
+// Grace systems) by the direct-load kernel, whose plain loads reach it (the
+// bulk-copy kernel is not used on host memory); pageable host memory cannot
+// be read by a kernel and is refused.  *host: some gradient is host memory.
+tide_status_t classify_gradients(const tide_plan_t *plan, bool *host)
+{
+    *host = false;
+    for (int32_t p = 0; p < plan->nparams; ++p) {
+        if (plan->dim0[p] * plan->row_numel[p] == 0)
+            continue;
+        for (int32_t u = 0; u < plan->world; ++u) {
+            void *ptr = reinterpret_cast<void *>(plan->ptrs[size_t(p) * plan->world + u]);
+            cudaPointerAttributes a{};
+            cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                return fail(TIDE_ERR_INVALID_ARG, "params[%d].rank_base[%d]: %s", p, u, cudaGetErrorString(e));
+            }
+            if (a.type == cudaMemoryTypeHost) {
+                if (a.devicePointer != ptr)
+                    return fail(TIDE_ERR_INVALID_ARG,
+                                "params[%d].rank_base[%d] is page-locked host memory not mapped at the same address "
+                                "on the device",
+                                p, u);
+                *host = true;
+            } else if (a.type == cudaMemoryTypeDevice) {
+                if (a.device != plan->device)
+                    return fail(TIDE_ERR_INVALID_ARG, "params[%d].rank_base[%d] is memory of device %d, not %d", p, u,
+                                a.device, plan->device);
+            } else if (a.type != cudaMemoryTypeManaged) {
+                return fail(TIDE_ERR_INVALID_ARG,
+                            "params[%d].rank_base[%d] is pageable host memory: a kernel cannot read it "
+                            "(use device, managed or page-locked host memory)",
+                            p, u);
+            }
+        }
+    }
+    return TIDE_OK;
+}
+
 bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
 
 // Does [lo, hi) overlap any gradient tensor of the plan?
@@ -426,6 +468,17 @@ static tide_status_t plan_build_impl(int32_t world, int32_t num_params, const ti
     if (e != cudaSuccess)
         return bail(cuda_fail(e, "query SM count"));
     plan->sms = sms;
+    st = classify_gradients(plan, &plan->host_grads);
+    if (st != TIDE_OK)
+        return bail(st);
+    if (plan->host_grads) {
+        if (f.kernel == TIDE_KERNEL_BULK || f.order != TIDE_ORDER_RANK_ASC || f.grad_dtype != TIDE_DTYPE_BF16)
+            return bail(fail(TIDE_ERR_UNSUPPORTED,
+                             "gradients in host memory are folded by the direct-load kernel (bf16, rank order)"));
+        plan->kernel = TIDE_KERNEL_DIRECT;
+        plan->block = tide::kFoldThreads;
+        plan->fold_smem = tide::fold_smem_bytes(TIDE_KERNEL_DIRECT, world, 0, 0, false);
+    }
     plan->whole_sm = plan->kernel == TIDE_KERNEL_BULK && f.cta_budget > 0 && f.cta_budget <= sms;
     if (plan->whole_sm)
         plan->fold_smem = tide::fold_smem_bytes(plan->kernel, world, f.fill_bytes / plan->elem_bytes, f.fill_ranks,
@@ -522,8 +575,18 @@ static tide_status_t plan_rebind_impl(tide_plan_t *plan, const tide_param_desc_t
     if (plan->host_only)
         return TIDE_OK;
     st = check_device(plan);
-    if (st != TIDE_OK)
+    bool host = false;
+    if (st == TIDE_OK)
+        st = classify_gradients(plan, &host);
+    if (st == TIDE_OK && host != plan->host_grads)
+        st = fail(TIDE_ERR_INVALID_ARG, "rebind cannot move gradients between host and device memory");
+    if (st != TIDE_OK) {
+        plan->ptrs.swap(keep_ptrs);
+        plan->segs.swap(keep_segs);
+        plan->src_lo = keep_lo;
+        plan->src_hi = keep_hi;
         return st;
+    }
     return upload_tables(plan, static_cast<cudaStream_t>(stream), true);
 }
 

@@ -559,12 +559,15 @@ def fold_record(w, rs_ms, peak):
             "p50_ms": pct(rs_ms, 0.5), "p90_ms": pct(rs_ms, 0.9), "thirds": thirds(rs_ms)}
 
 
-def graph_step(plan, w, out, slots, full_b, steps, step_bytes):
+def graph_step(plan, w, out, slots, full_b, steps, step_bytes, overlap=False):
     """The step (fold + placement) captured once in a CUDA graph and replayed:
     the time of the two kernels without the host's per-call enqueue, which
-    bounds small groups when launched one call at a time."""
+    bounds small groups when launched one call at a time.  overlap: the
+    placement runs on a second stream of the graph, beside the fold (the two
+    touch disjoint buffers, as a layer's reduce-scatter and the next layer's
+    all-gather do)."""
     import torch
-    side = torch.cuda.Stream()
+    side, side2 = torch.cuda.Stream(), torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):  # warm-up outside the capture
         plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
@@ -572,8 +575,13 @@ def graph_step(plan, w, out, slots, full_b, steps, step_bytes):
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=side):
+        if overlap:
+            side2.wait_stream(side)
         plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
-        plan.ag_place(slots, full_b, mode="sm")
+        with torch.cuda.stream(side2 if overlap else side):
+            plan.ag_place(slots, full_b, mode="sm")
+        if overlap:
+            side.wait_stream(side2)
     stream = torch.cuda.current_stream()
     for _ in range(3):
         g.replay()
@@ -586,8 +594,9 @@ def graph_step(plan, w, out, slots, full_b, steps, step_bytes):
     ms = [a.elapsed_time(b) for a, b in ev]
     mean = sum(ms) / steps
     del g
+    what = "tide_rs_fold + tide_ag_place captured once, graph replayed"
     return {"ms": round(mean, 4), "p50_ms": pct(ms, 0.5), "gbs": round(step_bytes / (mean * 1e-3) / 1e9, 1),
-            "what": "tide_rs_fold + tide_ag_place captured once, graph replayed"}
+            "what": what + (", placement on a second stream beside the fold" if overlap else "")}
 
 
 def measure_config(w, dev, steps, peak, gs=None, baseline=True):
@@ -619,6 +628,7 @@ def measure_config(w, dev, steps, peak, gs=None, baseline=True):
                          "p50_ms": pct(ag_ms, 0.5)},
            "step": {"ms": round(total / steps, 4), "gbs": round((rs_b + ag_b) / (total / steps * 1e-3) / 1e9, 1)}}
     rec["step_graph"] = graph_step(plan, w, out, slots, full_b, steps, rs_b + ag_b)
+    rec["step_graph_overlapped"] = graph_step(plan, w, out, slots, full_b, steps, rs_b + ag_b, overlap=True)
     if baseline:
         b = baselines.time_two_pass(w, gs.views, S, out, slots, full, steps=min(steps, 5))
         b["fused_speedup_rs"] = round(b["rs_ms"] / rec["fold"]["p50_ms"], 3)
@@ -880,13 +890,15 @@ def time_variants(plan, w, S, slots, full, dev, gs_views, steps: int = 20) -> di
 
 
 def e2e(args, w, gs, plan, S, out, dev, world):
-    """The metric end to end through the public API with host buffers: every
-    step uploads its W gradient sets (and, when accumulating, the old fp32
-    shards) from pinned host memory, runs tide_rs_fold, and reads the fp32
-    shards back.  Steps are pipelined over two device buffer sets on three
-    streams (upload, fold, read-back), so the host link carries both
-    directions at once; the value is the reduce-scatter's algorithmic bytes
-    over the time per step."""
+    """The metric end to end through the public API with host buffers.  Every
+    step's W gradient sets start in pinned host memory and its fp32 shards end
+    there.  Main form: a plan built on the host gradients folds them in place,
+    reading them over the host link (NVLink-C2C on Grace), and each step's
+    shards are read back while the next step folds (two device output
+    buffers).  For comparison (`staged`): the copy engines upload the
+    gradients to device buffers every step and the device-resident plan folds
+    them (two device buffer sets on upload / fold / read-back streams).  The
+    value is the reduce-scatter's algorithmic bytes over the time per step."""
     import os
 
     import torch
@@ -900,7 +912,10 @@ def e2e(args, w, gs, plan, S, out, dev, world):
     if use:
         os.sched_setaffinity(0, use)
     try:
-        res = _e2e_run(args, w, gs, plan, S, out, dev, world)
+        h_arenas = [_pinned_copy(a) for a in gs.arenas]  # every step's inputs: the same bytes
+        res = _e2e_in_place(args, w, gs, h_arenas, S, out, dev, world)
+        res["staged"] = _e2e_staged(args, w, gs, h_arenas, plan, S, out, dev, world)
+        del h_arenas
     finally:
         os.sched_setaffinity(0, saved)
     res["host_cpus"] = {"gpu_local": cpu_ranges(local) if local else None,
@@ -916,14 +931,74 @@ def _pinned_copy(t):
     return h
 
 
-def _e2e_run(args, w, gs, plan, S, out, dev, world):
+def _e2e_in_place(args, w, gs, h_arenas, S, out, dev, world):
+    import torch
+    import torch.distributed as dist
+
+    import all_gather_gb300 as tide
+    K = max(2, args.e2e_steps)
+    # the host gradients as per-parameter views into the pinned arenas (the device layout)
+    h_views = [[h[o:o + v.numel()].view(v.shape) for o, v in zip(gs.offsets, gs.views[u])]
+               for u, h in enumerate(h_arenas)]
+    plan_h = tide.Plan(h_views)  # gradients in host memory: folded in place over the host link
+    h_out0 = _pinned_copy(out)
+    outs = [torch.empty_like(out) for _ in range(2)]
+    h_outs = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+    h2d = sum(a.numel() * a.element_size() for a in h_arenas) + (h_out0.numel() * 4 if w.accumulate else 0)
+    d2h = h_out0.numel() * 4
+    s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("comp", "out")}
+
+    def step(i, first):
+        b = i % 2
+        with torch.cuda.stream(s_comp):
+            if not first[b]:
+                s_comp.wait_event(ev["out"][b])  # the shards of set b were read back
+            if w.accumulate:
+                outs[b].copy_(h_out0, non_blocking=True)
+            plan_h.rs_fold(outs[b], alpha=w.alpha, accumulate=w.accumulate, stream=s_comp)
+            ev["comp"][b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["comp"][b])
+            h_outs[b].copy_(outs[b], non_blocking=True)
+            ev["out"][b].record(s_out)
+        first[b] = False
+
+    first = [True, True]
+    for i in range(2):
+        step(i, first)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(s_comp)
+    for i in range(K):
+        step(i, first)
+    s_out.wait_stream(s_comp)
+    end.record(s_out)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(end) / K, world, dev)
+    last = (K - 1) % 2
+    ok = torch.equal(h_outs[last], outs[last].cpu())  # read-back == on-device result
+    plan_h.close()
+    del outs, h_outs, h_out0, h_views
+    torch.cuda.empty_cache()
+    return {"value": round(whole_job_gbs(rs_alg_bytes(w, w.total_numel()), world, ms), 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "steps": K,
+            "readback_matches_device": ok,
+            "mode": "gradients read in place from pinned host memory by tide_rs_fold (over the host link, no "
+                    "staging copy); fp32 shards -> pinned host every step",
+            "note": "h2d bytes: the gradients the fold reads from host memory each step (+ old shards when "
+                    "accumulating)"}
+
+
+def _e2e_staged(args, w, gs, h_arenas, plan, S, out, dev, world):
     import torch
     import torch.distributed as dist
 
     import all_gather_gb300 as tide
     import workloads
     K = max(2, args.e2e_steps)
-    h_arenas = [_pinned_copy(a) for a in gs.arenas]  # one set: every step uploads the same bytes
     h_out0 = _pinned_copy(out)
     h_outs = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
     gs2 = workloads.make_grads(w, device=dev)  # the second device buffer set has its own arenas and plan
@@ -971,14 +1046,14 @@ def _e2e_run(args, w, gs, plan, S, out, dev, world):
     end.record(s_out)
     torch.cuda.synchronize()
     ms = max_over_ranks(start.elapsed_time(end) / K, world, dev)
-    ok = torch.equal(h_outs[(K - 1) % 2], sets[(K - 1) % 2][2].cpu())  # read-back == on-device result
+    ok = torch.equal(h_outs[(K - 1) % 2], sets[(K - 1) % 2][2].cpu())
     plan2.close()
-    del gs2, sets, h_arenas, h_outs, h_out0
+    del gs2, sets, h_outs, h_out0
     torch.cuda.empty_cache()
     return {"value": round(whole_job_gbs(rs_alg_bytes(w, w.total_numel()), world, ms), 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "steps": K,
             "readback_matches_device": ok,
-            "note": "per step: pinned host gradients (+ old shards when accumulating) -> device, tide_rs_fold, "
+            "mode": "pinned host gradients -> device by the copy engines, tide_rs_fold on the device copies, "
                     "fp32 shards -> pinned host; two device buffer sets, upload / fold / read-back streams"}
 
 

@@ -81,11 +81,17 @@ typedef struct tide_plan tide_plan_t;
 
 /* One parameter of the group (Section 2.1 notation). */
 typedef struct {
-    /* Host array of W device pointers: rank_base[u] is G_p^(u), the gradient
-     * of this parameter on virtual rank u (bf16, or fp32 with
-     * TIDE_DTYPE_F32), row-major and contiguous (dim0 * row_numel elements).
-     * Aligned to the element size; 16-byte alignment enables the vector and
-     * bulk-copy paths.  The array itself is copied during the call. */
+    /* Host array of W pointers: rank_base[u] is G_p^(u), the gradient of
+     * this parameter on virtual rank u (bf16, or fp32 with TIDE_DTYPE_F32),
+     * row-major and contiguous (dim0 * row_numel elements).  Each points to
+     * memory of the current device, managed memory, or page-locked host
+     * memory mapped into the device's address space at the same address
+     * (cudaHostAlloc; cudaHostRegister where the device uses host pointers):
+     * gradients in host memory are read in place over the host link
+     * (NVLink-C2C on Grace systems) by the direct-load kernel.  Pageable host
+     * memory is refused.  Aligned to the element size; 16-byte alignment
+     * enables the vector and bulk-copy paths.  The array itself is copied
+     * during the call. */
     const void *const *rank_base;
     int64_t dim0;          /* D_p >= 0: extent of dimension 0 (0 = empty tensor, pointers may be NULL) */
     int64_t row_numel;     /* K_p >= 0: product of the trailing dimensions (1 for a vector) */
@@ -208,10 +214,12 @@ typedef struct {
  * asynchronous copies on `stream`.  `params` is a host array; `flags` may be
  * NULL for defaults.  On success *plan_out owns the tables.
  * Errors: INVALID_ARG (world, counts, dims, null pointers, overlapping
- * explicit offsets, nonzero reserved fields, node_size not dividing world),
+ * explicit offsets, nonzero reserved fields, node_size not dividing world,
+ * a gradient in pageable host memory or in another device's memory),
  * ALIGNMENT (a gradient pointer not aligned to its element size),
  * UNSUPPORTED (a combination this build lacks: orders other than rank order
- * and fp32 gradients run on the bulk kernel only),
+ * and fp32 gradients run on the bulk kernel only; gradients in host memory
+ * take the direct-load kernel, so bf16 in rank order only),
  * OOM, CUDA.
  */
 TIDE_API tide_status_t tide_plan_build(int32_t world, int32_t num_params, const tide_param_desc_t *params,
@@ -220,8 +228,9 @@ TIDE_API tide_status_t tide_plan_build(int32_t world, int32_t num_params, const 
 /*
  * Point an existing plan at new gradient storage with the same geometry (for
  * example, the next step's gradients).  dim0, row_numel and shard_offset must
- * equal the plan's.  The new pointer table is uploaded on `stream`, ordered
- * after earlier work on that stream.
+ * equal the plan's, and the gradients must stay in the same kind of memory
+ * (device or host) as at build.  The new pointer table is uploaded on
+ * `stream`, ordered after earlier work on that stream.
  */
 TIDE_API tide_status_t tide_plan_rebind(tide_plan_t *plan, const tide_param_desc_t *params, void *stream);
 

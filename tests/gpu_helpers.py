@@ -73,13 +73,15 @@ def sampled_rs_check(world: int, dims, grads_uv, out_before: torch.Tensor, out_a
 
 
 def full_rs_check(world: int, dims, grads_uv, out_before, out_after: torch.Tensor, alpha: float,
-                  accumulate: bool, what: str = "", window: int = 1 << 20) -> int:
+                  accumulate: bool, what: str = "", window: int = 1 << 20, order: str = "rank",
+                  node_size: int = 0) -> int:
     """Compare EVERY output element of a fold with the oracle, one parameter at
     a time (host memory stays at one parameter's W gradients): the W gradient
     tensors and the W output windows come to the host, the unchanged oracle
-    (oracle.rs_window, Eq. (3) + (5)) recomputes each (rank, window of at most
-    `window` elements) on all host cores, and the two are compared bit for
-    bit.  Returns the number of elements compared (W * S for prefix offsets)."""
+    (oracle.rs_window, Eq. (3) + (5); rs_window_ex for another order or fp32
+    gradients) recomputes each (rank, window of at most `window` elements) on
+    all host cores, and the two are compared bit for bit.  Returns the number
+    of elements compared (W * S for prefix offsets)."""
     orc = oracle.load()
     R, o, S = orc.geometry(world, dims)
     threads = max(1, len(os.sched_getaffinity(0)))
@@ -89,7 +91,9 @@ def full_rs_check(world: int, dims, grads_uv, out_before, out_after: torch.Tenso
             n = R[p] * k
             if n == 0:
                 continue
-            host = [bits16(grads_uv[u][p]) for u in range(world)]
+            f32 = grads_uv[0][p].dtype == torch.float32
+            host = [grads_uv[u][p].detach().reshape(-1).cpu().numpy() if f32 else bits16(grads_uv[u][p])
+                    for u in range(world)]
             got = out_after[:, o[p]:o[p] + n].cpu().numpy()
             old = out_before[:, o[p]:o[p] + n].cpu().numpy() if accumulate else None
             want = np.empty((world, n), dtype=np.float32)
@@ -103,8 +107,12 @@ def full_rs_check(world: int, dims, grads_uv, out_before, out_after: torch.Tenso
             def run(job):
                 r, a, b, nv = job
                 srcs = [h[r * n + a:r * n + a + nv] for h in host]
-                want[r, a:b] = orc.rs_window(srcs, nv, (b - a) - nv, alpha, accumulate,
-                                             old[r, a:b] if accumulate else None)
+                o_win = old[r, a:b] if accumulate else None
+                if order == "rank" and not f32:
+                    want[r, a:b] = orc.rs_window(srcs, nv, (b - a) - nv, alpha, accumulate, o_win)
+                else:
+                    want[r, a:b] = orc.rs_window_ex(srcs, nv, (b - a) - nv, alpha, accumulate, r, order,
+                                                    node_size, o_win)
 
             list(pool.map(run, jobs))
             if not np.array_equal(got.view(np.uint32), want.view(np.uint32)):

@@ -14,7 +14,7 @@ import all_gather_gb300 as tide
 import oracle
 import workloads
 from bits import assert_same_bf16, assert_same_f32, assert_same_u16, bf16_bits_to_f32, f32_to_bf16_bits
-from gpu_helpers import (ag_expected, bits16, oracle_rs_full, sampled_rs_check, sentinel_slots)
+from gpu_helpers import (ag_expected, bits16, full_rs_check, oracle_rs_full, sampled_rs_check, sentinel_slots)
 
 U = 2.0 ** -24  # half an ulp of 1.0 in binary32
 
@@ -896,7 +896,7 @@ def test_parameter_beyond_2g_elements():
 @pytest.mark.parametrize("index", [2, 5])
 def test_full_size_orders_and_fp32(index):
     """Full-size groups: the Section 4.3 orders, the tree order and fp32
-    gradients, sampled windows recomputed by the oracle in the same order."""
+    gradients, every output element recomputed by the oracle in the same order."""
     w = workloads.get(index)
     dims = w.dim0_rownumel()
     gs = workloads.make_grads(w, device="cuda")
@@ -904,13 +904,15 @@ def test_full_size_orders_and_fp32(index):
     L = w.world // 2
     for order, oname, ns in ((tide.TIDE_ORDER_STAGED_OWN, "staged", 0), (tide.TIDE_ORDER_NODES, "nodes", L),
                              (tide.TIDE_ORDER_TREE, "tree", 0)):
-        out = torch.empty(w.world, S, device="cuda")
+        out = torch.full((w.world, S), float("nan"), device="cuda")
         with tide.Plan(gs.views, tide.make_flags(order=order, node_size=ns)) as plan:
             plan.rs_fold(out, alpha=w.alpha)
             torch.cuda.synchronize()
-        n = sampled_rs_check(w.world, dims, gs.views, None, out, w.alpha, False, seed=index,
-                             what=f"{w.name} {oname}", order=oname, node_size=ns)
-        assert n > 0
+            assert plan.device_status() == tide.TIDE_OK
+        n = full_rs_check(w.world, dims, gs.views, None, out, w.alpha, False, what=f"{w.name} {oname}",
+                          order=oname, node_size=ns)
+        assert n == w.world * S
+        del out
     # fp32 gradients (the bf16 values plus a small fp32 perturbation), accumulate mode
     views32 = [[v.float() + 1e-6 * torch.randn(v.shape, device="cuda") for v in vs] for vs in gs.views]
     del gs
@@ -919,8 +921,8 @@ def test_full_size_orders_and_fp32(index):
     with tide.Plan(views32, tide.make_flags(grad_dtype=tide.TIDE_DTYPE_F32)) as plan:
         plan.rs_fold(out, alpha=1.0 / w.world, accumulate=True)
         torch.cuda.synchronize()
-    n = sampled_rs_check(w.world, dims, views32, before, out, 1.0 / w.world, True, seed=index + 1,
-                         what=f"{w.name} fp32 grads")
-    assert n > 0
+        assert plan.device_status() == tide.TIDE_OK
+    n = full_rs_check(w.world, dims, views32, before, out, 1.0 / w.world, True, what=f"{w.name} fp32 grads")
+    assert n == w.world * S
     del views32, out, before
     torch.cuda.empty_cache()
