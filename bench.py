@@ -906,6 +906,15 @@ def e2e(args, w, gs, plan, S, out, dev, world):
     # the allocating thread runs, and a GB300 tray has two Grace CPUs, each
     # attached to its own GPUs; buffers on the far one cross the CPU-to-CPU
     # link on every copy.
+    def pow2(n):  # torch's pinned-memory allocator rounds each block up to a power of two
+        return 1 << max(0, int(n - 1).bit_length())
+    grad_bytes = sum(pow2(a.numel() * a.element_size()) for a in gs.arenas)
+    out_bytes = pow2(out.numel() * 4)
+    need = grad_bytes + 3 * out_bytes  # pinned: the gradients, the old shards, two read-back buffers
+    avail = host_mem_available() // max(1, int(os.environ.get("LOCAL_WORLD_SIZE", "1")))
+    if need * 1.25 > avail:
+        return {"skipped": f"host memory: the pinned buffers need {need / 1e9:.1f} GB, "
+                           f"{avail / 1e9:.1f} GB available to this rank", "unit": UNIT}
     saved = os.sched_getaffinity(0)
     local = gpu_local_cpus(torch.device(dev).index or 0)
     use = (local & saved) if local else None
@@ -914,13 +923,26 @@ def e2e(args, w, gs, plan, S, out, dev, world):
     try:
         h_arenas = [_pinned_copy(a) for a in gs.arenas]  # every step's inputs: the same bytes
         res = _e2e_in_place(args, w, gs, h_arenas, S, out, dev, world)
-        res["staged"] = _e2e_staged(args, w, gs, h_arenas, plan, S, out, dev, world)
+        if world == 1:  # the comparison needs a second device copy of the gradients: one GPU only
+            res["staged"] = _e2e_staged(args, w, gs, h_arenas, plan, S, out, dev, world)
         del h_arenas
     finally:
         os.sched_setaffinity(0, saved)
     res["host_cpus"] = {"gpu_local": cpu_ranges(local) if local else None,
                         "used": cpu_ranges(use) if use else cpu_ranges(saved)}
     return res
+
+
+def host_mem_available() -> int:
+    """MemAvailable of /proc/meminfo in bytes (0 if unknown)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except (OSError, ValueError, IndexError):
+        pass
+    return 0
 
 
 def _pinned_copy(t):

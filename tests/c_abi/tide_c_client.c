@@ -102,6 +102,9 @@ static int host_checks(void)
     int32_t count[8], step[8];
     CHECK(tide_bruck_schedule(5, count, step, 8) == 3, "rounds");
     CHECK(count[0] == 1 && count[1] == 2 && count[2] == 1 && step[2] == 4, "recursive doubling counts");
+    /* Section 2.2, Equation (4): 36 slots, 128 CTAs in clusters of 4 -> (36 - 32) * 4 */
+    CHECK(tide_corun_cta_budget(36, 128, 4) == 16, "co-run budget");
+    CHECK(tide_corun_cta_budget(32, 128, 4) == 0 && tide_corun_cta_budget(0, 128, 4) == -1, "co-run budget edges");
     return 0;
 }
 
@@ -166,15 +169,27 @@ static int gpu_checks(void)
     CHECK(tide_rs_fold(plan, d_out, stride, 1.0f, 1, NULL) == TIDE_OK, "fold, accumulate");
     CUDA_OK(cudaMemcpy(h_out, d_out, sizeof(float) * (size_t)(W * stride), cudaMemcpyDeviceToHost));
     CHECK(tide_last_device_status(plan, NULL) == TIDE_OK, "device status");
+    /* the allocation-free fold on the same group: the same bits, and its own status word */
+    float h_out2[WMAX * 40];
+    float *d_out2;
+    CUDA_OK(cudaMalloc((void **)&d_out2, sizeof h_out2));
+    CUDA_OK(cudaMemset(d_out2, 0, sizeof(float) * (size_t)(W * stride)));
+    CHECK(tide_rs_fold_noalloc(W, P, desc, d_out2, stride, 0.25f, 0, NULL) == TIDE_OK, "allocation-free fold");
+    CHECK(tide_rs_fold_noalloc(W, P, desc, d_out2, stride, 1.0f, 1, NULL) == TIDE_OK, "allocation-free, accumulate");
+    CUDA_OK(cudaMemcpy(h_out2, d_out2, sizeof(float) * (size_t)(W * stride), cudaMemcpyDeviceToHost));
+    CHECK(tide_last_device_status(NULL, NULL) == TIDE_OK, "allocation-free fold's device status");
     const uint16_t *gp[P * WMAX];
     for (int p = 0; p < P; ++p)
         for (int u = 0; u < W; ++u)
             gp[p * W + u] = h_grads[p][u];
     CHECK(oracle_rs(W, P, kDim0, kRowNumel, gp, 0.25f, 0, want, stride) == 0, "oracle");
     CHECK(oracle_rs(W, P, kDim0, kRowNumel, gp, 1.0f, 1, want, stride) == 0, "oracle, accumulate");
-    for (int r = 0; r < W; ++r)
+    for (int r = 0; r < W; ++r) {
         CHECK(memcmp(h_out + r * stride, want + r * stride, sizeof(float) * (size_t)S) == 0,
               "fold differs from the oracle in rank slot %d", r);
+        CHECK(memcmp(h_out2 + r * stride, want + r * stride, sizeof(float) * (size_t)S) == 0,
+              "allocation-free fold differs from the oracle in rank slot %d", r);
+    }
 
     /* placement on the SM kernel and on the copy engines */
     uint16_t h_slots[WMAX * 40];
@@ -215,6 +230,7 @@ static int gpu_checks(void)
         free(h_full[p]);
     }
     CUDA_OK(cudaFree(d_out));
+    CUDA_OK(cudaFree(d_out2));
     CUDA_OK(cudaFree(d_slots));
     return 0;
 }
