@@ -33,8 +33,15 @@ AG_MODES = {"sm": TIDE_AG_SM, "ce2d": TIDE_AG_CE_2D, "ce1d": TIDE_AG_CE_1D}
 
 
 def _stream_handle(stream) -> int:
+    """cudaStream_t of `stream` (a torch stream or a raw handle); None = the
+    current stream of the current device (read through torch's raw accessor
+    when it has one: a fraction of the cost of building a Stream object, which
+    matters for groups small enough to be bound by the host's enqueue)."""
     import torch
     if stream is None:
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return raw(torch._C._cuda_getDevice())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream

@@ -254,7 +254,7 @@ extern "C" tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params,
     fp.stride = out_slot_stride;
     fp.alpha = alpha;
     fp.world = world;
-    fp.sched = TIDE_SCHED_DYNAMIC;  // the default schedule, as tide_plan_build resolves it
+    fp.sched = TIDE_SCHED_DYNAMIC;  // the default schedule, resolved below as tide_plan_build does
     fp.counters = reinterpret_cast<uint32_t *>(scratch + kCountersAt);
     fp.status = reinterpret_cast<int32_t *>(scratch);
     fp.wait_budget_ns = tide::kWaitBudgetNs;
@@ -272,7 +272,10 @@ extern "C" tide_status_t tide_rs_fold_noalloc(int32_t world, int32_t num_params,
     e = tide::fold_occupancy(TIDE_KERNEL_BULK, world, tide::kBulkThreads, bs.smem_bytes, &per_sm);
     if (e != cudaSuccess)
         return noalloc_fail(TIDE_ERR_CUDA, "launch geometry: %s", cudaGetErrorString(e));
-    const int grid = int(std::min<int64_t>(int64_t(std::max(per_sm, 1)) * sms, n_items));
+    const int64_t wave = int64_t(std::max(per_sm, 1)) * sms;
+    if (n_items <= wave)
+        fp.sched = TIDE_SCHED_STATIC;  // every CTA gets at most one work item: no claims needed
+    const int grid = int(std::min<int64_t>(wave, n_items));
     e = tide::launch_fold(fp, TIDE_KERNEL_BULK, accumulate, grid, tide::kBulkThreads, bs.smem_bytes, stream);
     if (e != cudaSuccess)
         return noalloc_fail(TIDE_ERR_CUDA, "fold launch: %s", cudaGetErrorString(e));

@@ -343,8 +343,12 @@ static tide_status_t plan_build_impl(int32_t world, int32_t num_params, const ti
         delete plan;
         return s;
     };
-    if (f.sched == TIDE_SCHED_AUTO)
-        f.sched = TIDE_SCHED_DYNAMIC;  // faster than the static split on every benchmark group
+    // The default schedule: dynamic claims (2-6% faster than the static split
+    // on the benchmark groups), or static when every CTA gets at most one
+    // work item (then a claim only adds latency); settled once the grid is known.
+    const bool auto_sched = f.sched == TIDE_SCHED_AUTO;
+    if (auto_sched)
+        f.sched = TIDE_SCHED_DYNAMIC;
     plan->world = world;
     plan->nparams = num_params;
     plan->flags = f;
@@ -495,6 +499,8 @@ static tide_status_t plan_build_impl(int32_t world, int32_t num_params, const ti
         return bail(fail(TIDE_ERR_UNSUPPORTED, "fold kernel does not fit on an SM (world %d)", world));
     plan->grid = f.sched == TIDE_SCHED_PER_ITEM ? int32_t(std::max<size_t>(plan->rs_items.size(), 1))
                  : f.cta_budget ? f.cta_budget : sms * per_sm;
+    if (auto_sched && int64_t(plan->rs_items.size()) <= int64_t(plan->grid))
+        plan->flags.sched = TIDE_SCHED_STATIC;
 
     size_t off = 0;
     auto carve = [&](size_t bytes) {

@@ -618,7 +618,18 @@ def measure_config(w, dev, steps, peak, gs=None, baseline=True):
     full_b = plan.bind_full(full)
     stream = torch.cuda.current_stream()
     timed_steps(plan, w, out, slots, full_b, "sm", 3, stream)
-    rs_ms, ag_ms, total = timed_steps(plan, w, out, slots, full_b, "sm", steps, stream)
+    rs_ms, ag_ms, _ = timed_steps(plan, w, out, slots, full_b, "sm", steps, stream)
+    # the step alone, events only around the whole region (per-part events cost
+    # host time that small groups would otherwise measure)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        plan.rs_fold(out, alpha=w.alpha, accumulate=w.accumulate)
+        plan.ag_place(slots, full_b, mode="sm")
+    end.record(stream)
+    torch.cuda.synchronize()
+    total = start.elapsed_time(end)
     numel = w.total_numel()
     rs_b, ag_b = alg_bytes(w, numel)
     ag_mean = sum(ag_ms) / steps

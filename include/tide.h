@@ -121,7 +121,8 @@ enum {
 
 /* Work distribution of the fold's persistent grid (bitwise identical results). */
 enum {
-    TIDE_SCHED_AUTO = 0,     /* the library's default: TIDE_SCHED_DYNAMIC */
+    TIDE_SCHED_AUTO = 0,     /* the library's default: TIDE_SCHED_DYNAMIC, or TIDE_SCHED_STATIC
+                                when every CTA of the grid gets at most one work item */
     TIDE_SCHED_DYNAMIC = 1,  /* CTAs claim items from a device counter that resets itself (bulk
                                 kernel: the producer lane claims each item and posts it to the
                                 CTA's consumer warps), so faster SMs take more items: 2-6% faster

@@ -629,9 +629,13 @@ def test_ag_shard_roundtrip_identity():
             assert_same_u16(bits16(f), bits16(x), f"AG(shard(x)) {mode} p={p}")
 
 
-def test_graph_captured_step():
+@pytest.mark.parametrize("kw", [{}, {"sched": tide.TIDE_SCHED_DYNAMIC},
+                                {"sched": tide.TIDE_SCHED_DYNAMIC, "cta_budget": 3}],
+                         ids=["default", "dynamic", "dynamic_3ctas"])
+def test_graph_captured_step(kw):
     """The step (fold, placement, mixed-precision placement) captured once in a
-    CUDA graph and replayed on new inputs copied into the same buffers."""
+    CUDA graph and replayed on new inputs copied into the same buffers; with
+    the dynamic schedule every replay must find the claim counters reset."""
     w = workloads.get(1)
     dims = w.dim0_rownumel()
     g1 = workloads.make_grads(w, device="cuda")
@@ -642,7 +646,7 @@ def test_graph_captured_step():
     slots32 = torch.randn(w.world, S, device="cuda")
     full = [torch.empty(s_, dtype=torch.bfloat16, device="cuda") for s_ in w.shapes]
     full32 = [torch.empty_like(f) for f in full]
-    with tide.Plan(g1.views) as plan:
+    with tide.Plan(g1.views, tide.make_flags(**kw) if kw else None) as plan:
         plan.rs_fold(out, alpha=0.25)  # warm-up outside the capture
         plan.ag_place(slots, full)
         plan.ag_place_f32(slots32, full32)
