@@ -175,6 +175,7 @@ struct tide_plan {
     int consumer_warps = tide::kBulkConsumerWarps;  // bulk kernel: consumer warps per CTA
     bool host_only = false;
     bool host_grads = false;             // some gradients are page-locked host memory (direct kernel only)
+    std::vector<uint8_t> ptr_host;       // [P * W]: that gradient is page-locked host memory
     int device = -1;
     uintptr_t src_lo = 0, src_hi = 0;    // hull of all gradient ranges
     // device side

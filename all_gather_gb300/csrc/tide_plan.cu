@@ -159,15 +159,26 @@ tide_status_t load_pointers(tide_plan_t *plan, const tide_param_desc_t *params)
 // device's address space is read in place over the host link (NVLink-C2C on
 // Grace systems) by the direct-load kernel, whose plain loads reach it (the
 // bulk-copy kernel is not used on host memory); pageable host memory cannot
-// be read by a kernel and is refused.  *host: some gradient is host memory.
-tide_status_t classify_gradients(const tide_plan_t *plan, bool *host)
+// be read by a kernel and is refused.  kinds[i] = 1 for host memory; *host:
+// some gradient is host memory.  A pointer equal to prev[i] keeps
+// prev_kinds[i] without a query (a rebind to the same buffers costs nothing).
+tide_status_t classify_gradients(const tide_plan_t *plan, bool *host, std::vector<uint8_t> &kinds,
+                                 const std::vector<uint64_t> *prev = nullptr,
+                                 const std::vector<uint8_t> *prev_kinds = nullptr)
 {
     *host = false;
+    kinds.assign(plan->ptrs.size(), 0);
     for (int32_t p = 0; p < plan->nparams; ++p) {
         if (plan->dim0[p] * plan->row_numel[p] == 0)
             continue;
         for (int32_t u = 0; u < plan->world; ++u) {
-            void *ptr = reinterpret_cast<void *>(plan->ptrs[size_t(p) * plan->world + u]);
+            const size_t i = size_t(p) * plan->world + u;
+            if (prev && prev_kinds && prev_kinds->size() == kinds.size() && (*prev)[i] == plan->ptrs[i]) {
+                kinds[i] = (*prev_kinds)[i];
+                *host = *host || kinds[i];
+                continue;
+            }
+            void *ptr = reinterpret_cast<void *>(plan->ptrs[i]);
             cudaPointerAttributes a{};
             cudaError_t e = cudaPointerGetAttributes(&a, ptr);
             if (e != cudaSuccess) {
@@ -180,6 +191,7 @@ tide_status_t classify_gradients(const tide_plan_t *plan, bool *host)
                                 "params[%d].rank_base[%d] is page-locked host memory not mapped at the same address "
                                 "on the device",
                                 p, u);
+                kinds[i] = 1;
                 *host = true;
             } else if (a.type == cudaMemoryTypeDevice) {
                 if (a.device != plan->device)
@@ -472,7 +484,7 @@ static tide_status_t plan_build_impl(int32_t world, int32_t num_params, const ti
     if (e != cudaSuccess)
         return bail(cuda_fail(e, "query SM count"));
     plan->sms = sms;
-    st = classify_gradients(plan, &plan->host_grads);
+    st = classify_gradients(plan, &plan->host_grads, plan->ptr_host);
     if (st != TIDE_OK)
         return bail(st);
     if (plan->host_grads) {
@@ -582,10 +594,13 @@ static tide_status_t plan_rebind_impl(tide_plan_t *plan, const tide_param_desc_t
         return TIDE_OK;
     st = check_device(plan);
     bool host = false;
+    std::vector<uint8_t> kinds;
     if (st == TIDE_OK)
-        st = classify_gradients(plan, &host);
+        st = classify_gradients(plan, &host, kinds, &keep_ptrs, &plan->ptr_host);
     if (st == TIDE_OK && host != plan->host_grads)
         st = fail(TIDE_ERR_INVALID_ARG, "rebind cannot move gradients between host and device memory");
+    if (st == TIDE_OK)
+        plan->ptr_host.swap(kinds);
     if (st != TIDE_OK) {
         plan->ptrs.swap(keep_ptrs);
         plan->segs.swap(keep_segs);

@@ -73,6 +73,8 @@ def parse():
     ap.add_argument("--no-variants", action="store_true", help="skip timing the other placement variants")
     ap.add_argument("--no-per-config", action="store_true", help="skip timing the five workloads one by one")
     ap.add_argument("--interference-rs", type=int, default=10, help="reduce-scatters per interference co-run")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU baseline: seconds of single-threaded oracle work (half that on all cores)")
     return ap.parse_args()
 
 
@@ -786,9 +788,9 @@ def run_ours(args):
         idx = sample_params(w)
         host = [[gs.views[u][i].reshape(-1).view(torch.int16).cpu().numpy().view(np.uint16) for u in range(w.world)]
                 for i in idx]
-        result["cpu_baseline"] = cpu_oracle_sample(w, host, idx)
+        result["cpu_baseline"] = cpu_oracle_sample(w, host, idx, min_seconds=args.cpu_seconds)
         result["cpu_baseline"]["cpu"] = cpu_model()
-        result["cpu_baseline"]["all_cores"] = cpu_oracle_all_cores(w, host, idx)
+        result["cpu_baseline"]["all_cores"] = cpu_oracle_all_cores(w, host, idx, min_seconds=args.cpu_seconds / 2)
 
     plan.close()
     del out, slots, full, full_b
