@@ -786,8 +786,8 @@ __global__ void __launch_bounds__(32 * (1 + CW), CW == kBulkConsumerWarps ? 2 : 
                         stop = true;
                         break;
                     }
-                    if ((fp.debug & TIDE_DEBUG_SKIP_FILL) && blockIdx.x == 0 && fills == 0) {
-                        skipped = fills;  // leave this stage unfilled: its consumers' wait expires
+                    if ((fp.debug & TIDE_DEBUG_SKIP_FILL) && it == 0 && c == 0 && g == 0) {
+                        skipped = fills;  // leave work item 0's first stage unfilled: its consumers' wait expires
                     } else {
                         mbar_arrive_expect_tx(&full[stage], uint32_t(nr) * bytes);
                         if (bytes) {

@@ -166,8 +166,9 @@ enum {
 #define TIDE_DEBUG_HOST_ONLY 0x1u  /* build geometry and work list only: no device tables, no CUDA calls.
                                       Such a plan can be inspected but not launched. */
 #define TIDE_DEBUG_SHORT_WAIT 0x2u /* bulk kernel: bound each device-side wait by 50 ms instead of 4 s */
-#define TIDE_DEBUG_SKIP_FILL 0x4u  /* bulk kernel: CTA 0 never fills its first stage, so its consumers'
-                                      bounded wait expires; exercises the TIMEOUT status path.  The
+#define TIDE_DEBUG_SKIP_FILL 0x4u  /* bulk kernel: the CTA that takes work item 0 never fills that
+                                      item's first stage, so its consumers' bounded wait expires;
+                                      exercises the TIMEOUT status path (whatever the schedule).  The
                                       output of that fold is incomplete. */
 
 typedef struct {

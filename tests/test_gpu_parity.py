@@ -421,22 +421,39 @@ def test_random_flag_combinations(seed):
             assert_same_u16(bits16(f), wf[p], f"seed {seed}: ag {mode} p={p}")
 
 
-def test_bulk_wait_timeout_reports_status():
+@pytest.mark.parametrize("sched_kw", [{}, {"sched": tide.TIDE_SCHED_DYNAMIC},
+                                      {"sched": tide.TIDE_SCHED_DYNAMIC, "cta_budget": 3}],
+                         ids=["default", "dynamic", "dynamic_3ctas"])
+def test_bulk_wait_timeout_reports_status(sched_kw):
     """A bounded device-side wait that expires is reported as TIMEOUT and the
-    context stays usable: CTA 0 of the bulk kernel skips its first stage fill
-    (debug flag), its consumers give up after 50 ms, the producer drains the
-    copies it issued, and the kernel returns."""
+    context stays usable: the CTA that takes work item 0 skips that item's
+    first stage fill (debug flag), its consumers give up after 50 ms, the
+    producer drains the copies it issued, and the kernel returns.  A second
+    launch of the same plan times out the same way, which under the dynamic
+    schedule shows that the aborted launch reset the claim counters (else
+    item 0 would never be claimed again); a plan with the same schedule and no
+    planted skip then matches the oracle."""
     w = workloads.get(1)
     gs = workloads.make_grads(w, device="cuda")
     _, _, S = oracle.geometry(w.world, w.dim0_rownumel())
     flags = tide.make_flags(kernel=tide.TIDE_KERNEL_BULK,
-                            debug=tide.TIDE_DEBUG_SHORT_WAIT | tide.TIDE_DEBUG_SKIP_FILL)
+                            debug=tide.TIDE_DEBUG_SHORT_WAIT | tide.TIDE_DEBUG_SKIP_FILL, **sched_kw)
     out = torch.zeros(w.world, S, device="cuda")
     with tide.Plan(gs.views, flags) as plan:
-        plan.rs_fold(out, alpha=0.25)
-        torch.cuda.synchronize()
-        assert plan.device_status() == tide.TIDE_ERR_TIMEOUT
-        assert plan.device_status() == tide.TIDE_OK  # reading clears the word
+        for _ in range(2):
+            plan.rs_fold(out, alpha=0.25)
+            torch.cuda.synchronize()
+            assert plan.device_status() == tide.TIDE_ERR_TIMEOUT
+            assert plan.device_status() == tide.TIDE_OK  # reading clears the word
+    if sched_kw:  # the same schedule without the planted skip, twice on one plan: counters reset
+        with tide.Plan(gs.views, tide.make_flags(kernel=tide.TIDE_KERNEL_BULK, **sched_kw)) as plan:
+            want = oracle_rs_full(w.world, w.dim0_rownumel(), gs.views, 0.25, False, torch.zeros(w.world, S))
+            for _ in range(2):
+                out = torch.zeros(w.world, S, device="cuda")
+                plan.rs_fold(out, alpha=0.25)
+                torch.cuda.synchronize()
+                assert plan.device_status() == tide.TIDE_OK
+                assert_same_f32(out.cpu().numpy(), want, "dynamic schedule after a timeout")
     # the context is healthy: a normal fold still matches the oracle
     out = torch.zeros(w.world, S, device="cuda")
     _fold(w, gs.views, 0.25, False, out, kernel=tide.TIDE_KERNEL_BULK)
