@@ -175,7 +175,9 @@ typedef struct {
     int32_t cta_budget;   /* CTAs of the fold's persistent grid; 0 = one wave at full occupancy (two
                              bulk CTAs per SM).  A budget of at most the SM count gives each bulk
                              CTA an SM: a 192 KB ring and, except in the tree order, 8 consumer
-                             warps and 16 KB copies per rank (the fastest shape per SM) */
+                             warps and 16 KB copies per rank (the fastest shape per SM).  Next to
+                             a clustered GEMM, tide_corun_cta_budget gives the budget that keeps
+                             the GEMM in one wave */
     int32_t chunk_bytes;  /* bf16 bytes per rank in one work item (multiple of 256); 0 = default */
     int32_t order;        /* TIDE_ORDER_* */
     int32_t sched;        /* TIDE_SCHED_* */
