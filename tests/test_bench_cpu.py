@@ -91,3 +91,10 @@ def test_reference_arm_prints_the_contract_line():
     assert d["config"]["workload"] == "toy" and d["steps"] == 2 and d["warmup"] == 1
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_host_memory_probe():
+    """The e2e leg sizes its pinned buffers against MemAvailable before pinning them."""
+    import bench
+    avail = bench.host_mem_available()
+    assert avail > 0 and avail % 1024 == 0
