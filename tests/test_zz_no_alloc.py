@@ -12,6 +12,8 @@ by the library.  These tests call it through the C ABI and check:
   (the tolerance of every fold parity test: none);
 * a group whose ranks' rows differ in 16-byte phase (the fold's scalar path)
   and a 32-rank group (several shared-memory stage fills per chunk);
+* the full-size Llama-3.1-70B block and MoE layer, element for element equal
+  to the plan-based fold;
 * that after a warm-up call, further calls leave the device's free memory and
   torch's allocation count unchanged, and that the entry point's device
   status word reads TIDE_OK through tide_last_device_status(NULL, stream);
@@ -106,6 +108,29 @@ def test_noalloc_ranks_in_different_phases_and_32_ranks():
     g32 = workloads.make_grads(w32, device="cuda")
     _check(w32.world, g32.views, 1.0 / 32, False, stride_extra=5, what="W = 32")
     _check(w32.world, g32.views, 1.0, True, what="W = 32, accumulate")
+
+
+@pytest.mark.parametrize("index", [3, 5])
+def test_noalloc_full_size_matches_plan_fold(index):
+    """The full-size Llama-3.1-70B block (accumulate) and MoE layer (389
+    parameters x 32 ranks: ~1.9 MB of tables, the largest benchmark request):
+    every output element equal to the plan-based fold's, which the full-size
+    parity tests compare with the oracle."""
+    torch.cuda.set_device(0)
+    w = workloads.get(index)
+    g = workloads.make_grads(w, device="cuda")
+    with tide.Plan(g.views) as plan:
+        S = plan.slot_numel
+        init = workloads.make_out_init(w, S, device="cuda") if w.accumulate else None
+        ref = init.clone() if w.accumulate else torch.full((w.world, S), float("nan"), device="cuda")
+        plan.rs_fold(ref, alpha=w.alpha, accumulate=w.accumulate)
+    got = init.clone() if w.accumulate else torch.full((w.world, S), float("nan"), device="cuda")
+    _noalloc(w.world, g.views, got, S, w.alpha, w.accumulate)
+    torch.cuda.synchronize()
+    assert tide.tide_last_device_status(0, _stream()) == tide.TIDE_OK
+    assert torch.equal(got.view(torch.int32), ref.view(torch.int32)), f"{w.name}: allocation-free fold differs"
+    del g, got, ref, init
+    torch.cuda.empty_cache()
 
 
 def test_noalloc_allocates_nothing_after_set_up():
