@@ -1,8 +1,12 @@
 """Parity of the CUDA path (through the C ABI) with the CPU oracle.
 
 Reduce-scatter fold: bit-exact (rank-ascending fp32 order is the contract).
-All-gather placement: bit-exact.  Small cases compare every element; the
-full-size workloads compare sampled windows, each recomputed by the oracle.
+All-gather placement: bit-exact.  Small cases compare every element.  At full
+size: every element of the other orders and fp32 gradients here
+(test_full_size_orders_and_fp32) and of the default fold in
+test_full_size_parity.py; the second epilogue of each workload, a parameter of
+2^31 + 1,024 elements and launch-shape determinism on sampled windows or
+bitwise across launches; every element of every placement mode.
 """
 import random
 
