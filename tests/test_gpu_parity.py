@@ -2,11 +2,10 @@
 
 Reduce-scatter fold: bit-exact (rank-ascending fp32 order is the contract).
 All-gather placement: bit-exact.  Small cases compare every element.  At full
-size: every element of the other orders and fp32 gradients here
-(test_full_size_orders_and_fp32) and of the default fold in
-test_full_size_parity.py; the second epilogue of each workload, a parameter of
-2^31 + 1,024 elements and launch-shape determinism on sampled windows or
-bitwise across launches; every element of every placement mode.
+size: every element of both epilogues of each workload, of the other orders
+and of fp32 gradients, and of every placement mode; a parameter of
+2^31 + 1,024 elements on sampled windows; launch-shape determinism bitwise
+across launches.
 """
 import random
 
@@ -748,7 +747,11 @@ def test_graph_captured_copy_engine_placement(mode, index):
 # ---------------------------------------------------------------------------
 # full-size workloads in the benchmark's launch configuration
 @pytest.mark.parametrize("index", [2, 3, 4, 5])
-def test_full_size_sampled(index):
+def test_full_size_epilogues_and_placements(index):
+    """Full-size workloads: the fold with the benchmark's epilogue and with the
+    other one (alpha = 1/W, accumulate flipped), every output element against
+    the oracle; every placement mode and the mixed-precision placement, every
+    element."""
     w = workloads.get(index)
     dims = w.dim0_rownumel()
     gs = workloads.make_grads(w, device="cuda")
@@ -760,9 +763,9 @@ def test_full_size_sampled(index):
             before = out.clone() if acc else None
             plan.rs_fold(out, alpha=alpha, accumulate=acc)
             torch.cuda.synchronize()
-            n = sampled_rs_check(w.world, dims, gs.views, before, out, alpha, acc, seed=index,
-                                 what=f"{w.name} alpha={alpha} acc={acc}")
-            assert n > 0
+            n = full_rs_check(w.world, dims, gs.views, before, out, alpha, acc,
+                              what=f"{w.name} alpha={alpha} acc={acc}")
+            assert n == w.world * S
             del out, before
         # all-gather placement of full-size slots, every element
         slots = workloads.make_slots(w, S, device="cuda")
