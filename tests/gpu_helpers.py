@@ -1,17 +1,16 @@
-"""Helpers for the GPU parity tests: host copies, oracle runs, sampled and
-every-element full-size checks."""
+"""Helpers for the GPU parity tests: host copies, oracle runs and the
+every-element full-size check."""
 from __future__ import annotations
 
 import os
-import random
 from concurrent.futures import ThreadPoolExecutor
-from typing import List, Sequence, Tuple
+from typing import List, Sequence
 
 import numpy as np
 import torch
 
 import oracle
-from bits import assert_same_f32, assert_same_u16
+from bits import assert_same_f32
 
 
 def bits16(t: torch.Tensor) -> np.ndarray:
@@ -26,50 +25,6 @@ def oracle_rs_full(world: int, dims, grads_uv: Sequence[Sequence[torch.Tensor]],
     want = out_before.detach().cpu().numpy().astype(np.float32, copy=True)
     oracle.rs(world, dims, host, alpha, accumulate, want)
     return want
-
-
-def row_windows(R: int, v: int, rnd: random.Random, span: int = 3) -> List[Tuple[int, int]]:
-    """Row windows of one piece: its first rows, its last rows (padding if any),
-    the boundary between real and padding rows, and one random window."""
-    if R == 0:
-        return []
-    wins = {(0, min(span, R)), (max(0, R - span), R)}
-    if 0 < v < R:
-        wins.add((max(0, v - 1), min(R, v + 1)))
-    a = rnd.randrange(R)
-    wins.add((a, min(R, a + span)))
-    return sorted(wins)
-
-
-def sampled_rs_check(world: int, dims, grads_uv, out_before: torch.Tensor, out_after: torch.Tensor, alpha: float,
-                     accumulate: bool, seed: int = 0, ranks_per_param: int = 3, what: str = "",
-                     order: str = "rank", node_size: int = 0) -> int:
-    """Compare sampled windows of a full-size fold with the oracle, window by
-    window (oracle.rs_window).  Returns the number of elements compared."""
-    rnd = random.Random(seed)
-    R, o, S = oracle.geometry(world, dims)
-    checked = 0
-    for p, (d, k) in enumerate(dims):
-        ranks = sorted({0, world - 1, rnd.randrange(world)} if ranks_per_param >= 3 else {rnd.randrange(world)})
-        for r in ranks:
-            v = oracle.valid_rows(d, R[p], r)
-            for (i0, i1) in row_windows(R[p], v, rnd):
-                lo, hi = i0 * k, i1 * k
-                nv = max(0, min(hi, v * k) - lo)
-                base = r * R[p] * k + lo
-                pieces = [grads_uv[u][p].reshape(-1)[base:base + nv] for u in range(world)]
-                old = out_before[r, o[p] + lo:o[p] + hi].cpu().numpy() if accumulate else None
-                if pieces[0].dtype == torch.float32 or order != "rank":
-                    srcs = [x.cpu().numpy() if x.dtype == torch.float32 else bits16(x) for x in pieces]
-                    want = oracle.load().rs_window_ex(srcs, nv, (hi - lo) - nv, alpha, accumulate, r, order,
-                                                      node_size, old)
-                else:
-                    srcs = [bits16(x) for x in pieces]
-                    want = oracle.rs_window(srcs, nv, (hi - lo) - nv, alpha, accumulate, old)
-                got = out_after[r, o[p] + lo:o[p] + hi].cpu().numpy()
-                assert_same_f32(got, want, f"{what} p={p} r={r} rows [{i0},{i1})")
-                checked += hi - lo
-    return checked
 
 
 def full_rs_check(world: int, dims, grads_uv, out_before, out_after: torch.Tensor, alpha: float,

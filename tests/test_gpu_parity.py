@@ -17,7 +17,7 @@ import all_gather_gb300 as tide
 import oracle
 import workloads
 from bits import assert_same_bf16, assert_same_f32, assert_same_u16, bf16_bits_to_f32, f32_to_bf16_bits
-from gpu_helpers import (ag_expected, bits16, full_rs_check, oracle_rs_full, sampled_rs_check, sentinel_slots)
+from gpu_helpers import ag_expected, bits16, full_rs_check, oracle_rs_full, sentinel_slots
 
 U = 2.0 ** -24  # half an ulp of 1.0 in binary32
 
@@ -880,8 +880,9 @@ def test_parameter_beyond_2g_elements():
     """One parameter of 2,097,153 x 1,024 = 2^31 + 1,024 elements on 2 ranks
     (about 26 GB with outputs): rank 1's rows start at element 1,073,742,848 and
     end past 2^31, so every offset of the fold and the placements must be 64-bit.
-    Sampled windows (piece starts, ends, random rows) against the oracle, both
-    kernels and the tree order; the placements on sampled rows, every mode."""
+    Every output element against the oracle, both kernels and the tree order;
+    every element of the placements, every mode (compared on the device with
+    Equation (2)'s two row ranges: rank r's shard is rows [r R, r R + v_r))."""
     world, shape = 2, (2_097_153, 1024)
     w = workloads.custom(world, [shape, (5, 3)], index=77)
     dims = w.dim0_rownumel()
@@ -895,9 +896,8 @@ def test_parameter_beyond_2g_elements():
             plan.rs_fold(out, alpha=0.5)
             torch.cuda.synchronize()
             assert plan.device_status() == tide.TIDE_OK
-        n = sampled_rs_check(world, dims, gs.views, None, out, 0.5, False, seed=5, what=f"2G+ {kw}",
-                             order=oname)
-        assert n > 0
+        n = full_rs_check(world, dims, gs.views, None, out, 0.5, False, what=f"2G+ {kw}", order=oname)
+        assert n == world * S
     del out
     torch.cuda.empty_cache()
     slots = workloads.make_slots(w, S, device="cuda")
@@ -909,14 +909,13 @@ def test_parameter_beyond_2g_elements():
                 f.fill_(float("nan"))
             plan.ag_place(slots, bound, mode=mode)
             torch.cuda.synchronize()
-            rnd = random.Random(9)
-            d, k = dims[0]
-            rows = [0, R[0] - 1, R[0], d - 1] + rnd.sample(range(d), 12)
-            for row in rows:
-                r, i = divmod(row, R[0])
-                got = full[0].reshape(-1)[row * k:(row + 1) * k]
-                ref = slots[r, o[0] + i * k:o[0] + (i + 1) * k]
-                assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), (mode, row)
+            for p, (d, k) in enumerate(dims):
+                flat = full[p].reshape(-1).view(torch.int16)
+                for r in range(world):
+                    v = oracle.valid_rows(d, R[p], r) * k
+                    got = flat[r * R[p] * k:r * R[p] * k + v]
+                    ref = slots[r, o[p]:o[p] + v].view(torch.int16)
+                    assert torch.equal(got, ref), (mode, p, r)
     del gs, full, slots
     torch.cuda.empty_cache()
 
