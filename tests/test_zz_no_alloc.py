@@ -13,7 +13,7 @@ by the library.  These tests call it through the C ABI and check:
 * a group whose ranks' rows differ in 16-byte phase (the fold's scalar path)
   and a 32-rank group (several shared-memory stage fills per chunk);
 * the full-size Llama-3.1-70B block and MoE layer, element for element equal
-  to the plan-based fold;
+  to the plan-based fold, and 60 seeded random ragged groups against the oracle;
 * that after a warm-up call, further calls leave the device's free memory and
   torch's allocation count unchanged, and that the entry point's device
   status word reads TIDE_OK through tide_last_device_status(NULL, stream);
@@ -131,6 +131,38 @@ def test_noalloc_full_size_matches_plan_fold(index):
     assert torch.equal(got.view(torch.int32), ref.view(torch.int32)), f"{w.name}: allocation-free fold differs"
     del g, got, ref, init
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_noalloc_random_groups(seed):
+    """Seeded random groups (1..40 ranks, ragged and zero-size parameters,
+    trailing ranks without rows, random scale and accumulate) through the
+    allocation-free fold, bit-exact against the oracle."""
+    import random
+    torch.cuda.set_device(0)
+    rnd = random.Random(5000 + seed)
+    world = rnd.choice([1, 2, 3, 5, 8, 13, 16, 32, 40])
+    shapes = []
+    for _ in range(rnd.randint(1, 6)):
+        d = rnd.choice([0, 1, world - 1 or 1, world, world + 1, rnd.randint(1, 9 * world + 5)])
+        shapes.append((d,) if rnd.random() < 0.2 else (d, rnd.choice([1, 2, 3, 8, 17, 64, 130])))
+    w = workloads.custom(world, shapes, index=600 + seed)
+    g = workloads.make_grads(w, device="cuda")
+    dims = w.dim0_rownumel()
+    R = [-(-d // world) for d, _ in dims]
+    S = sum(r * k for r, (_, k) in zip(R, dims))
+    stride = S + rnd.choice([0, 1, 7])
+    alpha = rnd.choice([1.0, 0.5, -0.25, 1.0 / world])
+    acc = rnd.random() < 0.4
+    init = torch.randn(world, max(stride, 1), device="cuda") if acc else torch.zeros(world, max(stride, 1),
+                                                                                      device="cuda")
+    got = init.clone()
+    _noalloc(world, g.views, got, stride, alpha, acc)
+    torch.cuda.synchronize()
+    assert tide.tide_last_device_status(0, _stream()) == tide.TIDE_OK
+    want = oracle_rs_full(world, dims, g.views, alpha, acc, init)
+    assert_same_f32(got[:, :S].cpu().numpy(), want[:, :S], f"seed {seed}: W={world} {shapes} acc={acc}")
+    assert torch.equal(got[:, S:stride], init[:, S:stride])
 
 
 def test_noalloc_allocates_nothing_after_set_up():
