@@ -124,3 +124,32 @@ def test_host_gradients_refusals():
         torch.cuda.synchronize()
         want = oracle_rs_full(w.world, w.dim0_rownumel(), gs.views, 1.0, False, torch.zeros_like(out))
         assert_same_f32(out.cpu().numpy(), want, "after a refused rebind")
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_host_gradients_random_groups(seed):
+    """Seeded random ragged groups (1..40 ranks, zero-size parameters, random
+    16-byte phases per rank, scale and accumulate) folded from page-locked
+    host memory, bit-exact against the oracle."""
+    import random
+    rnd = random.Random(7000 + seed)
+    world = rnd.choice([1, 2, 3, 5, 8, 16, 32, 40])
+    shapes = []
+    for _ in range(rnd.randint(1, 5)):
+        d = rnd.choice([0, 1, world, world + 1, rnd.randint(1, 9 * world + 5)])
+        shapes.append((d,) if rnd.random() < 0.2 else (d, rnd.choice([1, 3, 8, 64, 130])))
+    w = workloads.custom(world, shapes, index=700 + seed)
+    gs = workloads.make_grads(w, device="cuda")
+    host = _pinned(gs.views, shift=rnd.random() < 0.5)
+    dims = w.dim0_rownumel()
+    _, _, S = oracle.geometry(world, dims)
+    alpha = rnd.choice([1.0, 0.5, 1.0 / world])
+    acc = rnd.random() < 0.4
+    init = torch.randn(world, S + 2, device="cuda") if acc else torch.zeros(world, S + 2, device="cuda")
+    out = init.clone()
+    with tide.Plan(host) as plan:
+        plan.rs_fold(out, alpha=alpha, accumulate=acc)
+        torch.cuda.synchronize()
+        assert plan.device_status() == tide.TIDE_OK
+    want = oracle_rs_full(world, dims, gs.views, alpha, acc, init)
+    assert_same_f32(out.cpu().numpy()[:, :S], want[:, :S], f"seed {seed}: W={world} {shapes}")
