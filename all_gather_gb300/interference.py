@@ -23,7 +23,7 @@ import json
 import os
 import statistics
 import sys
-from typing import Callable, Dict, List
+from typing import Callable, Dict
 
 os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
 

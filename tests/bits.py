@@ -2,9 +2,8 @@
 with NaN-class matching, and the golden-fixture parser."""
 from __future__ import annotations
 
-import math
 import os
-from typing import Dict, List, Tuple
+from typing import Dict
 
 import numpy as np
 import torch

@@ -22,9 +22,7 @@ What pins what:
 """
 from __future__ import annotations
 
-import math
 import random
-from typing import List, Sequence, Tuple
 
 import numpy as np
 import torch

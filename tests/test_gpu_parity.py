@@ -16,7 +16,7 @@ import torch
 import all_gather_gb300 as tide
 import oracle
 import workloads
-from bits import assert_same_bf16, assert_same_f32, assert_same_u16, bf16_bits_to_f32, f32_to_bf16_bits
+from bits import assert_same_bf16, assert_same_f32, assert_same_u16, bf16_bits_to_f32
 from gpu_helpers import ag_expected, bits16, full_rs_check, oracle_rs_full, sentinel_slots
 
 U = 2.0 ** -24  # half an ulp of 1.0 in binary32
