@@ -923,12 +923,19 @@ def test_parameter_beyond_2g_elements():
 @pytest.mark.parametrize("index", [2, 5])
 def test_full_size_orders_and_fp32(index):
     """Full-size groups: the Section 4.3 orders, the tree order and fp32
-    gradients, every output element recomputed by the oracle in the same order."""
+    gradients, every output element recomputed by the oracle in the same order,
+    and each order within 1e-6 of the rank-order fold in the max-norm over
+    every parameter tensor (the reordered-variant tolerance)."""
     w = workloads.get(index)
     dims = w.dim0_rownumel()
     gs = workloads.make_grads(w, device="cuda")
     _, _, S = oracle.geometry(w.world, dims)
     L = w.world // 2
+    R, o, _ = oracle.geometry(w.world, dims)
+    rank_out = torch.empty(w.world, S, device="cuda")
+    with tide.Plan(gs.views) as plan:
+        plan.rs_fold(rank_out, alpha=w.alpha)
+        torch.cuda.synchronize()
     for order, oname, ns in ((tide.TIDE_ORDER_STAGED_OWN, "staged", 0), (tide.TIDE_ORDER_NODES, "nodes", L),
                              (tide.TIDE_ORDER_TREE, "tree", 0)):
         out = torch.full((w.world, S), float("nan"), device="cuda")
@@ -939,7 +946,13 @@ def test_full_size_orders_and_fp32(index):
         n = full_rs_check(w.world, dims, gs.views, None, out, w.alpha, False, what=f"{w.name} {oname}",
                           order=oname, node_size=ns)
         assert n == w.world * S
+        # the reordered-variant tolerance against rank order, max-norm over each parameter tensor
+        for p, (d, k) in enumerate(dims):
+            a = out[:, o[p]:o[p] + R[p] * k].double()
+            b = rank_out[:, o[p]:o[p] + R[p] * k].double()
+            assert float((a - b).abs().max()) <= 1e-6 * float(b.abs().max()), f"{w.name} {oname} p={p}"
         del out
+    del rank_out
     # fp32 gradients (the bf16 values plus a small fp32 perturbation), accumulate mode
     views32 = [[v.float() + 1e-6 * torch.randn(v.shape, device="cuda") for v in vs] for vs in gs.views]
     del gs
