@@ -98,3 +98,24 @@ def test_host_memory_probe():
     import bench
     avail = bench.host_mem_available()
     assert avail > 0 and avail % 1024 == 0
+
+
+def test_reference_arm_under_torchrun_prints_one_line():
+    """Launched as the multi-GPU bench is (torchrun, 2 ranks, 127.0.0.1), the
+    reference arm runs on rank 0 only and prints exactly one JSON line; the
+    other rank exits 0 without work."""
+    import json
+    import socket
+    import subprocess
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr",
+           "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"), "--impl", "reference",
+           "--workload", "toy", "--gpus", "2", "--steps", "1", "--warmup", "0"]
+    res = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
