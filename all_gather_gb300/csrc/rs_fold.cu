@@ -18,8 +18,11 @@
 //   fold_bulk_kernel (default): one producer lane per CTA stages the rank rows
 //     in a shared-memory ring with bulk asynchronous copies (the TMA engine),
 //     four consumer warps add them in fp32 registers and store the shard;
+//     the producer claims work items from a device counter and posts them to
+//     the consumers (dynamic schedule), or takes every gridDim-th item;
 //   fold_direct_kernel: every thread loads 16-byte vectors of the rank rows
-//     straight into registers (static or dynamic item scheduling).
+//     straight into registers (static or dynamic item scheduling); the kernel
+//     for gradients in page-locked host memory.
 #include <cuda_runtime.h>
 
 #include "tide_internal.h"
@@ -297,10 +300,12 @@ FoldKernel pick_direct(int world)
 }
 
 // ---------------------------------------------------------------------------
-// Bulk-copy kernel.  Warp 0 is the producer: one elected lane streams each
-// work item's W rank rows into a ring of shared-memory stages with
-// cp.async.bulk (the TMA engine's non-tensor copy), one copy per rank per
-// fill, completing on the stage's "full" mbarrier with a transaction count.
+// Bulk-copy kernel.  Warp 0 is the producer: one elected lane takes the work
+// items (under the dynamic schedule it claims each from the device counter
+// and posts its index through the item queue) and streams each item's W rank
+// rows into a ring of shared-memory stages with cp.async.bulk (the TMA
+// engine's non-tensor copy), one copy per rank per fill, completing on the
+// stage's "full" mbarrier with a transaction count.
 // Warps 1..4 consume a stage (fp32 adds in rank order from shared memory,
 // scale, optional accumulate, 16-byte streaming stores) and release it on
 // its "empty" mbarrier.  Every wait is bounded by %globaltimer: on expiry
