@@ -214,9 +214,11 @@ typedef struct {
  * Build a plan for one parameter group of `num_params` parameters sharded over
  * `world` virtual ranks (1 <= world <= 1024).  Computes R_p, o_p, S and the
  * P*W shard pieces (Section 2.1), splits them into work items, validates
- * every descriptor, allocates the plan's device tables and uploads them with
- * asynchronous copies on `stream`.  `params` is a host array; `flags` may be
- * NULL for defaults.  On success *plan_out owns the tables.
+ * every descriptor, queries the memory kind of every gradient pointer
+ * (cudaPointerGetAttributes, about 1 us each), allocates the plan's device
+ * tables and uploads them with asynchronous copies on `stream`.  `params` is
+ * a host array; `flags` may be NULL for defaults.  On success *plan_out owns
+ * the tables.
  * Errors: INVALID_ARG (world, counts, dims, null pointers, overlapping
  * explicit offsets, nonzero reserved fields, node_size not dividing world,
  * a gradient in pageable host memory or in another device's memory),
@@ -233,8 +235,9 @@ TIDE_API tide_status_t tide_plan_build(int32_t world, int32_t num_params, const 
  * Point an existing plan at new gradient storage with the same geometry (for
  * example, the next step's gradients).  dim0, row_numel and shard_offset must
  * equal the plan's, and the gradients must stay in the same kind of memory
- * (device or host) as at build.  The new pointer table is uploaded on
- * `stream`, ordered after earlier work on that stream.
+ * (device or host) as at build; only pointers that changed are queried
+ * again.  The new pointer table is uploaded on `stream`, ordered after
+ * earlier work on that stream.
  */
 TIDE_API tide_status_t tide_plan_rebind(tide_plan_t *plan, const tide_param_desc_t *params, void *stream);
 
@@ -328,7 +331,10 @@ TIDE_API uint64_t tide_launch_count(void);
  *   Arguments: as tide_plan_build's (world, num_params, params) followed by
  *   tide_rs_fold's (out_base, out_slot_stride, alpha, accumulate, stream);
  *   S is computed from params the same way; explicit shard offsets must be
- *   given in increasing order (each at least the previous shard's end).
+ *   given in increasing order (each at least the previous shard's end).  The
+ *   gradients must be device (or managed) memory of the current device: this
+ *   entry point does not query pointer kinds and always runs the bulk-copy
+ *   kernel, so gradients in host memory take tide_plan_build.
  *   Limit: the call's tables (8 bytes per gradient pointer, 48 per
  *   (parameter, rank) piece, 16 per work item of 8,192 elements, plus
  *   alignment) must fit in TIDE_NOALLOC_SCRATCH_BYTES; larger requests return
